@@ -1,0 +1,344 @@
+#!/usr/bin/env python3
+"""Benchmark of the ForkAttention token-mixing layer on one round.
+
+A step is one pass of the whole layer over one synthetic round: metadata
+build, full attention, sliding-window attention, GDN trunk call, GDN branch
+call, options readout.  The default workload is the long-document round (4
+requests, trunks of 4096-6144 tokens, 8-20 questions of 32-64 tokens each;
+attention 32 q-heads / 8 kv-heads, d=128, RoPE; SWA W=1024; GDN 32 heads,
+d=128, chunk 64; T_cap 32768).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_ID = 3
+METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.rows = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1]
+        note = "timed region"
+        if not rows:
+            rows = [r for (_, r) in self.rows]
+            note = "around the timed region (region shorter than the sampling period)"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "note": note}
+
+
+def _gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def oracle_sample(rnd, trunk_cap=None, n_questions=1):
+    """Time the CPU oracle on request 0 (trunk, optionally cut to trunk_cap
+    tokens, plus its first n_questions questions).  Returns (tokens, seconds)."""
+    from oracle import forkattn as orc
+    from tree_forked_hybrid_gb300 import workloads as wl
+    P0 = int(rnd.trunk_len[0])
+    P = P0 if trunk_cap is None else min(P0, trunk_cap)
+    nq = min(n_questions, int(rnd.n_q[0]))
+    ql = rnd.q_len[:nq]
+    # the sample as a round of its own: trunk rows [0, P) and the chosen questions' rows
+    m = orc.meta_ref(rnd.desc(), rnd.R, rnd.Nq, rnd.T_cap, 32)
+    rows = list(range(0, P))
+    for i in range(nq):
+        st, L = int(m["seg_start"][rnd.R + i]), int(m["seg_len"][rnd.R + i])
+        rows.extend(range(st, st + L))
+    rows = np.array(rows)
+    desc = np.concatenate([[P], [nq], ql, [0], [-1]]).astype(np.int32)
+    T_s = int(P + ql.sum())
+    lay = {}
+    for name, d in rnd.layers.items():
+        lay[name] = {k: (wl.bf16_to_f32(v[rows]) if v.dtype == np.uint16 else
+                         (v[rows] if k != "conv_w" else v)) for k, v in d.items()}
+    view = orc.RoundView(desc, 1, nq, T_s, lay)
+    t0 = time.perf_counter()
+    for a in rnd.attn_shapes:
+        orc.run_attention(view, a.name, window=a.window, rope_theta=a.rope_theta)
+    g = orc.run_gdn(view, rnd.gdn_shape.name)
+    off = np.concatenate([[0], np.cumsum(rnd.n_opt[:nq])]).astype(np.int32)
+    orc.run_readout(view, g["o"].reshape(T_s, -1), rnd.w_opt_f32()[:off[-1]], off)
+    return T_s, time.perf_counter() - t0
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from tree_forked_hybrid_gb300 import workloads as wl
+    rnd = wl.make_round(WORKLOAD_ID)
+    cores = len(os.sched_getaffinity(0))
+    cap = 512
+    for _ in range(args.warmup):
+        oracle_sample(rnd, cap)
+    tok = 0
+    t = 0.0
+    for _ in range(args.steps):
+        n, dt = oracle_sample(rnd, cap)
+        tok += n
+        t += dt
+    value = tok / t
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "impl": "reference",
+           "config": _config(rnd),
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": f"per step: request 0 of the round, trunk cut to its first {cap} tokens, "
+                                      f"plus its first question, run through the oracle (numpy fp32)"},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def _config(rnd):
+    return {"workload": "long-document round: R=4, P~U[4096,6144], n~U{8..20}, |q|~U[32,64]; "
+                        "attn 32q/8kv d=128 RoPE; SWA W=1024; GDN 32 heads d=128 chunk 64; readout D=4096",
+            "T": rnd.T, "T_cap": rnd.T_cap, "R": rnd.R, "Nq": rnd.Nq,
+            "l2": "inputs larger than L2 (about 1.2 GB of layer inputs per step)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    ws, rank, local = _dist()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from tree_forked_hybrid_gb300 import build as B
+    B.build()
+    from tree_forked_hybrid_gb300 import workloads as wl
+    from tree_forked_hybrid_gb300 import roofline as RL
+    from tree_forked_hybrid_gb300.runner import DeviceRound
+
+    # every rank runs its own round (requests shard across GPUs with no exchange)
+    rnd = wl.make_round(WORKLOAD_ID, seed=WORKLOAD_ID + 1000 * rank)
+    dr = DeviceRound(rnd, device=f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    calls = [("meta", dr.step_meta)] + [(f"attn_{a.name}", (lambda n=a.name: dr.step_attn(n)))
+                                        for a in rnd.attn_shapes]
+    calls += [("gdn_trunk", dr.step_gdn_trunk), ("gdn_branches", dr.step_gdn_branches),
+              ("readout", dr.step_readout)]
+    for _ in range(max(args.warmup, 3)):
+        dr.run()
+    torch.cuda.synchronize()
+    if dr.status() != 0:
+        raise RuntimeError(f"device status {dr.status():#x}")
+    if dist:
+        dist.barrier()
+    sampler = ClockSampler(_gpu_uuid(torch, local))
+    time.sleep(0.3)
+    ev = {name: [] for name, _ in calls}
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        for name, fn in calls:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ev[name].append((e0, e1))
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    per_call = {name: statistics.mean(a.elapsed_time(b) for a, b in lst) for name, lst in ev.items()}
+    tokens_all = rnd.T * ws
+    value = tokens_all * args.steps / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / args.steps
+
+    peaks = _peaks()
+    work = RL.round_work(rnd)
+    t_roof = RL.roofline_time(work, peaks["bf16_tflops"], peaks["hbm_gbs"])
+    # dominant call and its roofline
+    top = max(per_call, key=per_call.get)
+    if top.startswith("attn_"):
+        f = work["attn"][top[5:]]["flops"]
+        ach = f / (per_call[top] / 1e3) / 1e12
+        roof = {"kernel": f"fork_attn ({top[5:]}): rotary tables + key rotation + attention",
+                "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"], "traffic": None,
+                "peak_note": f"bf16 dense sustained ({peaks['source']}); kernel timed inside a long step"}
+    else:
+        key = "gdn" if top.startswith("gdn") else "readout"
+        b = work[key]["bytes"] if key != "gdn" else work["gdn"]["bytes"]
+        ach = b / (per_call[top] / 1e3) / 1e9
+        roof = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": None, "peak_note": f"HBM copy ({peaks['source']})"}
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(rnd),
+           "roofline": roof,
+           "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_meas_us": ms_per_step * 1e3,
+                              "frac": t_roof / (ms_per_step / 1e3), "flops": work["flops"],
+                              "bytes": work["bytes"],
+                              "peaks": f"{peaks['bf16_tflops']} TFLOP/s bf16, {peaks['hbm_gbs']} GB/s "
+                                       f"({peaks['source']})"},
+           "per_call_us": {k: v * 1e3 for k, v in per_call.items()},
+           "gpu_launches": dr.launches_per_round() * args.steps,
+           "clocks": sampler.summary(w0, w1)}
+
+    if not args.no_e2e:
+        out["e2e"] = e2e(torch, dr, rnd, args, stream, dist, local, ws)
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        n, dt = oracle_sample(rnd, None, 1)
+        out["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                               "kind": "oracle",
+                               "sample": f"request 0 of the round (trunk of {int(rnd.trunk_len[0])} tokens) with "
+                                         f"its first question, {n} stream tokens, {dt:.1f} s, numpy fp32"}
+    if rank == 0:
+        print(json.dumps(out))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def e2e(torch, dr, rnd, args, stream, dist, local, ws):
+    """Same metric through the public API with host buffers: every step copies
+    the round's inputs from pinned host memory, runs the layer and reads the
+    option probabilities back."""
+    T = rnd.T
+    host = []
+    h2d = 0
+    for name, lay in dr.inputs.items():
+        for k, t in lay.items():
+            rows = t if k == "conv_w" else t[:T]
+            hp = torch.empty(rows.shape, dtype=rows.dtype, pin_memory=True)
+            hp.copy_(rows.cpu())
+            host.append((hp, rows))
+            h2d += hp.numel() * hp.element_size()
+    for src in (dr.desc, dr.w_opt, dr.opt_off):
+        hp = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
+        hp.copy_(src.cpu())
+        host.append((hp, src))
+        h2d += hp.numel() * hp.element_size()
+    p_host = torch.empty(dr.p.shape, dtype=dr.p.dtype, pin_memory=True)
+    d2h = p_host.numel() * p_host.element_size()
+
+    def step():
+        for hp, dev in host:
+            dev.copy_(hp, non_blocking=True)
+        dr.run()
+        p_host.copy_(dr.p, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": T * ws * args.steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * forkattn.h - C ABI of the GB300 ForkAttention token-mixing layer.
+ *
+ * The layer is the data-parallel hot path of Flide ("Flide: Accelerating
+ * Decision Inference with Exact State Forking"): a round of R requests
+ * r = (s, q_1..q_n) is packed into one unpadded flat token stream, every
+ * token carries device-resident metadata (request j, branch c, position t),
+ * and the token mixers (fork-masked attention, two-call Gated DeltaNet) plus
+ * the options readout run over that stream.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers named d_* or described as "device" are CUDA device
+ *     pointers; the caller allocates and owns every buffer (metadata,
+ *     workspace, inputs, outputs).  The library allocates nothing and keeps
+ *     no global state between calls.
+ *   - bf16 tensors are passed as uint16_t bit patterns (bfloat16), row-major
+ *     with the layout stated per argument.  Every base pointer must be
+ *     16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous and stream-ordered; none synchronises the host except
+ *     fork_read_status, so a sequence of calls can be captured in a CUDA
+ *     graph.  Grid sizes depend only on the capacities fixed at metadata
+ *     build time (T_cap, max_req, max_q) and on the shape arguments.
+ *   - Return value: FORK_OK or a host-detected error code (nothing is
+ *     launched then).  Errors found on the device (an inconsistent
+ *     descriptor) set bits of the status word inside the metadata and turn
+ *     every later kernel of the round into a no-op; fork_read_status reads it.
+ *     No kernel traps, asserts or waits without a bound.
+ *   - Requires an sm_103 device (FORK_EUNSUPPORTED otherwise).
+ */
+#ifndef FORKATTN_H
+#define FORKATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes (host) */
+#define FORK_OK 0
+#define FORK_EINVAL 1       /* null pointer, bad shape or size, misaligned buffer */
+#define FORK_ECAPACITY 2    /* round larger than the metadata capacities */
+#define FORK_EUNSUPPORTED 3 /* device is not sm_103 */
+#define FORK_ECUDA 4        /* a CUDA runtime/driver call or launch failed */
+
+/* Device status word bits (fork_read_status) */
+#define FORK_STATUS_BAD_DESC 0x1   /* descriptor lengths inconsistent (negative, q_len < 1, ...) */
+#define FORK_STATUS_CAPACITY 0x2   /* descriptor's stream longer than T_cap */
+#define FORK_STATUS_BAD_CKPT 0x4   /* checkpoint position outside [prefix_len, P] */
+#define FORK_STATUS_TIMEOUT 0x8    /* a bounded wait inside a kernel gave up */
+#define FORK_STATUS_BAD_PREFIX 0x10 /* a request's prefix rows lie outside the prefix buffers or
+                                       the resume state/window buffers are missing */
+
+/* Flags */
+#define FORK_DETERMINISTIC 0x1u /* bitwise identical results for a question under any round
+                                   composition.  Every kernel here already computes each output
+                                   from segment-aligned tiles and chunks in a fixed order, so the
+                                   flag is accepted and changes nothing. */
+#define FORK_CHECKS 0x2u        /* extra device-side consistency checks (status word) */
+
+/* ------------------------------------------------------------------------
+ * Metadata (Flide pages: onedev summary "무엇과 다른가" - per-token (j, c, t),
+ * question positions continue from P; rainbus summary "方法步骤详情" steps 1
+ * and 3 - stream order s(1)|s(2)|...|q1(1)|..., segment lengths, positions,
+ * key ranges and state indices written to device buffers; onedev "어떻게 쓰나").
+ * ------------------------------------------------------------------------ */
+
+/* Host-side handle of a metadata buffer.  Plain data, filled by
+ * fork_meta_init and passed by pointer to every later call; the library
+ * derives every launch shape from these capacities, never from the buffer
+ * contents (so nothing has to be read back before a launch). */
+typedef struct fork_meta {
+  void* d_buf;         /* device buffer of at least fork_meta_bytes(...) bytes */
+  size_t bytes;        /* its size */
+  int32_t T_cap;       /* stream capacity in tokens */
+  int32_t max_req;     /* most requests a round may hold */
+  int32_t max_q;       /* most questions a round may hold */
+  int32_t tile_tokens; /* attention query-tile length in tokens: 128 / (Hq / Hkv) */
+} fork_meta;
+
+/* Bytes of the metadata buffer for a stream capacity T_cap (tokens), at most
+ * max_req requests and max_q questions per round.  Returns 0 for invalid
+ * capacities (T_cap < 1 or > 1<<20, max_req < 1 or > 1<<16, max_q < 0 or
+ * > 1<<18). */
+size_t fork_meta_bytes(int32_t T_cap, int32_t max_req, int32_t max_q);
+
+/* Fill *m (host only, no CUDA call).  tile_tokens in {8,16,32,64,128}.
+ * Errors: FORK_EINVAL (null, invalid capacity, buffer too small or not
+ * 16-byte aligned). */
+int fork_meta_init(fork_meta* m, void* d_buf, size_t bytes, int32_t T_cap, int32_t max_req,
+                   int32_t max_q, int32_t tile_tokens);
+
+/* Build the round metadata on the device.
+ *   d_desc   device int32 [4R + Nq]: R trunk lengths P_j (prefix included) |
+ *            R question counts n_j | Nq question lengths (request order) |
+ *            R prefix lengths (trunk tokens held outside the stream, from a
+ *            checkpoint; 0 normally) | R checkpoint positions (-1 = none).
+ *   R, Nq    counts (host ints); Nq must equal sum n_j (checked on device).
+ * Produces: per-token request/branch/position (pad rows = -1); the segment
+ * table (R trunk segments, then the Nq question segments in stream order)
+ * with start, length, first position, request, branch, trunk start and
+ * length, state index; per-request tables; the last stream row of every
+ * question; the attention work list (segment, offset) of tile_tokens-token
+ * tiles aligned to each segment's start, each segment's last tile first;
+ * and the status word (cleared, then set if the descriptor is
+ * inconsistent, in which case the round is empty for every later kernel).
+ * Errors: FORK_EINVAL (null pointers, R < 0, Nq < 0), FORK_ECAPACITY
+ * (R > max_req, Nq > max_q). */
+int fork_build_meta(const fork_meta* m, const int32_t* d_desc, int32_t R, int32_t Nq,
+                    uint32_t flags, void* stream);
+
+/* Copy the device status word of a metadata buffer to *h_status.  Enqueues a
+ * device-to-host copy on `stream` and synchronises that stream. */
+int fork_read_status(const fork_meta* m, int32_t* h_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Fork-masked attention (rainbus "方法步骤详情" step 2: key y is visible to
+ * query x iff j_y = j_x, c_y in {0, c_x}, t_y <= t_x, and for a sliding
+ * window layer t_x - t_y < W; onedev "무엇과 다른가": questions receive the
+ * rotary positions they would have alone).
+ * ------------------------------------------------------------------------ */
+
+/* Workspace bytes fork_attn needs: rotated keys for the stream and the prefix
+ * rows (0 when rope_theta == 0). */
+size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hkv, int32_t d,
+                                 float rope_theta);
+
+/* o_x = sum_y softmax_y(<R(q_x,t_x), R(k_y,t_y)> * scale) v_y over visible y.
+ *   q [T_cap, Hq, d], k and v [T_cap, Hkv, d] bf16 (stream rows; pad rows
+ *   ignored); o [T_cap, Hq, d] bf16 (pad rows not written).  q-head h reads
+ *   kv-head h / (Hq / Hkv).  d in {64, 128}; Hq / Hkv * tile_tokens == 128.
+ *   window 0 = full attention, else W > 0.  rope_theta 0 = no rotary
+ *   embedding, else rotate-half pairs (i, i + d/2) by t * theta^(-2i/d).
+ *   scale: score scale (1/sqrt(d) in the workloads).
+ *   prefix_k/prefix_v [prefix_rows, Hkv, d] bf16, un-rotated: keys/values of
+ *   trunk positions 0..prefix_len_j-1 held outside the stream (incremental
+ *   resume), request j's rows starting at the sum of earlier prefix lengths;
+ *   NULL when no request has a prefix.
+ *   workspace: device buffer of fork_attn_workspace_bytes(...) bytes. */
+int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+              uint16_t* o, int32_t Hq, int32_t Hkv, int32_t d, int32_t window, float rope_theta,
+              float scale, const uint16_t* prefix_k, const uint16_t* prefix_v, int32_t prefix_rows,
+              void* workspace, size_t ws_bytes, uint32_t flags, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Gated DeltaNet, two calls (onedev "무엇과 다른가"; rainbus "前置知识" and
+ * "方法步骤详情" step 2: the first call processes every trunk segment and
+ * emits each request's float32 state S_P and conv window; the second call
+ * processes every question segment at once, each resuming from its own
+ * S_P by index, the causal conv reading the trunk's last tokens).
+ *
+ * Per head, after a depthwise causal conv of width K (tap K-1 multiplies
+ * the current token) and SiLU on the q, k, v channels and an L2
+ * normalisation of q and k (x * (sum x^2 + 1e-6)^(-1/2)):
+ *   S_t = alpha_t S_{t-1} (I - eta_t k_t k_t^T) + eta_t v_t k_t^T,  o_t = S_t q_t
+ * with S of shape d x d (rows index v, columns index k).
+ * Shared arguments:
+ *   q, k, v [T_cap, H, d] bf16; alpha, eta [T_cap, H] float32 (gates after
+ *   the sigmoid); conv_w [3 (q,k,v), H, d, K] float32; d = dk = dv in
+ *   {64, 128}; K = 4; chunk = 64 (chunks are aligned to each segment's
+ *   start); o [T_cap, H, d] bf16 (only the call's own segment rows written).
+ * ------------------------------------------------------------------------ */
+
+/* Call 1: every trunk segment.
+ *   init_state [R, H, d, d] float32 and init_conv [R, K-1, 3, H, d] bf16:
+ *   state and raw conv inputs at position prefix_len_j for requests with a
+ *   prefix (a checkpoint being resumed); NULL when no request has a prefix.
+ *   Outputs: S_P [R, H, d, d] float32 (state after the whole trunk);
+ *   conv_win [R, K-1, 3, H, d] bf16 (raw q,k,v inputs of trunk positions
+ *   P-K+1..P-1, zero before position 0); S_ckpt / conv_ckpt (same layouts,
+ *   may be NULL when no request has a checkpoint): state after positions
+ *   < m and raw inputs of positions m-K+1..m-1 for requests with ckpt_pos m.
+ */
+int fork_gdn_trunk(const fork_meta* m, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   const float* alpha, const float* eta, const float* conv_w, int32_t H, int32_t d,
+                   int32_t K, int32_t chunk, const float* init_state, const uint16_t* init_conv,
+                   float* S_P, uint16_t* conv_win, float* S_ckpt, uint16_t* conv_ckpt, uint16_t* o,
+                   uint32_t flags, void* stream);
+
+/* Call 2: every question segment; question i of request j starts from
+ * S_P[j] and conv_win[j] (read by index, never copied). */
+int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const float* alpha, const float* eta, const float* conv_w, int32_t H,
+                      int32_t d, int32_t K, int32_t chunk, const float* S_P,
+                      const uint16_t* conv_win, uint16_t* o, uint32_t flags, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Selective readout, eq. (1) (onedev "어떻게 동작하나"; rainbus "前置知识"):
+ * p_i(o) = exp(w_o . h_i) / sum_{o' in O_i} exp(w_o' . h_i), h_i the hidden
+ * row of question i's last token.
+ *   h [T_cap, D] bf16 (the GDN output, heads flattened); w_opt [sum O, D]
+ *   bf16; opt_off device int32 [Nq + 1] CSR offsets (opt_off[0] = 0, at
+ *   least one option per question); p [sum O] float32.  Logits and the
+ *   softmax are float32; D a multiple of 8, at most 16384.
+ * ------------------------------------------------------------------------ */
+int fork_readout(const fork_meta* m, const uint16_t* h, int32_t D, const uint16_t* w_opt,
+                 const int32_t* opt_off, float* p, uint32_t flags, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FORKATTN_H */

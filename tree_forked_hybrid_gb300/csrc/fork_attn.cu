@@ -1,0 +1,178 @@
+// fork_attn entry point: rotary tables, key rotation, then the attention kernel.
+//
+// Rotary embedding (onedev summary "무엇과 다른가": a question's positions
+// continue from P so it gets the rotary positions of its isolated prompt):
+// pair (i, i + d/2) of a head vector at position t is rotated by the angle
+// t * theta^(-2i/d).  Angles are formed in float64 on the device as
+// t = 64 a + b with two small tables of (cos, sin), combined in float32 by the
+// angle-addition formula.
+#include <algorithm>
+#include <cmath>
+
+#include "fork_attn.cuh"
+
+namespace fork {
+
+static int64_t rope_hi_rows(int64_t max_pos) { return (max_pos + 128 + 63) / 64; }
+
+__global__ void rope_tables_kernel(float2* hi, int hi_rows, float2* lo, int half, double theta) {
+  const int64_t n_hi = static_cast<int64_t>(hi_rows) * half;
+  const int64_t n = n_hi + 64 * half;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool is_hi = idx < n_hi;
+    const int64_t e = is_hi ? idx : idx - n_hi;
+    const int i = static_cast<int>(e % half);
+    const int64_t t = is_hi ? (e / half) * 64 : e / half;
+    const double f = pow(theta, -2.0 * i / (2.0 * half));
+    const double ang = static_cast<double>(t) * f;
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    const float2 v = make_float2(static_cast<float>(cs), static_cast<float>(sn));
+    if (is_hi) hi[e] = v; else lo[e] = v;
+  }
+}
+
+// Rotate every key row of the stream (position from the metadata) and of the
+// prefix (position = row index inside its request's prefix).
+template <int D>
+__global__ void rope_keys_kernel(const int32_t* __restrict__ meta, MetaLayout L,
+                                 const uint16_t* __restrict__ k, const uint16_t* __restrict__ pk,
+                                 uint16_t* __restrict__ kr, uint16_t* __restrict__ pkr,
+                                 int prefix_rows, int Hkv, const float2* __restrict__ hi,
+                                 const float2* __restrict__ lo, int hi_rows) {
+  if (meta[H_VALID] == 0) return;
+  const int T = meta[H_T];
+  const int R = meta[H_R];
+  constexpr int HALF = D / 2;
+  const int64_t rows = static_cast<int64_t>(T + prefix_rows) * Hkv;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       idx < rows * HALF; idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(idx % HALF);
+    const int64_t rh = idx / HALF;  // row * Hkv + head
+    const int64_t row = rh / Hkv;
+    const uint16_t* src;
+    uint16_t* dst;
+    int t;
+    if (row < T) {
+      t = meta[L.tok_pos + row];
+      src = k + rh * D;
+      dst = kr + rh * D;
+    } else {
+      const int pr = static_cast<int>(row - T);
+      // request owning prefix row pr: last j with prefix_off[j] <= pr
+      int a = 0, b = R;
+      while (b - a > 1) {
+        const int mid = (a + b) >> 1;
+        if (meta[L.req_prefix_off + mid] <= pr) a = mid; else b = mid;
+      }
+      t = pr - meta[L.req_prefix_off + a];
+      src = pk + (rh - static_cast<int64_t>(T) * Hkv) * D;
+      dst = pkr + (rh - static_cast<int64_t>(T) * Hkv) * D;
+    }
+    if (t < 0 || (t >> 6) >= hi_rows) {
+      // position beyond the rotary table: the prefix buffers given to fork_attn are
+      // shorter than the descriptor's prefix lengths
+      atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
+      continue;
+    }
+    float cs, sn;
+    rope_cs(hi, lo, HALF, t, i, &cs, &sn);
+    const float x0 = bf2f(src[i]), x1 = bf2f(src[i + HALF]);
+    dst[i] = f2bf(x0 * cs - x1 * sn);
+    dst[i + HALF] = f2bf(x1 * cs + x0 * sn);
+  }
+}
+
+struct AttnWs {
+  size_t kr, pkr, hi, lo, total;
+};
+
+static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hkv, int64_t d) {
+  AttnWs w;
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  w.kr = 0;
+  w.pkr = al(w.kr + static_cast<size_t>(T_cap) * Hkv * d * 2);
+  w.hi = al(w.pkr + static_cast<size_t>(prefix_rows) * Hkv * d * 2);
+  w.lo = al(w.hi + static_cast<size_t>(rope_hi_rows(T_cap + prefix_rows)) * (d / 2) * 8);
+  w.total = al(w.lo + static_cast<size_t>(64) * (d / 2) * 8);
+  return w;
+}
+
+}  // namespace fork
+
+using namespace fork;
+
+extern "C" size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hkv,
+                                            int32_t d, float rope_theta) {
+  if (T_cap < 1 || prefix_rows < 0 || Hkv < 1 || (d != 64 && d != 128)) return 0;
+  if (rope_theta == 0.f) return 0;
+  return attn_ws(T_cap, prefix_rows, Hkv, d).total;
+}
+
+extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k,
+                         const uint16_t* v, uint16_t* o, int32_t Hq, int32_t Hkv, int32_t d,
+                         int32_t window, float rope_theta, float scale, const uint16_t* prefix_k,
+                         const uint16_t* prefix_v, int32_t prefix_rows, void* workspace,
+                         size_t ws_bytes, uint32_t flags, void* stream) {
+  (void)flags;
+  MetaLayout L;
+  int rc = check_meta(m, &L);
+  if (rc != FORK_OK) return rc;
+  if (!q || !k || !v || !o) return FORK_EINVAL;
+  if (!is_aligned16(q) || !is_aligned16(k) || !is_aligned16(v) || !is_aligned16(o)) return FORK_EINVAL;
+  if (d != 64 && d != 128) return FORK_EINVAL;
+  if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0) return FORK_EINVAL;
+  const int G = Hq / Hkv;
+  if (G * m->tile_tokens != 128) return FORK_EINVAL;
+  if (window < 0 || prefix_rows < 0 || !(scale > 0.f) || !std::isfinite(scale)) return FORK_EINVAL;
+  if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return FORK_EINVAL;
+  if (prefix_rows > 0 && (!prefix_k || !prefix_v || !is_aligned16(prefix_k) || !is_aligned16(prefix_v)))
+    return FORK_EINVAL;
+  if ((rc = check_device()) != FORK_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  AttnParams p;
+  p.meta = static_cast<const int32_t*>(m->d_buf);
+  p.L = L;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.prefix_k = prefix_k;
+  p.prefix_v = prefix_v;
+  p.o = o;
+  p.rope_hi = nullptr;
+  p.rope_lo = nullptr;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.prefix_rows = prefix_k ? prefix_rows : 0;
+  p.window = window;
+  p.rope_theta = rope_theta;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  if (rope_theta != 0.f) {
+    const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hkv, d);
+    if (!workspace || ws_bytes < w.total || !is_aligned16(workspace)) return FORK_EINVAL;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    uint16_t* kr = reinterpret_cast<uint16_t*>(ws + w.kr);
+    uint16_t* pkr = reinterpret_cast<uint16_t*>(ws + w.pkr);
+    float2* hi = reinterpret_cast<float2*>(ws + w.hi);
+    float2* lo = reinterpret_cast<float2*>(ws + w.lo);
+    const int hi_rows = static_cast<int>(rope_hi_rows(static_cast<int64_t>(L.T_cap) + prefix_rows));
+    rope_tables_kernel<<<64, 256, 0, s>>>(hi, hi_rows, lo, d / 2, static_cast<double>(rope_theta));
+    const int blocks = 4 * 152;
+    if (d == 64)
+      rope_keys_kernel<64><<<blocks, 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows, Hkv, hi, lo, hi_rows);
+    else
+      rope_keys_kernel<128><<<blocks, 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows, Hkv, hi, lo, hi_rows);
+    p.k = kr;
+    p.prefix_k = pkr;
+    p.rope_hi = hi;
+    p.rope_lo = lo;
+  }
+  if (cudaGetLastError() != cudaSuccess) return FORK_ECUDA;
+  const int grid_x = static_cast<int>(std::min<int64_t>(
+      L.max_work, (L.T_cap + m->tile_tokens - 1) / m->tile_tokens + L.max_seg));
+  return d == 64 ? launch_attn_mma<64>(p, grid_x, s) : launch_attn_mma<128>(p, grid_x, s);
+}

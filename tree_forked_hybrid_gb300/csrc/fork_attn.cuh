@@ -1,0 +1,48 @@
+// Shared definitions of the fork-masked attention kernels.
+#pragma once
+
+#include "fork_common.cuh"
+
+namespace fork {
+
+// One contiguous key range of a query tile (see fork_attn_mma.cu).
+struct KeyRange {
+  const uint16_t* k;
+  const uint16_t* v;
+  int row0;  // first row in k/v
+  int len;   // rows in the range
+  int pos0;  // position of row0
+};
+
+struct AttnParams {
+  const int32_t* meta;
+  MetaLayout L;
+  const uint16_t* q;         // [T_cap, Hq, d]
+  const uint16_t* k;         // stream keys [T_cap, Hkv, d] (rotated copy when rope is on)
+  const uint16_t* v;         // [T_cap, Hkv, d]
+  const uint16_t* prefix_k;  // [prefix_rows, Hkv, d] (rotated copy when rope is on)
+  const uint16_t* prefix_v;
+  uint16_t* o;
+  const float2* rope_hi;     // (cos, sin) of 64*a*f_i, [a][d/2]
+  const float2* rope_lo;     // (cos, sin) of b*f_i,    [b < 64][d/2]
+  int Hq, Hkv, G;
+  int prefix_rows;           // rows of prefix_k / prefix_v
+  int window;
+  float rope_theta;          // 0 = off
+  float scale_log2;          // scale * log2(e)
+};
+
+// (cos, sin) of t * f_i from the two-level table: t = 64 a + b,
+// angle(t) = angle(64 a) + angle(b), combined by the angle-addition formula.
+__device__ __forceinline__ void rope_cs(const float2* hi, const float2* lo, int half, int t, int i,
+                                        float* cs, float* sn) {
+  const float2 A = hi[(t >> 6) * half + i];
+  const float2 B = lo[(t & 63) * half + i];
+  *cs = A.x * B.x - A.y * B.y;
+  *sn = A.y * B.x + A.x * B.y;
+}
+
+template <int D>
+int launch_attn_mma(const AttnParams& p, int grid_x, cudaStream_t s);
+
+}  // namespace fork
