@@ -42,8 +42,20 @@ def check_meta_equal(desc, R, Nq, T_cap, tile, **kw):
 
 @pytest.mark.parametrize("name", sorted(load_meta_cases()))
 def test_meta_golden(name):
+    """Hand-derived fixtures: tile-independent fields equal the fixture; the
+    work list (the device takes tiles of 8..128 tokens) equals the oracle's."""
     c = load_meta_cases()[name]
-    check_meta_equal(c["desc"], int(c["R"][0]), int(c["Nq"][0]), int(c["T_cap"][0]), int(c["tile"][0]))
+    R, Nq, T_cap = int(c["R"][0]), int(c["Nq"][0]), int(c["T_cap"][0])
+    tile = max(8, int(c["tile"][0]))
+    check_meta_equal(c["desc"], R, Nq, T_cap, tile)
+    got, _ = device_meta(c["desc"], R, Nq, T_cap, tile)
+    for key, want in c.items():
+        if key in ("R", "Nq", "T_cap", "tile", "desc") or key.startswith("work_"):
+            continue
+        if key == "T":
+            assert got["T"] == int(want[0])
+            continue
+        assert got[key][:want.shape[0]].tolist() == want.tolist(), key
 
 
 @pytest.mark.parametrize("wid", [0, 1, 2, 3, 4])

@@ -14,12 +14,15 @@
 // triangular solve (I + X) U = beta V, output): with the chunk's start state
 // S0, G_t = sum_{s<=t} log alpha_s and Gamma_ts = exp(G_t - G_s),
 //   u_t = eta_t (v_t - alpha_t S_{t-1} k_t),  S_t = alpha_t S_{t-1} + u_t k_t^T,
-//   (I + A) U = diag(eta) V - diag(eta e^G) K S0^T,  A_ts = eta_t Gamma_ts k_t.k_s (s<t),
+//   (I + A) U = diag(eta) (V - diag(e^G) K S0^T),  A_ts = eta_t Gamma_ts k_t.k_s (s<t),
 //   O = diag(e^G) Q S0^T + (tril(Gamma) * Q K^T) U,
 //   S_end = e^{G_last} S0 + U^T diag(Gamma_last,.) K.
-// Rows of S (the v index) evolve independently given the keys, so each CTA
-// owns a slice of 32 rows; chunks are aligned to the segment start, so a
-// question's result never depends on the rest of the round.
+// One CTA per (segment, head) keeps S (d x d, float32) in shared memory for
+// the whole segment.  The contractions run on the tensor cores with TF32
+// operands rounded to nearest (mma.sync m16n8k8), accumulation in float32;
+// T = (I + A)^{-1} is formed by blocked forward substitution in float32.
+// Chunks are aligned to the segment start, so a question's result never
+// depends on the rest of the round.
 #include "fork_common.cuh"
 
 namespace fork {
@@ -44,34 +47,113 @@ struct GdnParams {
 };
 
 namespace {
-constexpr int C = 64;     // chunk length
-constexpr int DVS = 32;   // rows of S per CTA
-constexpr int NT = 256;   // threads
+constexpr int C = 64;    // chunk length
+constexpr int NT = 256;  // threads (8 warps)
+constexpr int LDC = C + 4;  // stride of 64-wide fp32 tiles (== 4 mod 32)
 
 template <int D>
 struct GdnSmem {
-  static constexpr int LDD = D + 1;
-  static constexpr int LDV = DVS + 1;
-  static constexpr int LDC = C + 1;
-  float S[DVS * LDD];
-  float Q[C * LDD];
-  float K[C * LDD];
-  float W[C * LDD];
-  float U[C * LDV];
-  float A[C * LDC];
-  float QK[C * LDC];
-  float G[C];
-  float EG[C];
-  float GL[C];  // Gamma_{last, s} = exp(G_last - G_s)
+  static constexpr int LDD = D + 4;  // stride of D-wide fp32 tiles (== 4 mod 32)
+  float S[D * LDD];    // state, rows = v index, cols = k index
+  float Qh[C * LDD];   // normalised q of the chunk
+  float Kh[C * LDD];   // normalised k
+  float RU[C * LDD];   // v, then R = eta (v - e^G K S0^T), then U
+  float Pm[C * LDC];   // tril(Gamma) * Q K^T
+  float Am[C * LDC];   // strictly lower eta Gamma K K^T
+  float Tm[C * LDC];   // (I + A)^{-1}
+  float X[3 * 256];    // scratch of the blocked inverse
+  float G[C];          // inclusive cumulative log alpha
+  float EG[C];         // exp(G)
+  float GL[C];         // exp(G_last - G_s)
   float ETA[C];
 };
+
+__device__ __forceinline__ uint32_t tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Fragment loads (g = lane/4, t = lane%4).  A tile at (m0, k0):
+//   row-major A[m][k] = base[m*ld + k];  col-major A[m][k] = base[k*ld + m].
+__device__ __forceinline__ void lda_row(const float* base, int ld, int m0, int k0, int g, int t,
+                                        uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+  a0 = tf32(base[(m0 + g) * ld + k0 + t]);
+  a1 = tf32(base[(m0 + g + 8) * ld + k0 + t]);
+  a2 = tf32(base[(m0 + g) * ld + k0 + t + 4]);
+  a3 = tf32(base[(m0 + g + 8) * ld + k0 + t + 4]);
+}
+__device__ __forceinline__ void lda_col(const float* base, int ld, int m0, int k0, int g, int t,
+                                        uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+  a0 = tf32(base[(k0 + t) * ld + m0 + g]);
+  a1 = tf32(base[(k0 + t) * ld + m0 + g + 8]);
+  a2 = tf32(base[(k0 + t + 4) * ld + m0 + g]);
+  a3 = tf32(base[(k0 + t + 4) * ld + m0 + g + 8]);
+}
+// B tile at (k0, n0): n-major B[k][n] = X[n*ld + k];  k-major B[k][n] = Y[k*ld + n].
+__device__ __forceinline__ void ldb_n(const float* base, int ld, int k0, int n0, int g, int t,
+                                      uint32_t& b0, uint32_t& b1) {
+  b0 = tf32(base[(n0 + g) * ld + k0 + t]);
+  b1 = tf32(base[(n0 + g) * ld + k0 + t + 4]);
+}
+__device__ __forceinline__ void ldb_k(const float* base, int ld, int k0, int n0, int g, int t,
+                                      uint32_t& b0, uint32_t& b1) {
+  b0 = tf32(base[(k0 + t) * ld + n0 + g]);
+  b1 = tf32(base[(k0 + t + 4) * ld + n0 + g]);
+}
 }  // namespace
+
+// S[m0..m0+15][n0..n0+8*NTL) = e^{G_last} S + U^T diag(Gamma_last) K   (rows = v index)
+template <int D, int NTL>
+__device__ __forceinline__ void state_update(GdnSmem<D>& sm, int m0, int n0, int g, int t4) {
+  constexpr int LDD = GdnSmem<D>::LDD;
+  const float egl = sm.EG[C - 1];
+  float acc[NTL][4];
+#pragma unroll
+  for (int nt = 0; nt < NTL; ++nt) {
+    const int cc = n0 + nt * 8 + 2 * t4;
+    acc[nt][0] = egl * sm.S[(m0 + g) * LDD + cc];
+    acc[nt][1] = egl * sm.S[(m0 + g) * LDD + cc + 1];
+    acc[nt][2] = egl * sm.S[(m0 + g + 8) * LDD + cc];
+    acc[nt][3] = egl * sm.S[(m0 + g + 8) * LDD + cc + 1];
+  }
+  for (int k0 = 0; k0 < C; k0 += 8) {
+    uint32_t a0, a1, a2, a3;
+    lda_col(sm.RU, LDD, m0, k0, g, t4, a0, a1, a2, a3);
+    const float gl0 = sm.GL[k0 + t4], gl1 = sm.GL[k0 + t4 + 4];
+#pragma unroll
+    for (int nt = 0; nt < NTL; ++nt) {
+      const int nn = n0 + nt * 8 + g;
+      const uint32_t b0 = tf32(gl0 * sm.Kh[(k0 + t4) * LDD + nn]);
+      const uint32_t b1 = tf32(gl1 * sm.Kh[(k0 + t4 + 4) * LDD + nn]);
+      mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTL; ++nt) {
+    const int cc = n0 + nt * 8 + 2 * t4;
+    sm.S[(m0 + g) * LDD + cc] = acc[nt][0];
+    sm.S[(m0 + g) * LDD + cc + 1] = acc[nt][1];
+    sm.S[(m0 + g + 8) * LDD + cc] = acc[nt][2];
+    sm.S[(m0 + g + 8) * LDD + cc + 1] = acc[nt][3];
+  }
+}
 
 template <int D, bool BRANCH>
 __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   GdnSmem<D>& sm = *reinterpret_cast<GdnSmem<D>*>(smem_raw);
-  constexpr int LDD = GdnSmem<D>::LDD, LDV = GdnSmem<D>::LDV, LDC = GdnSmem<D>::LDC;
+  constexpr int LDD = GdnSmem<D>::LDD;
+  constexpr int NTD = D / 8;  // n-tiles over D
   const int32_t* meta = p.meta;
   const MetaLayout& L = p.L;
   if (meta[H_VALID] == 0) return;
@@ -88,30 +170,27 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
     j = idx;
   }
   const int h = blockIdx.y;
-  const int z = blockIdx.z;  // slice of S rows [z*DVS, z*DVS + DVS)
   const int H = p.H, K = p.K;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t4 = lane & 3;
   const int start = meta[L.seg_start + seg];
   const int len = meta[L.seg_len + seg];
   const int pos0 = meta[L.seg_pos0 + seg];
   const int pl = meta[L.req_prefix_len + j];
   const int ck = BRANCH ? -1 : meta[L.req_ckpt_pos + j];
 
-  // history rows (raw inputs before the segment): trunk -> resume window or zeros;
-  // question -> its request's trunk window (by index)
-  const uint16_t* hist = nullptr;
-  if (BRANCH) hist = p.hist_in;
-  else if (pl > 0) hist = p.hist_in;
-  const float* S0 = nullptr;
-  if (BRANCH) S0 = p.state_in;
-  else if (pl > 0) S0 = p.state_in;
-  if (!BRANCH && pl > 0 && (!p.state_in || !p.hist_in)) {
+  const bool resumed = !BRANCH && pl > 0;
+  if (resumed && (!p.state_in || !p.hist_in)) {
     if (tid == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
     return;
   }
+  // history rows (raw inputs before the segment): trunk -> resume window or zeros;
+  // question -> its request's trunk window, by index
+  const uint16_t* hist = (BRANCH || resumed) ? p.hist_in : nullptr;
+  const float* S0 = (BRANCH || resumed) ? p.state_in : nullptr;
+  const int64_t state_base = (static_cast<int64_t>(j) * H + h) * D * D;
 
   auto raw = [&](int o_seg, int s, int c) -> float {
-    // raw input of stream s (0 q, 1 k, 2 v), channel c, at segment offset o_seg (may be < 0)
     if (o_seg >= 0) {
       const uint16_t* x = s == 0 ? p.q : (s == 1 ? p.k : p.v);
       return bf2f(x[(static_cast<int64_t>(start + o_seg) * H + h) * D + c]);
@@ -120,168 +199,281 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
     if (r < 0 || hist == nullptr) return 0.f;
     return bf2f(hist[((static_cast<int64_t>(j * (K - 1) + r) * 3 + s) * H + h) * D + c]);
   };
-  auto conv = [&](int o_seg, int s, int c) -> float {
-    const float* w = p.conv_w + ((static_cast<int64_t>(s) * H + h) * D + c) * K;
-    float y = 0.f;
-    for (int i = 0; i < K; ++i) y += w[i] * raw(o_seg - (K - 1) + i, s, c);
-    return y / (1.f + expf(-y));  // SiLU
-  };
 
-  // initial state slice
-  for (int e = tid; e < DVS * D; e += NT) {
-    const int r = e / D, c = e % D;
-    sm.S[r * LDD + c] =
-        S0 ? S0[((static_cast<int64_t>(j) * H + h) * D + z * DVS + r) * D + c] : 0.f;
+  // initial state
+  for (int e = tid; e < D * D / 4; e += NT) {
+    const int r = e / (D / 4), c4 = (e % (D / 4)) * 4;
+    float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (S0) v4 = *reinterpret_cast<const float4*>(S0 + state_base + static_cast<int64_t>(r) * D + c4);
+    *reinterpret_cast<float4*>(&sm.S[r * LDD + c4]) = v4;
   }
   __syncthreads();
   if (!BRANCH && ck >= 0 && ck - pos0 == 0 && p.S_ckpt) {
-    for (int e = tid; e < DVS * D; e += NT) {
-      const int r = e / D, c = e % D;
-      p.S_ckpt[((static_cast<int64_t>(j) * H + h) * D + z * DVS + r) * D + c] = sm.S[r * LDD + c];
-    }
+    for (int e = tid; e < D * D; e += NT)
+      p.S_ckpt[state_base + e] = sm.S[(e / D) * LDD + e % D];
   }
 
   for (int c0 = 0; c0 < len; c0 += C) {
     const int n = min(C, len - c0);
-    // ---- gates ---------------------------------------------------------------
+    const bool need_state = !BRANCH || (c0 + C < len);
+    // ---- gates: G = inclusive cumsum of log alpha (two-warp scan) ---------------
     if (tid < C) {
       const int u = tid;
       const int64_t row = static_cast<int64_t>(start + c0 + u) * H + h;
-      sm.ETA[u] = u < n ? p.eta[row] : 0.f;
-      sm.G[u] = u < n ? logf(p.alpha[row]) : 0.f;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float acc = 0.f;
-      for (int u = 0; u < C; ++u) {
-        acc += sm.G[u];
-        sm.G[u] = acc;
-        sm.EG[u] = expf(acc);
+      const float e = u < n ? p.eta[row] : 0.f;
+      float x = u < n ? logf(p.alpha[row]) : 0.f;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
       }
-      for (int u = 0; u < C; ++u) sm.GL[u] = expf(acc - sm.G[u]);
-    }
-    // ---- conv + SiLU ----------------------------------------------------------
-    for (int e = tid; e < C * D; e += NT) {
-      const int u = e / D, c = e % D;
-      const bool ok = u < n;
-      sm.Q[u * LDD + c] = ok ? conv(c0 + u, 0, c) : 0.f;
-      sm.K[u * LDD + c] = ok ? conv(c0 + u, 1, c) : 0.f;
-    }
-    for (int e = tid; e < C * DVS; e += NT) {
-      const int u = e / DVS, c = e % DVS;
-      sm.U[u * LDV + c] = u < n ? conv(c0 + u, 2, z * DVS + c) : 0.f;
+      sm.ETA[u] = e;
+      sm.G[u] = x;  // per-warp inclusive scan; warp 1 adds warp 0's total below
     }
     __syncthreads();
-    // ---- L2 normalisation of q and k rows (one warp per row) -------------------
+    if (tid >= 32 && tid < C) sm.G[tid] += sm.G[31];
+    __syncthreads();
+    if (tid < C) {
+      sm.EG[tid] = expf(sm.G[tid]);
+      sm.GL[tid] = expf(sm.G[C - 1] - sm.G[tid]);
+    }
+    // ---- conv + SiLU: thread item = (stream, channel, half of the rows) -----------
+    for (int it = tid; it < 3 * D * 2; it += NT) {
+      const int s = it / (2 * D), c = (it / 2) % D, hf = it % 2;
+      const float* w = p.conv_w + ((static_cast<int64_t>(s) * H + h) * D + c) * K;
+      float w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3];
+      const int u0 = hf * 32;
+      float* dst = s == 0 ? sm.Qh : (s == 1 ? sm.Kh : sm.RU);
+      if (u0 >= n) {  // no token of this half in the chunk: zero rows, read nothing
+        for (int u = u0; u < u0 + 32; ++u) dst[u * LDD + c] = 0.f;
+        continue;
+      }
+      float x0 = raw(c0 + u0 - 3, s, c), x1 = raw(c0 + u0 - 2, s, c), x2 = raw(c0 + u0 - 1, s, c);
+      for (int u = u0; u < u0 + 32; ++u) {
+        float y = 0.f;
+        if (u < n) {
+          const float x3 = raw(c0 + u, s, c);
+          y = w0 * x0 + w1 * x1 + w2 * x2 + w3 * x3;
+          y = y / (1.f + expf(-y));
+          x0 = x1;
+          x1 = x2;
+          x2 = x3;
+        }
+        dst[u * LDD + c] = y;
+      }
+    }
+    __syncthreads();
+    // ---- L2 normalisation of q and k rows; v scaled later with R -----------------
+    for (int u = warp; u < 2 * C; u += NT / 32) {
+      float* row = (u < C) ? &sm.Qh[u * LDD] : &sm.Kh[(u - C) * LDD];
+      float ss = 0.f;
+      for (int c = lane; c < D; c += 32) ss += row[c] * row[c];
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float inv = 1.f / sqrtf(ss + 1e-6f);
+      for (int c = lane; c < D; c += 32) row[c] *= inv;
+    }
+    __syncthreads();
+
+    // ---- M1: [Q; K] K^T -> P (warps 0-3) and A (warps 4-7) -----------------------
     {
-      const int warp = tid >> 5, lane = tid & 31;
-      for (int u = warp; u < 2 * C; u += NT / 32) {
-        float* row = (u < C) ? &sm.Q[u * LDD] : &sm.K[(u - C) * LDD];
-        float ss = 0.f;
-        for (int c = lane; c < D; c += 32) ss += row[c] * row[c];
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float inv = 1.f / sqrtf(ss + 1e-6f);
-        for (int c = lane; c < D; c += 32) row[c] *= inv;
-      }
-    }
-    __syncthreads();
-    // RHS: W <- eta e^G K, U <- eta V
-    for (int e = tid; e < C * D; e += NT) {
-      const int u = e / D, c = e % D;
-      sm.W[u * LDD + c] = sm.ETA[u] * sm.EG[u] * sm.K[u * LDD + c];
-    }
-    for (int e = tid; e < C * DVS; e += NT) {
-      const int u = e / DVS, c = e % DVS;
-      sm.U[u * LDV + c] *= sm.ETA[u];
-    }
-    // ---- Gram and query-key matrices -------------------------------------------
-    for (int e = tid; e < C * C; e += NT) {
-      const int t = e / C, s = e % C;
-      float kk = 0.f, qk = 0.f;
-      if (s <= t) {
-        for (int c = 0; c < D; ++c) {
-          const float ks = sm.K[s * LDD + c];
-          kk += sm.K[t * LDD + c] * ks;
-          qk += sm.Q[t * LDD + c] * ks;
+      const float* X = warp < 4 ? sm.Qh : sm.Kh;
+      const int m0 = (warp & 3) * 16;
+      float acc[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      for (int k0 = 0; k0 < D; k0 += 8) {
+        uint32_t a0, a1, a2, a3;
+        lda_row(X, LDD, m0, k0, g, t4, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          uint32_t b0, b1;
+          ldb_n(sm.Kh, LDD, k0, nt * 8, g, t4, b0, b1);
+          mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
         }
       }
-      const float gam = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
-      sm.A[t * LDC + s] = s < t ? sm.ETA[t] * gam * kk : 0.f;
-      sm.QK[t * LDC + s] = gam * qk;
-    }
-    __syncthreads();
-    // ---- forward substitution (I + A) X = RHS, one column per thread ------------
-    if (tid < D + DVS) {
-      float* X;
-      int ld, c;
-      if (tid < D) { X = sm.W; ld = LDD; c = tid; }
-      else { X = sm.U; ld = LDV; c = tid - D; }
-      for (int t = 1; t < C; ++t) {
-        float acc = X[t * ld + c];
-        for (int s = 0; s < t; ++s) acc -= sm.A[t * LDC + s] * X[s * ld + c];
-        X[t * ld + c] = acc;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tr = m0 + g + (e >> 1) * 8;
+          const int sc = nt * 8 + 2 * t4 + (e & 1);
+          const float gam = sc <= tr ? expf(sm.G[tr] - sm.G[sc]) : 0.f;
+          if (warp < 4) sm.Pm[tr * LDC + sc] = gam * acc[nt][e];
+          else sm.Am[tr * LDC + sc] = sc < tr ? sm.ETA[tr] * gam * acc[nt][e] : 0.f;
+        }
       }
     }
     __syncthreads();
-    // ---- U = U~ - W S0^T ----------------------------------------------------------
-    for (int e = tid; e < C * DVS; e += NT) {
-      const int t = e / DVS, r = e % DVS;
-      float acc = 0.f;
-      for (int c = 0; c < D; ++c) acc += sm.W[t * LDD + c] * sm.S[r * LDD + c];
-      sm.U[t * LDV + r] -= acc;
+    // ---- T = (I + A)^{-1}: diagonal 16x16 blocks, then off-diagonal blocks -------
+    if (tid < 64) {
+      const int bi = tid >> 4, c = tid & 15, base = bi * 16;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int m = 0; m < r; ++m) acc -= sm.Am[(base + r) * LDC + base + m] * x[m];
+        x[r] = r < c ? 0.f : acc;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sm.Tm[(base + r) * LDC + base + c] = x[r];
     }
     __syncthreads();
-    // ---- outputs: O = e^G Q S0^T + (tril(Gamma) * QK^T) U ---------------------------
-    for (int e = tid; e < C * DVS; e += NT) {
-      const int t = e / DVS, r = e % DVS;
-      if (t >= n) continue;
-      float acc = 0.f;
-      for (int c = 0; c < D; ++c) acc += sm.Q[t * LDD + c] * sm.S[r * LDD + c];
-      acc *= sm.EG[t];
-      for (int s = 0; s <= t; ++s) acc += sm.QK[t * LDC + s] * sm.U[s * LDV + r];
-      p.o[(static_cast<int64_t>(start + c0 + t) * H + h) * D + z * DVS + r] = f2bf(acc);
+    for (int dist = 1; dist < 4; ++dist) {
+      const int npair = 4 - dist;
+      // X_p = sum_{k=j}^{i-1} A_ik T_kj  for pair p: (i = dist + p, j = p)
+      for (int e = tid; e < npair * 256; e += NT) {
+        const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
+        const int bi = dist + pr, bj = pr;
+        float acc = 0.f;
+        for (int m = bj * 16; m < bi * 16; ++m) acc += sm.Am[(bi * 16 + r) * LDC + m] * sm.Tm[m * LDC + bj * 16 + c];
+        sm.X[e] = acc;
+      }
+      __syncthreads();
+      for (int e = tid; e < npair * 256; e += NT) {
+        const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
+        const int bi = dist + pr, bj = pr;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc += sm.Tm[(bi * 16 + r) * LDC + bi * 16 + m] * sm.X[(pr << 8) + m * 16 + c];
+        sm.Tm[(bi * 16 + r) * LDC + bj * 16 + c] = -acc;
+      }
+      __syncthreads();
     }
-    // ---- checkpoint inside this chunk: state after r_ck tokens of it --------------
+
+    // ---- M3: [Q; K] S0^T; warps 0-3 keep e^G Q S0^T, warps 4-7 form R --------------
+    float qs[NTD][4];
+    {
+      const float* X = warp < 4 ? sm.Qh : sm.Kh;
+      const int m0 = (warp & 3) * 16;
+#pragma unroll
+      for (int i = 0; i < NTD; ++i) qs[i][0] = qs[i][1] = qs[i][2] = qs[i][3] = 0.f;
+      for (int k0 = 0; k0 < D; k0 += 8) {
+        uint32_t a0, a1, a2, a3;
+        lda_row(X, LDD, m0, k0, g, t4, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt) {
+          uint32_t b0, b1;
+          ldb_n(sm.S, LDD, k0, nt * 8, g, t4, b0, b1);
+          mma_tf32(qs[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      const float eg0 = sm.EG[m0 + g], eg1 = sm.EG[m0 + g + 8];
+      if (warp < 4) {
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt) {
+          qs[nt][0] *= eg0;
+          qs[nt][1] *= eg0;
+          qs[nt][2] *= eg1;
+          qs[nt][3] *= eg1;
+        }
+      } else {
+        const float et0 = sm.ETA[m0 + g], et1 = sm.ETA[m0 + g + 8];
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt) {
+          const int cc = nt * 8 + 2 * t4;
+          float* r0 = &sm.RU[(m0 + g) * LDD + cc];
+          float* r1 = &sm.RU[(m0 + g + 8) * LDD + cc];
+          r0[0] = et0 * (r0[0] - eg0 * qs[nt][0]);
+          r0[1] = et0 * (r0[1] - eg0 * qs[nt][1]);
+          r1[0] = et1 * (r1[0] - eg1 * qs[nt][2]);
+          r1[1] = et1 * (r1[1] - eg1 * qs[nt][3]);
+        }
+      }
+    }
+    __syncthreads();
+    // ---- M4: U = T R (T lower triangular: k-steps up to the diagonal) --------------
+    {
+      constexpr int NH = NTD / 2;  // n-tiles per warp
+      const int rt = warp & 3, m0 = rt * 16, n0 = (warp >> 2) * NH * 8;
+      float acc[NH][4];
+#pragma unroll
+      for (int i = 0; i < NH; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      for (int k0 = 0; k0 < m0 + 16; k0 += 8) {
+        uint32_t a0, a1, a2, a3;
+        lda_row(sm.Tm, LDC, m0, k0, g, t4, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NH; ++nt) {
+          uint32_t b0, b1;
+          ldb_k(sm.RU, LDD, k0, n0 + nt * 8, g, t4, b0, b1);
+          mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int nt = 0; nt < NH; ++nt) {
+        const int cc = n0 + nt * 8 + 2 * t4;
+        sm.RU[(m0 + g) * LDD + cc] = acc[nt][0];
+        sm.RU[(m0 + g) * LDD + cc + 1] = acc[nt][1];
+        sm.RU[(m0 + g + 8) * LDD + cc] = acc[nt][2];
+        sm.RU[(m0 + g + 8) * LDD + cc + 1] = acc[nt][3];
+      }
+    }
+    __syncthreads();
+    // ---- checkpoint inside this chunk: state after r_ck of its tokens (rare) -------
     if (!BRANCH && ck >= 0 && p.S_ckpt) {
       const int r_ck = ck - pos0 - c0;
       if (r_ck >= 1 && r_ck <= n) {
         const float gl = sm.G[r_ck - 1];
-        for (int e = tid; e < DVS * D; e += NT) {
+        for (int e = tid; e < D * D; e += NT) {
           const int r = e / D, c = e % D;
           float acc = expf(gl) * sm.S[r * LDD + c];
-          for (int s = 0; s < r_ck; ++s)
-            acc += expf(gl - sm.G[s]) * sm.U[s * LDV + r] * sm.K[s * LDD + c];
-          p.S_ckpt[((static_cast<int64_t>(j) * H + h) * D + z * DVS + r) * D + c] = acc;
+          for (int s = 0; s < r_ck; ++s) acc += expf(gl - sm.G[s]) * sm.RU[s * LDD + r] * sm.Kh[s * LDD + c];
+          p.S_ckpt[state_base + e] = acc;
+        }
+        __syncthreads();  // S is updated below
+      }
+    }
+    // ---- M5 (warps 0-3): O = e^G Q S0^T + P U  ->  global -----------------------
+    // ---- M6 (warps 4-7, then all): S = e^{G_last} S0 + U^T diag(Gamma_last) K ----
+    if (warp < 4) {
+      const int m0 = warp * 16;
+      for (int k0 = 0; k0 < m0 + 16; k0 += 8) {
+        uint32_t a0, a1, a2, a3;
+        lda_row(sm.Pm, LDC, m0, k0, g, t4, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt) {
+          uint32_t b0, b1;
+          ldb_k(sm.RU, LDD, k0, nt * 8, g, t4, b0, b1);
+          mma_tf32(qs[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      const int t0 = m0 + g, t1 = m0 + g + 8;
+#pragma unroll
+      for (int nt = 0; nt < NTD; ++nt) {
+        const int cc = nt * 8 + 2 * t4;
+        if (t0 < n) {
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(qs[nt][0], qs[nt][1]);
+          *reinterpret_cast<__nv_bfloat162*>(p.o + (static_cast<int64_t>(start + c0 + t0) * H + h) * D + cc) = v2;
+        }
+        if (t1 < n) {
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(qs[nt][2], qs[nt][3]);
+          *reinterpret_cast<__nv_bfloat162*>(p.o + (static_cast<int64_t>(start + c0 + t1) * H + h) * D + cc) = v2;
         }
       }
     }
-    __syncthreads();
-    // ---- state update: S = e^{G_last} S + U^T diag(Gamma_last,.) K ------------------
-    {
-      const float egl = sm.EG[C - 1];
-      for (int e = tid; e < DVS * D; e += NT) {
-        const int r = e / D, c = e % D;
-        float acc = egl * sm.S[r * LDD + c];
-        for (int s = 0; s < n; ++s) acc += sm.GL[s] * sm.U[s * LDV + r] * sm.K[s * LDD + c];
-        sm.S[r * LDD + c] = acc;
-      }
+    if (need_state) {
+      // warps 4-7 take row tiles 0..3 (all columns); then every warp takes half the
+      // columns of one of the remaining row tiles
+      if (warp >= 4) state_update<D, D / 8>(sm, (warp - 4) * 16, 0, g, t4);
+      __syncthreads();
+      for (int w = warp; w < (D / 16 - 4) * 2; w += NT / 32)
+        state_update<D, D / 16>(sm, (4 + (w >> 1)) * 16, (w & 1) * (D / 2), g, t4);
     }
     __syncthreads();
   }
 
   if (!BRANCH) {
-    for (int e = tid; e < DVS * D; e += NT) {
-      const int r = e / D, c = e % D;
-      p.S_P[((static_cast<int64_t>(j) * H + h) * D + z * DVS + r) * D + c] = sm.S[r * LDD + c];
+    for (int e = tid; e < D * D / 4; e += NT) {
+      const int r = e / (D / 4), c4 = (e % (D / 4)) * 4;
+      *reinterpret_cast<float4*>(p.S_P + state_base + static_cast<int64_t>(r) * D + c4) =
+          *reinterpret_cast<const float4*>(&sm.S[r * LDD + c4]);
     }
-    if (z == 0) {
-      // conv windows: raw inputs of the last K-1 positions before the end / before m
-      for (int e = tid; e < (K - 1) * 3 * D; e += NT) {
-        const int i = e / (3 * D), s = (e / D) % 3, c = e % D;
-        const int64_t dst = ((static_cast<int64_t>(j * (K - 1) + i) * 3 + s) * H + h) * D + c;
-        p.conv_win[dst] = f2bf(raw(len - (K - 1) + i, s, c));
-        if (ck >= 0 && p.conv_ckpt) p.conv_ckpt[dst] = f2bf(raw(ck - pos0 - (K - 1) + i, s, c));
-      }
+    // conv windows: raw inputs of the last K-1 positions before the end / before m
+    for (int e = tid; e < (K - 1) * 3 * D; e += NT) {
+      const int i = e / (3 * D), s = (e / D) % 3, c = e % D;
+      const int64_t dst = ((static_cast<int64_t>(j * (K - 1) + i) * 3 + s) * H + h) * D + c;
+      p.conv_win[dst] = f2bf(raw(len - (K - 1) + i, s, c));
+      if (ck >= 0 && p.conv_ckpt) p.conv_ckpt[dst] = f2bf(raw(ck - pos0 - (K - 1) + i, s, c));
     }
   }
 }
@@ -292,7 +484,7 @@ static int launch_gdn(const GdnParams& p, int grid_x, cudaStream_t s) {
   if (cudaFuncSetAttribute(gdn_chunk_kernel<D, BRANCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return FORK_ECUDA;
-  dim3 grid(grid_x, p.H, D / DVS);
+  dim3 grid(grid_x, p.H);
   gdn_chunk_kernel<D, BRANCH><<<grid, NT, smem, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? FORK_OK : FORK_ECUDA;
 }
@@ -304,7 +496,8 @@ static int gdn_common_checks(const fork_meta* m, MetaLayout* L, const uint16_t* 
   int rc = check_meta(m, L);
   if (rc != FORK_OK) return rc;
   if (!q || !k || !v || !alpha || !eta || !conv_w || !o) return FORK_EINVAL;
-  if (H < 1 || (d != 64 && d != 128) || K != 4 || chunk != C) return FORK_EINVAL;
+  if (H < 1 || H > 65535 || (d != 64 && d != 128) || K != 4 || chunk != C) return FORK_EINVAL;
+  if (!is_aligned16(q) || !is_aligned16(k) || !is_aligned16(v) || !is_aligned16(o)) return FORK_EINVAL;
   return FORK_OK;
 }
 
@@ -322,9 +515,10 @@ extern "C" int fork_gdn_trunk(const fork_meta* m, const uint16_t* q, const uint1
   MetaLayout L;
   int rc = gdn_common_checks(m, &L, q, k, v, alpha, eta, conv_w, H, d, K, chunk, o);
   if (rc != FORK_OK) return rc;
-  if (!S_P || !conv_win) return FORK_EINVAL;
+  if (!S_P || !conv_win || !is_aligned16(S_P)) return FORK_EINVAL;
   if ((S_ckpt == nullptr) != (conv_ckpt == nullptr)) return FORK_EINVAL;
   if ((init_state == nullptr) != (init_conv == nullptr)) return FORK_EINVAL;
+  if (init_state && !is_aligned16(init_state)) return FORK_EINVAL;
   if ((rc = check_device()) != FORK_OK) return rc;
   GdnParams p;
   p.meta = static_cast<const int32_t*>(m->d_buf);
@@ -357,7 +551,7 @@ extern "C" int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const ui
   MetaLayout L;
   int rc = gdn_common_checks(m, &L, q, k, v, alpha, eta, conv_w, H, d, K, chunk, o);
   if (rc != FORK_OK) return rc;
-  if (!S_P || !conv_win) return FORK_EINVAL;
+  if (!S_P || !conv_win || !is_aligned16(S_P)) return FORK_EINVAL;
   if ((rc = check_device()) != FORK_OK) return rc;
   if (m->max_q == 0) return FORK_OK;
   GdnParams p;
