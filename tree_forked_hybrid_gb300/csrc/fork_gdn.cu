@@ -47,21 +47,24 @@ struct GdnParams {
 };
 
 namespace {
-constexpr int C = 64;    // chunk length
-constexpr int NT = 256;  // threads (8 warps)
-constexpr int LDC = C + 4;  // stride of 64-wide fp32 tiles (== 4 mod 32)
+constexpr int C = 64;         // chunk length
+constexpr int NT = 256;       // threads (8 warps)
+constexpr int LDC = C + 8;    // stride of 64-wide fp32 tiles (== 8 mod 32)
+constexpr int KW = 4;         // conv width
+constexpr int HR = C + KW - 1;  // staged raw rows per chunk (history + chunk)
 
 template <int D>
 struct GdnSmem {
-  static constexpr int LDD = D + 4;  // stride of D-wide fp32 tiles (== 4 mod 32)
-  float S[D * LDD];    // state, rows = v index, cols = k index
-  float Qh[C * LDD];   // normalised q of the chunk
+  static constexpr int LDD = D + 8;  // stride of D-wide fp32 tiles (== 8 mod 32)
+  float Qh[C * LDD];   // normalised q of the chunk; later the bf16 output staging
   float Kh[C * LDD];   // normalised k
-  float RU[C * LDD];   // v, then R = eta (v - e^G K S0^T), then U
+  float Vh[C * LDD];   // conv'd v
   float Pm[C * LDC];   // tril(Gamma) * Q K^T
   float Am[C * LDC];   // strictly lower eta Gamma K K^T
   float Tm[C * LDC];   // (I + A)^{-1}
   float X[3 * 256];    // scratch of the blocked inverse
+  uint16_t raw[3 * HR * D];  // staged raw q, k, v rows (bf16) of the next chunk
+  float ga[C], ge[C];  // staged alpha, eta of the next chunk
   float G[C];          // inclusive cumulative log alpha
   float EG[C];         // exp(G)
   float GL[C];         // exp(G_last - G_s)
@@ -83,77 +86,64 @@ __device__ __forceinline__ void mma_tf32(float* c, uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Fragment loads (g = lane/4, t = lane%4).  A tile at (m0, k0):
-//   row-major A[m][k] = base[m*ld + k];  col-major A[m][k] = base[k*ld + m].
-__device__ __forceinline__ void lda_row(const float* base, int ld, int m0, int k0, int g, int t,
-                                        uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-  a0 = tf32(base[(m0 + g) * ld + k0 + t]);
-  a1 = tf32(base[(m0 + g + 8) * ld + k0 + t]);
-  a2 = tf32(base[(m0 + g) * ld + k0 + t + 4]);
-  a3 = tf32(base[(m0 + g + 8) * ld + k0 + t + 4]);
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void lda_col(const float* base, int ld, int m0, int k0, int g, int t,
-                                        uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-  a0 = tf32(base[(k0 + t) * ld + m0 + g]);
-  a1 = tf32(base[(k0 + t) * ld + m0 + g + 8]);
-  a2 = tf32(base[(k0 + t + 4) * ld + m0 + g]);
-  a3 = tf32(base[(k0 + t + 4) * ld + m0 + g + 8]);
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0));
 }
-// B tile at (k0, n0): n-major B[k][n] = X[n*ld + k];  k-major B[k][n] = Y[k*ld + n].
-__device__ __forceinline__ void ldb_n(const float* base, int ld, int k0, int n0, int g, int t,
-                                      uint32_t& b0, uint32_t& b1) {
-  b0 = tf32(base[(n0 + g) * ld + k0 + t]);
-  b1 = tf32(base[(n0 + g) * ld + k0 + t + 4]);
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 4 : 0));
 }
-__device__ __forceinline__ void ldb_k(const float* base, int ld, int k0, int n0, int g, int t,
-                                      uint32_t& b0, uint32_t& b1) {
-  b0 = tf32(base[(k0 + t) * ld + n0 + g]);
-  b1 = tf32(base[(k0 + t + 4) * ld + n0 + g]);
+
+// Every contraction below sums over an index k in blocks of 8.  Inside a
+// block the fragment slot k' = t (t = lane % 4) carries index 2t and slot
+// k' = t + 4 carries 2t + 1 (the same on both operands, so the sum is
+// unchanged).  This makes an accumulator tile (columns 2t, 2t+1 per thread)
+// directly usable as the A operand of the next product, and turns shared
+// memory operand loads into float2 loads.
+struct Frag {
+  uint32_t a0, a1, a2, a3;
+};
+// A operand from an accumulator tile acc[4] = {(g,2t), (g,2t+1), (g+8,2t), (g+8,2t+1)}.
+__device__ __forceinline__ Frag a_from_acc(const float* acc) {
+  return {tf32(acc[0]), tf32(acc[2]), tf32(acc[1]), tf32(acc[3])};
+}
+// A operand rows m0.., block k0, from a row-major fp32 tile.
+__device__ __forceinline__ Frag a_from_rows(const float* base, int ld, int m0, int k0, int g, int t) {
+  const float2 lo = *reinterpret_cast<const float2*>(base + (m0 + g) * ld + k0 + 2 * t);
+  const float2 hi = *reinterpret_cast<const float2*>(base + (m0 + g + 8) * ld + k0 + 2 * t);
+  return {tf32(lo.x), tf32(hi.x), tf32(lo.y), tf32(hi.y)};
+}
+// B operand B[k][n] = X[n][k] (X row-major), tile (k0, n0).
+__device__ __forceinline__ void b_from_rows(const float* base, int ld, int k0, int n0, int g, int t,
+                                            uint32_t& b0, uint32_t& b1) {
+  const float2 v = *reinterpret_cast<const float2*>(base + (n0 + g) * ld + k0 + 2 * t);
+  b0 = tf32(v.x);
+  b1 = tf32(v.y);
+}
+__device__ __forceinline__ void mma(float* c, const Frag& a, uint32_t b0, uint32_t b1) {
+  mma_tf32(c, a.a0, a.a1, a.a2, a.a3, b0, b1);
 }
 }  // namespace
 
-// S[m0..m0+15][n0..n0+8*NTL) = e^{G_last} S + U^T diag(Gamma_last) K   (rows = v index)
-template <int D, int NTL>
-__device__ __forceinline__ void state_update(GdnSmem<D>& sm, int m0, int n0, int g, int t4) {
-  constexpr int LDD = GdnSmem<D>::LDD;
-  const float egl = sm.EG[C - 1];
-  float acc[NTL][4];
-#pragma unroll
-  for (int nt = 0; nt < NTL; ++nt) {
-    const int cc = n0 + nt * 8 + 2 * t4;
-    acc[nt][0] = egl * sm.S[(m0 + g) * LDD + cc];
-    acc[nt][1] = egl * sm.S[(m0 + g) * LDD + cc + 1];
-    acc[nt][2] = egl * sm.S[(m0 + g + 8) * LDD + cc];
-    acc[nt][3] = egl * sm.S[(m0 + g + 8) * LDD + cc + 1];
-  }
-  for (int k0 = 0; k0 < C; k0 += 8) {
-    uint32_t a0, a1, a2, a3;
-    lda_col(sm.RU, LDD, m0, k0, g, t4, a0, a1, a2, a3);
-    const float gl0 = sm.GL[k0 + t4], gl1 = sm.GL[k0 + t4 + 4];
-#pragma unroll
-    for (int nt = 0; nt < NTL; ++nt) {
-      const int nn = n0 + nt * 8 + g;
-      const uint32_t b0 = tf32(gl0 * sm.Kh[(k0 + t4) * LDD + nn]);
-      const uint32_t b1 = tf32(gl1 * sm.Kh[(k0 + t4 + 4) * LDD + nn]);
-      mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
-    }
-  }
-#pragma unroll
-  for (int nt = 0; nt < NTL; ++nt) {
-    const int cc = n0 + nt * 8 + 2 * t4;
-    sm.S[(m0 + g) * LDD + cc] = acc[nt][0];
-    sm.S[(m0 + g) * LDD + cc + 1] = acc[nt][1];
-    sm.S[(m0 + g + 8) * LDD + cc] = acc[nt][2];
-    sm.S[(m0 + g + 8) * LDD + cc + 1] = acc[nt][3];
-  }
-}
-
+// One CTA per (segment, head).  The state S (d x d, rows = v index) lives in
+// registers: warp w < d/16 holds rows 16w..16w+15 as an accumulator tile.
+// Per chunk (all products TF32 on the tensor cores, float32 accumulation):
+//   M1  [Q; K] K^T            -> P = tril(Gamma) * QK^T, A = eta Gamma KK^T (strict)
+//   T = (I + A)^{-1}          (float32, blocked forward substitution)
+//   M3  S [K; Q]^T            -> (K S^T)^T, (Q S^T)^T               (A = S from registers)
+//   R^T = eta (V - e^G K S^T)^T;  U^T = R^T T^T;  O^T = e^G (Q S^T)^T + U^T P^T
+//   S  <- e^{G_last} S + U^T diag(Gamma_last) K
 template <int D, bool BRANCH>
 __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   GdnSmem<D>& sm = *reinterpret_cast<GdnSmem<D>*>(smem_raw);
   constexpr int LDD = GdnSmem<D>::LDD;
-  constexpr int NTD = D / 8;  // n-tiles over D
+  constexpr int NTD = D / 8;    // 8-wide tiles over d
+  constexpr int NWS = D / 16;   // warps holding the state
   const int32_t* meta = p.meta;
   const MetaLayout& L = p.L;
   if (meta[H_VALID] == 0) return;
@@ -170,7 +160,7 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
     j = idx;
   }
   const int h = blockIdx.y;
-  const int H = p.H, K = p.K;
+  const int H = p.H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
   const int start = meta[L.seg_start + seg];
@@ -189,80 +179,116 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
   const uint16_t* hist = (BRANCH || resumed) ? p.hist_in : nullptr;
   const float* S0 = (BRANCH || resumed) ? p.state_in : nullptr;
   const int64_t state_base = (static_cast<int64_t>(j) * H + h) * D * D;
+  const uint16_t* xs[3] = {p.q, p.k, p.v};
 
   auto raw = [&](int o_seg, int s, int c) -> float {
-    if (o_seg >= 0) {
-      const uint16_t* x = s == 0 ? p.q : (s == 1 ? p.k : p.v);
-      return bf2f(x[(static_cast<int64_t>(start + o_seg) * H + h) * D + c]);
-    }
-    const int r = K - 1 + o_seg;
+    if (o_seg >= 0) return bf2f(xs[s][(static_cast<int64_t>(start + o_seg) * H + h) * D + c]);
+    const int r = KW - 1 + o_seg;
     if (r < 0 || hist == nullptr) return 0.f;
-    return bf2f(hist[((static_cast<int64_t>(j * (K - 1) + r) * 3 + s) * H + h) * D + c]);
+    return bf2f(hist[((static_cast<int64_t>(j * (KW - 1) + r) * 3 + s) * H + h) * D + c]);
+  };
+  // stage raw rows c0n-3 .. c0n+C-1 (zero beyond the segment) and the gates of a chunk
+  auto prefetch = [&](int c0n) {
+    constexpr int CPR = D / 8;
+    for (int e = tid; e < 3 * HR * CPR; e += NT) {
+      const int s = e / (HR * CPR), r = (e / CPR) % HR, ch = e % CPR;
+      const int o_seg = c0n - (KW - 1) + r;
+      const uint16_t* src = p.q;
+      bool valid = false;
+      if (o_seg >= 0 && o_seg < len) {
+        src = xs[s] + (static_cast<int64_t>(start + o_seg) * H + h) * D + ch * 8;
+        valid = true;
+      } else if (o_seg < 0 && hist != nullptr) {
+        src = hist + ((static_cast<int64_t>(j * (KW - 1) + (KW - 1) + o_seg) * 3 + s) * H + h) * D + ch * 8;
+        valid = true;
+      }
+      cp_async16(&sm.raw[(s * HR + r) * D + ch * 8], src, valid);
+    }
+    for (int u = tid; u < 2 * C; u += NT) {
+      const int o_seg = c0n + (u % C);
+      const bool valid = o_seg < len;
+      const float* src = (u < C ? p.alpha : p.eta) + (static_cast<int64_t>(start + (valid ? o_seg : 0)) * H + h);
+      cp_async4(u < C ? &sm.ga[u] : &sm.ge[u - C], src, valid);
+    }
+    asm volatile("cp.async.commit_group;\n" ::);
   };
 
-  // initial state
-  for (int e = tid; e < D * D / 4; e += NT) {
-    const int r = e / (D / 4), c4 = (e % (D / 4)) * 4;
-    float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (S0) v4 = *reinterpret_cast<const float4*>(S0 + state_base + static_cast<int64_t>(r) * D + c4);
-    *reinterpret_cast<float4*>(&sm.S[r * LDD + c4]) = v4;
+  // state rows of this warp, as an accumulator tile
+  float st[NTD][4];
+  const bool holds_state = warp < NWS;
+  const int m0 = warp * 16;  // first state row of this warp
+#pragma unroll
+  for (int nt = 0; nt < NTD; ++nt) {
+    st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.f;
+    if (holds_state && S0) {
+      const int cc = nt * 8 + 2 * t4;
+      const float2 a = *reinterpret_cast<const float2*>(S0 + state_base + (m0 + g) * D + cc);
+      const float2 b = *reinterpret_cast<const float2*>(S0 + state_base + (m0 + g + 8) * D + cc);
+      st[nt][0] = a.x;
+      st[nt][1] = a.y;
+      st[nt][2] = b.x;
+      st[nt][3] = b.y;
+    }
   }
-  __syncthreads();
-  if (!BRANCH && ck >= 0 && ck - pos0 == 0 && p.S_ckpt) {
-    for (int e = tid; e < D * D; e += NT)
-      p.S_ckpt[state_base + e] = sm.S[(e / D) * LDD + e % D];
-  }
+  auto store_state = [&](float* dst, const float (*v)[4]) {
+#pragma unroll
+    for (int nt = 0; nt < NTD; ++nt) {
+      const int cc = nt * 8 + 2 * t4;
+      *reinterpret_cast<float2*>(dst + state_base + (m0 + g) * D + cc) = make_float2(v[nt][0], v[nt][1]);
+      *reinterpret_cast<float2*>(dst + state_base + (m0 + g + 8) * D + cc) = make_float2(v[nt][2], v[nt][3]);
+    }
+  };
+  if (!BRANCH && ck >= 0 && ck - pos0 == 0 && p.S_ckpt && holds_state) store_state(p.S_ckpt, st);
 
+  if (len > 0) prefetch(0);
   for (int c0 = 0; c0 < len; c0 += C) {
     const int n = min(C, len - c0);
     const bool need_state = !BRANCH || (c0 + C < len);
-    // ---- gates: G = inclusive cumsum of log alpha (two-warp scan) ---------------
-    if (tid < C) {
-      const int u = tid;
-      const int64_t row = static_cast<int64_t>(start + c0 + u) * H + h;
-      const float e = u < n ? p.eta[row] : 0.f;
-      float x = u < n ? logf(p.alpha[row]) : 0.f;
+    asm volatile("cp.async.wait_group 0;\n" ::);
+    __syncthreads();
+    // ---- gates (warp 0): G = inclusive cumsum of log alpha ---------------------
+    if (warp == 0) {
+      const int u0 = 2 * lane, u1 = u0 + 1;
+      const float l0 = u0 < n ? logf(sm.ga[u0]) : 0.f, l1 = u1 < n ? logf(sm.ga[u1]) : 0.f;
+      float x = l0 + l1;
       for (int o = 1; o < 32; o <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
       }
-      sm.ETA[u] = e;
-      sm.G[u] = x;  // per-warp inclusive scan; warp 1 adds warp 0's total below
+      const float g1 = x, g0 = x - l1;
+      const float glast = __shfl_sync(0xffffffffu, x, 31);
+      sm.G[u0] = g0;
+      sm.G[u1] = g1;
+      sm.EG[u0] = expf(g0);
+      sm.EG[u1] = expf(g1);
+      sm.GL[u0] = expf(glast - g0);
+      sm.GL[u1] = expf(glast - g1);
+      sm.ETA[u0] = u0 < n ? sm.ge[u0] : 0.f;
+      sm.ETA[u1] = u1 < n ? sm.ge[u1] : 0.f;
     }
-    __syncthreads();
-    if (tid >= 32 && tid < C) sm.G[tid] += sm.G[31];
-    __syncthreads();
-    if (tid < C) {
-      sm.EG[tid] = expf(sm.G[tid]);
-      sm.GL[tid] = expf(sm.G[C - 1] - sm.G[tid]);
-    }
-    // ---- conv + SiLU: thread item = (stream, channel, half of the rows) -----------
+    // ---- conv + SiLU from the staged rows: item = (stream, channel, half) -------
     for (int it = tid; it < 3 * D * 2; it += NT) {
       const int s = it / (2 * D), c = (it / 2) % D, hf = it % 2;
-      const float* w = p.conv_w + ((static_cast<int64_t>(s) * H + h) * D + c) * K;
-      float w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3];
+      const float* w = p.conv_w + ((static_cast<int64_t>(s) * H + h) * D + c) * KW;
+      const float w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3];
+      const uint16_t* col = &sm.raw[s * HR * D + c];
+      float* dst = s == 0 ? sm.Qh : (s == 1 ? sm.Kh : sm.Vh);
       const int u0 = hf * 32;
-      float* dst = s == 0 ? sm.Qh : (s == 1 ? sm.Kh : sm.RU);
-      if (u0 >= n) {  // no token of this half in the chunk: zero rows, read nothing
-        for (int u = u0; u < u0 + 32; ++u) dst[u * LDD + c] = 0.f;
-        continue;
-      }
-      float x0 = raw(c0 + u0 - 3, s, c), x1 = raw(c0 + u0 - 2, s, c), x2 = raw(c0 + u0 - 1, s, c);
+      float x0 = bf2f(col[u0 * D]), x1 = bf2f(col[(u0 + 1) * D]), x2 = bf2f(col[(u0 + 2) * D]);
+#pragma unroll 4
       for (int u = u0; u < u0 + 32; ++u) {
-        float y = 0.f;
-        if (u < n) {
-          const float x3 = raw(c0 + u, s, c);
-          y = w0 * x0 + w1 * x1 + w2 * x2 + w3 * x3;
-          y = y / (1.f + expf(-y));
-          x0 = x1;
-          x1 = x2;
-          x2 = x3;
-        }
-        dst[u * LDD + c] = y;
+        const float x3 = bf2f(col[(u + 3) * D]);
+        float y = w0 * x0 + w1 * x1 + w2 * x2 + w3 * x3;
+        y = y / (1.f + expf(-y));
+        dst[u * LDD + c] = u < n ? y : 0.f;
+        x0 = x1;
+        x1 = x2;
+        x2 = x3;
       }
     }
     __syncthreads();
-    // ---- L2 normalisation of q and k rows; v scaled later with R -----------------
+    if (c0 + C < len) prefetch(c0 + C);  // the staging buffer is free again
+    // ---- L2 normalisation of q and k rows --------------------------------------
     for (int u = warp; u < 2 * C; u += NT / 32) {
       float* row = (u < C) ? &sm.Qh[u * LDD] : &sm.Kh[(u - C) * LDD];
       float ss = 0.f;
@@ -275,30 +301,37 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
 
     // ---- M1: [Q; K] K^T -> P (warps 0-3) and A (warps 4-7) -----------------------
     {
-      const float* X = warp < 4 ? sm.Qh : sm.Kh;
-      const int m0 = (warp & 3) * 16;
+      const float* Xs = warp < 4 ? sm.Qh : sm.Kh;
+      const int r0 = (warp & 3) * 16;
       float acc[8][4];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll 2
       for (int k0 = 0; k0 < D; k0 += 8) {
-        uint32_t a0, a1, a2, a3;
-        lda_row(X, LDD, m0, k0, g, t4, a0, a1, a2, a3);
+        const Frag a = a_from_rows(Xs, LDD, r0, k0, g, t4);
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           uint32_t b0, b1;
-          ldb_n(sm.Kh, LDD, k0, nt * 8, g, t4, b0, b1);
-          mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+          b_from_rows(sm.Kh, LDD, k0, nt * 8, g, t4, b0, b1);
+          mma(acc[nt], a, b0, b1);
         }
       }
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tr = m0 + g + (e >> 1) * 8;
-          const int sc = nt * 8 + 2 * t4 + (e & 1);
-          const float gam = sc <= tr ? expf(sm.G[tr] - sm.G[sc]) : 0.f;
-          if (warp < 4) sm.Pm[tr * LDC + sc] = gam * acc[nt][e];
-          else sm.Am[tr * LDC + sc] = sc < tr ? sm.ETA[tr] * gam * acc[nt][e] : 0.f;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int tr = r0 + g + hh * 8;
+          const int sc = nt * 8 + 2 * t4;
+          const float v0 = acc[nt][2 * hh], v1 = acc[nt][2 * hh + 1];
+          const float gam0 = sc <= tr ? expf(sm.G[tr] - sm.G[sc]) : 0.f;
+          const float gam1 = sc + 1 <= tr ? expf(sm.G[tr] - sm.G[sc + 1]) : 0.f;
+          if (warp < 4) {
+            *reinterpret_cast<float2*>(&sm.Pm[tr * LDC + sc]) = make_float2(gam0 * v0, gam1 * v1);
+          } else {
+            const float et = sm.ETA[tr];
+            *reinterpret_cast<float2*>(&sm.Am[tr * LDC + sc]) =
+                make_float2(sc < tr ? et * gam0 * v0 : 0.f, sc + 1 < tr ? et * gam1 * v1 : 0.f);
+          }
         }
       }
     }
@@ -320,7 +353,6 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
     __syncthreads();
     for (int dist = 1; dist < 4; ++dist) {
       const int npair = 4 - dist;
-      // X_p = sum_{k=j}^{i-1} A_ik T_kj  for pair p: (i = dist + p, j = p)
       for (int e = tid; e < npair * 256; e += NT) {
         const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
         const int bi = dist + pr, bj = pr;
@@ -340,140 +372,142 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
       __syncthreads();
     }
 
-    // ---- M3: [Q; K] S0^T; warps 0-3 keep e^G Q S0^T, warps 4-7 form R --------------
-    float qs[NTD][4];
-    {
-      const float* X = warp < 4 ? sm.Qh : sm.Kh;
-      const int m0 = (warp & 3) * 16;
+    // ---- state products (warps holding S) ---------------------------------------
+    float rk[8][4];  // (K S^T)^T, then R^T
+    float oq[8][4];  // e^G (Q S^T)^T, then O^T
+    float ut[8][4];  // U^T
+    if (holds_state) {
 #pragma unroll
-      for (int i = 0; i < NTD; ++i) qs[i][0] = qs[i][1] = qs[i][2] = qs[i][3] = 0.f;
-      for (int k0 = 0; k0 < D; k0 += 8) {
-        uint32_t a0, a1, a2, a3;
-        lda_row(X, LDD, m0, k0, g, t4, a0, a1, a2, a3);
+      for (int i = 0; i < 8; ++i)
+        rk[i][0] = rk[i][1] = rk[i][2] = rk[i][3] = oq[i][0] = oq[i][1] = oq[i][2] = oq[i][3] = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < NTD; ++nt) {
+      for (int kb = 0; kb < NTD; ++kb) {
+        const Frag a = a_from_acc(st[kb]);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
           uint32_t b0, b1;
-          ldb_n(sm.S, LDD, k0, nt * 8, g, t4, b0, b1);
-          mma_tf32(qs[nt], a0, a1, a2, a3, b0, b1);
+          b_from_rows(sm.Kh, LDD, kb * 8, nt * 8, g, t4, b0, b1);
+          mma(rk[nt], a, b0, b1);
+          b_from_rows(sm.Qh, LDD, kb * 8, nt * 8, g, t4, b0, b1);
+          mma(oq[nt], a, b0, b1);
         }
       }
-      const float eg0 = sm.EG[m0 + g], eg1 = sm.EG[m0 + g + 8];
-      if (warp < 4) {
+      // R^T[v][t] = eta_t (V[t][v] - e^{G_t} (K S^T)^T[v][t]);  O^T starts at e^{G_t} (Q S^T)^T
 #pragma unroll
-        for (int nt = 0; nt < NTD; ++nt) {
-          qs[nt][0] *= eg0;
-          qs[nt][1] *= eg0;
-          qs[nt][2] *= eg1;
-          qs[nt][3] *= eg1;
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int v = m0 + g + (e >> 1) * 8, t = nt * 8 + 2 * t4 + (e & 1);
+          const float eg = sm.EG[t];
+          rk[nt][e] = sm.ETA[t] * (sm.Vh[t * LDD + v] - eg * rk[nt][e]);
+          oq[nt][e] *= eg;
         }
-      } else {
-        const float et0 = sm.ETA[m0 + g], et1 = sm.ETA[m0 + g + 8];
+      }
+      // U^T = R^T T^T   (T lower triangular: block kb contributes to token tiles nt >= kb)
 #pragma unroll
-        for (int nt = 0; nt < NTD; ++nt) {
-          const int cc = nt * 8 + 2 * t4;
-          float* r0 = &sm.RU[(m0 + g) * LDD + cc];
-          float* r1 = &sm.RU[(m0 + g + 8) * LDD + cc];
-          r0[0] = et0 * (r0[0] - eg0 * qs[nt][0]);
-          r0[1] = et0 * (r0[1] - eg0 * qs[nt][1]);
-          r1[0] = et1 * (r1[0] - eg1 * qs[nt][2]);
-          r1[1] = et1 * (r1[1] - eg1 * qs[nt][3]);
+      for (int i = 0; i < 8; ++i) ut[i][0] = ut[i][1] = ut[i][2] = ut[i][3] = 0.f;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        const Frag a = a_from_acc(rk[kb]);
+#pragma unroll
+        for (int nt = kb; nt < 8; ++nt) {
+          uint32_t b0, b1;
+          b_from_rows(sm.Tm, LDC, kb * 8, nt * 8, g, t4, b0, b1);
+          mma(ut[nt], a, b0, b1);
+        }
+      }
+      // O^T += U^T P^T   (P lower triangular incl. diagonal)
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        const Frag a = a_from_acc(ut[kb]);
+#pragma unroll
+        for (int nt = kb; nt < 8; ++nt) {
+          uint32_t b0, b1;
+          b_from_rows(sm.Pm, LDC, kb * 8, nt * 8, g, t4, b0, b1);
+          mma(oq[nt], a, b0, b1);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done reading Qh: reuse it to stage the output
+    uint16_t* ost = reinterpret_cast<uint16_t*>(sm.Qh);  // [C][D + 8] bf16
+    constexpr int LDO = D + 8;
+    if (holds_state) {
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int v = m0 + g + (e >> 1) * 8, t = nt * 8 + 2 * t4 + (e & 1);
+          ost[t * LDO + v] = f2bf(oq[nt][e]);
         }
       }
     }
     __syncthreads();
-    // ---- M4: U = T R (T lower triangular: k-steps up to the diagonal) --------------
     {
-      constexpr int NH = NTD / 2;  // n-tiles per warp
-      const int rt = warp & 3, m0 = rt * 16, n0 = (warp >> 2) * NH * 8;
-      float acc[NH][4];
-#pragma unroll
-      for (int i = 0; i < NH; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-      for (int k0 = 0; k0 < m0 + 16; k0 += 8) {
-        uint32_t a0, a1, a2, a3;
-        lda_row(sm.Tm, LDC, m0, k0, g, t4, a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NH; ++nt) {
-          uint32_t b0, b1;
-          ldb_k(sm.RU, LDD, k0, n0 + nt * 8, g, t4, b0, b1);
-          mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
-        }
-      }
-      __syncthreads();
-#pragma unroll
-      for (int nt = 0; nt < NH; ++nt) {
-        const int cc = n0 + nt * 8 + 2 * t4;
-        sm.RU[(m0 + g) * LDD + cc] = acc[nt][0];
-        sm.RU[(m0 + g) * LDD + cc + 1] = acc[nt][1];
-        sm.RU[(m0 + g + 8) * LDD + cc] = acc[nt][2];
-        sm.RU[(m0 + g + 8) * LDD + cc + 1] = acc[nt][3];
+      constexpr int CPR = D / 8;
+      for (int e = tid; e < n * CPR; e += NT) {
+        const int t = e / CPR, ch = e % CPR;
+        *reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(start + c0 + t) * H + h) * D + ch * 8) =
+            *reinterpret_cast<const uint4*>(&ost[t * LDO + ch * 8]);
       }
     }
-    __syncthreads();
-    // ---- checkpoint inside this chunk: state after r_ck of its tokens (rare) -------
-    if (!BRANCH && ck >= 0 && p.S_ckpt) {
+    // ---- checkpoint inside this chunk (rare): state after r_ck of its tokens -------
+    if (!BRANCH && ck >= 0 && p.S_ckpt && holds_state) {
       const int r_ck = ck - pos0 - c0;
       if (r_ck >= 1 && r_ck <= n) {
-        const float gl = sm.G[r_ck - 1];
-        for (int e = tid; e < D * D; e += NT) {
-          const int r = e / D, c = e % D;
-          float acc = expf(gl) * sm.S[r * LDD + c];
-          for (int s = 0; s < r_ck; ++s) acc += expf(gl - sm.G[s]) * sm.RU[s * LDD + r] * sm.Kh[s * LDD + c];
-          p.S_ckpt[state_base + e] = acc;
+        const float gr = sm.G[r_ck - 1];
+        const float egr = expf(gr);
+        float sc[NTD][4];
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[nt][e] = egr * st[nt][e];
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          const Frag a = a_from_acc(ut[kb]);
+          const int s0 = kb * 8 + 2 * t4;
+          const float f0 = s0 < r_ck ? expf(gr - sm.G[s0]) : 0.f;
+          const float f1 = s0 + 1 < r_ck ? expf(gr - sm.G[s0 + 1]) : 0.f;
+#pragma unroll
+          for (int nt = 0; nt < NTD; ++nt) {
+            const uint32_t b0 = tf32(f0 * sm.Kh[s0 * LDD + nt * 8 + g]);
+            const uint32_t b1 = tf32(f1 * sm.Kh[(s0 + 1) * LDD + nt * 8 + g]);
+            mma(sc[nt], a, b0, b1);
+          }
         }
-        __syncthreads();  // S is updated below
+        store_state(p.S_ckpt, sc);
       }
     }
-    // ---- M5 (warps 0-3): O = e^G Q S0^T + P U  ->  global -----------------------
-    // ---- M6 (warps 4-7, then all): S = e^{G_last} S0 + U^T diag(Gamma_last) K ----
-    if (warp < 4) {
-      const int m0 = warp * 16;
-      for (int k0 = 0; k0 < m0 + 16; k0 += 8) {
-        uint32_t a0, a1, a2, a3;
-        lda_row(sm.Pm, LDC, m0, k0, g, t4, a0, a1, a2, a3);
+    // ---- S <- e^{G_last} S + U^T diag(Gamma_last) K ---------------------------------
+    if (need_state && holds_state) {
+      const float egl = sm.EG[C - 1];
+#pragma unroll
+      for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st[nt][e] *= egl;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        const Frag a = a_from_acc(ut[kb]);
+        const int s0 = kb * 8 + 2 * t4;
+        const float f0 = sm.GL[s0], f1 = sm.GL[s0 + 1];
 #pragma unroll
         for (int nt = 0; nt < NTD; ++nt) {
-          uint32_t b0, b1;
-          ldb_k(sm.RU, LDD, k0, nt * 8, g, t4, b0, b1);
-          mma_tf32(qs[nt], a0, a1, a2, a3, b0, b1);
+          const uint32_t b0 = tf32(f0 * sm.Kh[s0 * LDD + nt * 8 + g]);
+          const uint32_t b1 = tf32(f1 * sm.Kh[(s0 + 1) * LDD + nt * 8 + g]);
+          mma(st[nt], a, b0, b1);
         }
       }
-      const int t0 = m0 + g, t1 = m0 + g + 8;
-#pragma unroll
-      for (int nt = 0; nt < NTD; ++nt) {
-        const int cc = nt * 8 + 2 * t4;
-        if (t0 < n) {
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(qs[nt][0], qs[nt][1]);
-          *reinterpret_cast<__nv_bfloat162*>(p.o + (static_cast<int64_t>(start + c0 + t0) * H + h) * D + cc) = v2;
-        }
-        if (t1 < n) {
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(qs[nt][2], qs[nt][3]);
-          *reinterpret_cast<__nv_bfloat162*>(p.o + (static_cast<int64_t>(start + c0 + t1) * H + h) * D + cc) = v2;
-        }
-      }
-    }
-    if (need_state) {
-      // warps 4-7 take row tiles 0..3 (all columns); then every warp takes half the
-      // columns of one of the remaining row tiles
-      if (warp >= 4) state_update<D, D / 8>(sm, (warp - 4) * 16, 0, g, t4);
-      __syncthreads();
-      for (int w = warp; w < (D / 16 - 4) * 2; w += NT / 32)
-        state_update<D, D / 16>(sm, (4 + (w >> 1)) * 16, (w & 1) * (D / 2), g, t4);
     }
     __syncthreads();
   }
 
   if (!BRANCH) {
-    for (int e = tid; e < D * D / 4; e += NT) {
-      const int r = e / (D / 4), c4 = (e % (D / 4)) * 4;
-      *reinterpret_cast<float4*>(p.S_P + state_base + static_cast<int64_t>(r) * D + c4) =
-          *reinterpret_cast<const float4*>(&sm.S[r * LDD + c4]);
-    }
+    if (holds_state) store_state(p.S_P, st);
     // conv windows: raw inputs of the last K-1 positions before the end / before m
-    for (int e = tid; e < (K - 1) * 3 * D; e += NT) {
+    for (int e = tid; e < (KW - 1) * 3 * D; e += NT) {
       const int i = e / (3 * D), s = (e / D) % 3, c = e % D;
-      const int64_t dst = ((static_cast<int64_t>(j * (K - 1) + i) * 3 + s) * H + h) * D + c;
-      p.conv_win[dst] = f2bf(raw(len - (K - 1) + i, s, c));
-      if (ck >= 0 && p.conv_ckpt) p.conv_ckpt[dst] = f2bf(raw(ck - pos0 - (K - 1) + i, s, c));
+      const int64_t dst = ((static_cast<int64_t>(j * (KW - 1) + i) * 3 + s) * H + h) * D + c;
+      p.conv_win[dst] = f2bf(raw(len - (KW - 1) + i, s, c));
+      if (ck >= 0 && p.conv_ckpt) p.conv_ckpt[dst] = f2bf(raw(ck - pos0 - (KW - 1) + i, s, c));
     }
   }
 }
