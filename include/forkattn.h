@@ -59,6 +59,8 @@ extern "C" {
                                    from segment-aligned tiles and chunks in a fixed order, so the
                                    flag is accepted and changes nothing. */
 #define FORK_CHECKS 0x2u        /* extra device-side consistency checks (status word) */
+#define FORK_WARP_MMA 0x4u      /* fork_attn only: run the warp-level mma.sync kernel instead of the
+                                   tcgen05 one (same results within rounding; for comparisons) */
 
 /* ------------------------------------------------------------------------
  * Metadata (Flide pages: onedev summary "무엇과 다른가" - per-token (j, c, t),

@@ -244,3 +244,14 @@ def test_pad_rows_untouched():
     for o in list(dr.attn_out.values()) + [dr.gdn_out]:
         assert torch.isnan(o[T:].float()).all()
         assert torch.isfinite(o[:T].float()).all()
+
+
+def test_warp_mma_variant_matches_oracle():
+    """The warp-level mma.sync attention kernel (FORK_WARP_MMA) against the oracle."""
+    torch = require_gpu()
+    from tree_forked_hybrid_gb300 import fork as F
+    rnd = wl.make_round(2)
+    dr = run_device(rnd, flags=F.FORK_WARP_MMA)
+    view = oracle_view(rnd)
+    for a in rnd.attn_shapes:
+        check_attention(rnd, dr, view, a.name)

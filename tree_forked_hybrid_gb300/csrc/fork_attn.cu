@@ -6,8 +6,11 @@
 // t * theta^(-2i/d).  Angles are formed in float64 on the device as
 // t = 64 a + b with two small tables of (cos, sin), combined in float32 by the
 // angle-addition formula.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "fork_attn.cuh"
 
@@ -84,6 +87,38 @@ __global__ void rope_keys_kernel(const int32_t* __restrict__ meta, MetaLayout L,
   }
 }
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link-time
+// dependency on the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor [rows][heads][d] read in boxes of {64 elements, box_heads, box_rows},
+// 128-byte swizzle, zero fill outside the tensor.
+static bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int box_heads,
+                     int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct AttnWs {
   size_t kr, pkr, hi, lo, total;
 };
@@ -115,7 +150,6 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
                          int32_t window, float rope_theta, float scale, const uint16_t* prefix_k,
                          const uint16_t* prefix_v, int32_t prefix_rows, void* workspace,
                          size_t ws_bytes, uint32_t flags, void* stream) {
-  (void)flags;
   MetaLayout L;
   int rc = check_meta(m, &L);
   if (rc != FORK_OK) return rc;
@@ -174,5 +208,15 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   if (cudaGetLastError() != cudaSuccess) return FORK_ECUDA;
   const int grid_x = static_cast<int>(std::min<int64_t>(
       L.max_work, (L.T_cap + m->tile_tokens - 1) / m->tile_tokens + L.max_seg));
-  return d == 64 ? launch_attn_mma<64>(p, grid_x, s) : launch_attn_mma<128>(p, grid_x, s);
+  if (flags & FORK_WARP_MMA)
+    return d == 64 ? launch_attn_mma<64>(p, grid_x, s) : launch_attn_mma<128>(p, grid_x, s);
+  alignas(128) CUtensorMap maps[5];
+  const uint16_t* pk = p.prefix_rows > 0 ? p.prefix_k : p.k;
+  const uint16_t* pv = p.prefix_rows > 0 ? p.prefix_v : p.v;
+  const int prow = p.prefix_rows > 0 ? p.prefix_rows : L.T_cap;
+  if (!make_map(&maps[0], q, d, Hq, L.T_cap, G, m->tile_tokens) ||
+      !make_map(&maps[1], p.k, d, Hkv, L.T_cap, 1, 128) || !make_map(&maps[2], v, d, Hkv, L.T_cap, 1, 128) ||
+      !make_map(&maps[3], pk, d, Hkv, prow, 1, 128) || !make_map(&maps[4], pv, d, Hkv, prow, 1, 128))
+    return FORK_ECUDA;
+  return d == 64 ? launch_attn_tc<64>(p, maps, grid_x, s) : launch_attn_tc<128>(p, maps, grid_x, s);
 }

@@ -1,6 +1,8 @@
 // Shared definitions of the fork-masked attention kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "fork_common.cuh"
 
 namespace fork {
@@ -44,5 +46,9 @@ __device__ __forceinline__ void rope_cs(const float2* hi, const float2* lo, int 
 
 template <int D>
 int launch_attn_mma(const AttnParams& p, int grid_x, cudaStream_t s);
+
+// maps: q, k, v, prefix k, prefix v (CUtensorMap, 128-byte aligned)
+template <int D>
+int launch_attn_tc(const AttnParams& p, const CUtensorMap* maps, int grid_x, cudaStream_t s);
 
 }  // namespace fork

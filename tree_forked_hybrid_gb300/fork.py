@@ -18,6 +18,7 @@ STATUS = {0: "FORK_OK", 1: "FORK_EINVAL", 2: "FORK_ECAPACITY", 3: "FORK_EUNSUPPO
 STATUS_BITS = {0x1: "BAD_DESC", 0x2: "CAPACITY", 0x4: "BAD_CKPT", 0x8: "TIMEOUT", 0x10: "BAD_PREFIX"}
 FORK_DETERMINISTIC = 0x1
 FORK_CHECKS = 0x2
+FORK_WARP_MMA = 0x4
 
 _lib = None
 
