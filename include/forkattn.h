@@ -146,6 +146,32 @@ int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k, const ui
               float scale, const uint16_t* prefix_k, const uint16_t* prefix_v, int32_t prefix_rows,
               void* workspace, size_t ws_bytes, uint32_t flags, void* stream);
 
+/* fork_attn for callers that cannot allocate device memory.  The Flide pages
+ * have no counterpart: this entry point exists for callers that hold only
+ * pointers to their inputs and outputs and may not allocate (for example a
+ * runtime that plans all device memory ahead and forbids allocation in its
+ * serving loop, because cudaMalloc and cudaFree synchronise the device).
+ * Arguments and results are those of fork_attn without the workspace: the
+ * scratch fork_attn needs (rotated keys, rotary tables) is taken from an array
+ * of FORK_NOALLOC_SCRATCH_BYTES bytes owned by the library, which every GPU
+ * that loads the library keeps allocated until the process exits.
+ *   - Returns FORK_ECAPACITY when fork_attn_workspace_bytes(T_cap,
+ *     prefix_rows, Hkv, d, rope_theta) exceeds FORK_NOALLOC_SCRATCH_BYTES
+ *     (e.g. T_cap = 16384 with Hkv = 4, d = 128 fits; T_cap = 32768 with
+ *     Hkv = 8 does not).
+ *   - Calls no allocating routine.  The first call on a device looks up the
+ *     array's device address (and loads the module there); make that first
+ *     call before any stream capture.
+ *   - Every call, on any stream, uses the same array and leaves its contents
+ *     behind.  Nothing in it has to start at zero (each call writes every
+ *     value it reads), but two calls that overlap on the GPU race on it:
+ *     order them on one stream or with events. */
+#define FORK_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int fork_attn_noalloc(const fork_meta* m, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      uint16_t* o, int32_t Hq, int32_t Hkv, int32_t d, int32_t window,
+                      float rope_theta, float scale, const uint16_t* prefix_k,
+                      const uint16_t* prefix_v, int32_t prefix_rows, uint32_t flags, void* stream);
+
 /* ------------------------------------------------------------------------
  * Gated DeltaNet, two calls (onedev "무엇과 다른가"; rainbus "前置知识" and
  * "方法步骤详情" step 2: the first call processes every trunk segment and

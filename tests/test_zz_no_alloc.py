@@ -1,0 +1,57 @@
+"""fork_attn_noalloc, the entry point for callers that may not allocate device memory.
+
+Such callers hold only pointers to their inputs and outputs; the variant takes
+its scratch from an array owned by the library.  Its output must match
+fork_attn's (which uses a caller workspace) within the parity tolerance, on
+two calls in a row (the second one finds the first one's scratch contents).
+This file is collected last so that a failure here does not stop the others.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from tests.gpu_util import ATOL_OUT, require_gpu
+from tree_forked_hybrid_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    torch = require_gpu()
+    from tree_forked_hybrid_gb300 import fork as F
+    from tree_forked_hybrid_gb300.runner import DeviceRound
+
+    rnd = wl.make_round(2)  # T_cap 16384, 16 q-heads / 4 kv-heads, d 128, full and sliding window
+    dr = DeviceRound(rnd)
+    dr.step_meta()
+    T = rnd.T
+    for call, a in enumerate(rnd.attn_shapes):  # two calls in a row: full, then window
+        inp = dr.inputs[a.name]
+        scale = 1.0 / math.sqrt(a.d)
+        need = F.fork_attn_workspace_bytes(rnd.T_cap, 0, a.Hkv, a.d, a.rope_theta)
+        assert 0 < need <= F.FORK_NOALLOC_SCRATCH_BYTES
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        ref = torch.zeros((rnd.T_cap, a.Hq, a.d), dtype=torch.bfloat16, device="cuda")
+        got = torch.zeros_like(ref)
+        F.fork_attn(dr.meta, inp["q"], inp["k"], inp["v"], ref, a.Hq, a.Hkv, a.d, a.window, a.rope_theta,
+                    scale, None, None, ws)
+        F.fork_attn_noalloc(dr.meta, inp["q"], inp["k"], inp["v"], got, a.Hq, a.Hkv, a.d, a.window,
+                            a.rope_theta, scale)
+        torch.cuda.synchronize()
+        assert F.fork_read_status(dr.meta) == 0
+        r = ref[:T].float().cpu().numpy()
+        g = got[:T].float().cpu().numpy()
+        assert np.isfinite(g).all()
+        assert np.abs(g - r).max() <= ATOL_OUT, f"call {call}: max |delta| {np.abs(g - r).max():.3e}"
+
+
+def test_noalloc_rejects_rounds_beyond_its_scratch():
+    require_gpu()
+    from tree_forked_hybrid_gb300 import fork as F
+    meta = F.Meta(32768, 4, 80, 32)  # long-document capacity: 32768 x 8 kv-heads x 128 needs 64 MiB
+    import torch
+    x = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(F.ForkError) as e:
+        F.fork_attn_noalloc(meta, x, x, x, x, 32, 8, 128, 0, 10000.0, 0.088)
+    assert e.value.code == 2  # FORK_ECAPACITY

@@ -220,3 +220,55 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     return FORK_ECUDA;
   return d == 64 ? launch_attn_tc<64>(p, maps, grid_x, s) : launch_attn_tc<128>(p, maps, grid_x, s);
 }
+
+// ---- fork_attn_noalloc: fork_attn with the library's own scratch area -------------
+//
+// Some callers cannot allocate device memory at all: they only hold pointers to
+// their inputs and outputs (for example a host runtime that plans every device
+// buffer up front and forbids allocation inside its serving loop, since
+// cudaMalloc and cudaFree synchronise the device).  For them the scratch that
+// fork_attn needs (rotated keys and rotary tables) lives in this file-scope
+// device array instead of a caller workspace.  The module that holds it is loaded
+// on each GPU that uses the library, and the array stays allocated there until
+// the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FORK_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};  // device address of the array, per device
+}  // namespace
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once per
+// device with that device current (this also loads the module on that device).
+static int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FORK_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FORK_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FORK_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return FORK_OK;
+}
+
+extern "C" int fork_attn_noalloc(const fork_meta* m, const uint16_t* q, const uint16_t* k,
+                                 const uint16_t* v, uint16_t* o, int32_t Hq, int32_t Hkv, int32_t d,
+                                 int32_t window, float rope_theta, float scale,
+                                 const uint16_t* prefix_k, const uint16_t* prefix_v,
+                                 int32_t prefix_rows, uint32_t flags, void* stream) {
+  MetaLayout L;
+  int rc = check_meta(m, &L);
+  if (rc != FORK_OK) return rc;
+  if (prefix_rows < 0 || Hkv < 1 || (d != 64 && d != 128)) return FORK_EINVAL;
+  const size_t need = fork_attn_workspace_bytes(L.T_cap, prefix_rows, Hkv, d, rope_theta);
+  if (need > FORK_NOALLOC_SCRATCH_BYTES) return FORK_ECAPACITY;
+  void* scratch = nullptr;
+  if (need > 0 && (rc = noalloc_scratch(&scratch)) != FORK_OK) return rc;
+  return fork_attn(m, q, k, v, o, Hq, Hkv, d, window, rope_theta, scale, prefix_k, prefix_v, prefix_rows,
+                   scratch, need > 0 ? FORK_NOALLOC_SCRATCH_BYTES : 0, flags, stream);
+}

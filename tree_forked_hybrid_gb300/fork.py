@@ -19,6 +19,7 @@ STATUS_BITS = {0x1: "BAD_DESC", 0x2: "CAPACITY", 0x4: "BAD_CKPT", 0x8: "TIMEOUT"
 FORK_DETERMINISTIC = 0x1
 FORK_CHECKS = 0x2
 FORK_WARP_MMA = 0x4
+FORK_NOALLOC_SCRATCH_BYTES = 32 << 20  # size of the library's scratch array (include/forkattn.h)
 
 _lib = None
 
@@ -57,6 +58,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fork_attn_workspace_bytes": (sz, [i32, i32, i32, i32, f32]),
         "fork_attn": (ctypes.c_int, [MP, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, vp, vp, i32, vp,
                                      sz, u32, vp]),
+        "fork_attn_noalloc": (ctypes.c_int, [MP, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, vp, vp, i32,
+                                             u32, vp]),
         "fork_gdn_trunk": (ctypes.c_int, [MP, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                           vp, vp, vp, u32, vp]),
         "fork_gdn_branches": (ctypes.c_int, [MP, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
@@ -136,6 +139,15 @@ def fork_attn(meta: Meta, q, k, v, o, Hq: int, Hkv: int, d: int, window: int, ro
     _check("fork_attn", load().fork_attn(meta.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(o), Hq, Hkv, d, window,
                                          rope_theta, scale, _ptr(prefix_k), _ptr(prefix_v), prefix_rows,
                                          _ptr(workspace), ws_bytes, flags, _stream(stream)))
+
+
+def fork_attn_noalloc(meta: Meta, q, k, v, o, Hq: int, Hkv: int, d: int, window: int, rope_theta: float,
+                      scale: float, prefix_k=None, prefix_v=None, flags: int = 0, stream=None):
+    """fork_attn without a workspace argument (the library's own scratch array)."""
+    prefix_rows = 0 if prefix_k is None else int(prefix_k.shape[0])
+    _check("fork_attn_noalloc", load().fork_attn_noalloc(
+        meta.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(o), Hq, Hkv, d, window, rope_theta, scale,
+        _ptr(prefix_k), _ptr(prefix_v), prefix_rows, flags, _stream(stream)))
 
 
 def fork_gdn_trunk(meta: Meta, q, k, v, alpha, eta, conv_w, H: int, d: int, K: int, chunk: int,
