@@ -59,8 +59,9 @@ extern "C" {
                                    from segment-aligned tiles and chunks in a fixed order, so the
                                    flag is accepted and changes nothing. */
 #define FORK_CHECKS 0x2u        /* extra device-side consistency checks (status word) */
-#define FORK_WARP_MMA 0x4u      /* fork_attn only: run the warp-level mma.sync kernel instead of the
-                                   tcgen05 one (same results within rounding; for comparisons) */
+#define FORK_WARP_MMA 0x4u      /* fork_attn, fork_gdn_*: run the warp-level mma.sync kernels instead
+                                   of the tcgen05 ones (same results within rounding; for
+                                   comparisons; d = 64 GDN always uses them) */
 
 /* ------------------------------------------------------------------------
  * Metadata (Flide pages: onedev summary "무엇과 다른가" - per-token (j, c, t),
@@ -124,10 +125,10 @@ int fork_read_status(const fork_meta* m, int32_t* h_status, void* stream);
  * rotary positions they would have alone).
  * ------------------------------------------------------------------------ */
 
-/* Workspace bytes fork_attn needs: rotated keys for the stream and the prefix
- * rows (0 when rope_theta == 0). */
-size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hkv, int32_t d,
-                                 float rope_theta);
+/* Workspace bytes fork_attn needs: rotated queries and keys of the stream,
+ * rotated prefix keys and two small rotary tables (0 when rope_theta == 0). */
+size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq, int32_t Hkv,
+                                 int32_t d, float rope_theta);
 
 /* o_x = sum_y softmax_y(<R(q_x,t_x), R(k_y,t_y)> * scale) v_y over visible y.
  *   q [T_cap, Hq, d], k and v [T_cap, Hkv, d] bf16 (stream rows; pad rows
@@ -156,9 +157,9 @@ int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k, const ui
  * of FORK_NOALLOC_SCRATCH_BYTES bytes owned by the library, which every GPU
  * that loads the library keeps allocated until the process exits.
  *   - Returns FORK_ECAPACITY when fork_attn_workspace_bytes(T_cap,
- *     prefix_rows, Hkv, d, rope_theta) exceeds FORK_NOALLOC_SCRATCH_BYTES
- *     (e.g. T_cap = 16384 with Hkv = 4, d = 128 fits; T_cap = 32768 with
- *     Hkv = 8 does not).
+ *     prefix_rows, Hq, Hkv, d, rope_theta) exceeds FORK_NOALLOC_SCRATCH_BYTES
+ *     (e.g. T_cap = 4096 with 16 q-heads, 4 kv-heads, d = 128 fits;
+ *     T_cap = 16384 with the same heads does not).
  *   - Calls no allocating routine.  The first call on a device looks up the
  *     array's device address (and loads the module there); make that first
  *     call before any stream capture.

@@ -22,14 +22,19 @@ def test_noalloc_matches_workspace_entry_point_twice():
     from tree_forked_hybrid_gb300 import fork as F
     from tree_forked_hybrid_gb300.runner import DeviceRound
 
-    rnd = wl.make_round(2)  # T_cap 16384, 16 q-heads / 4 kv-heads, d 128, full and sliding window
+    # 16 q-heads / 4 kv-heads, d 128, full and sliding window, T_cap 4096 (fits the scratch array)
+    a = wl.AttnShape("attn", 16, 4, 128, 0, 10000.0)
+    s = wl.AttnShape("swa", 16, 4, 128, 512, 10000.0)
+    g = wl.GdnShape("gdn", 2, 64, 64, 4, 64)
+    rnd = wl.custom_round([700, 1300, 5], [3, 2, 1], [40, 12, 64, 33, 1, 9], attn_shapes=(a, s), gdn_shape=g,
+                          T_cap=4096, seed=21)
     dr = DeviceRound(rnd)
     dr.step_meta()
     T = rnd.T
     for call, a in enumerate(rnd.attn_shapes):  # two calls in a row: full, then window
         inp = dr.inputs[a.name]
         scale = 1.0 / math.sqrt(a.d)
-        need = F.fork_attn_workspace_bytes(rnd.T_cap, 0, a.Hkv, a.d, a.rope_theta)
+        need = F.fork_attn_workspace_bytes(rnd.T_cap, 0, a.Hq, a.Hkv, a.d, a.rope_theta)
         assert 0 < need <= F.FORK_NOALLOC_SCRATCH_BYTES
         ws = torch.empty(need, dtype=torch.uint8, device="cuda")
         ref = torch.zeros((rnd.T_cap, a.Hq, a.d), dtype=torch.bfloat16, device="cuda")
@@ -49,7 +54,7 @@ def test_noalloc_matches_workspace_entry_point_twice():
 def test_noalloc_rejects_rounds_beyond_its_scratch():
     require_gpu()
     from tree_forked_hybrid_gb300 import fork as F
-    meta = F.Meta(32768, 4, 80, 32)  # long-document capacity: 32768 x 8 kv-heads x 128 needs 64 MiB
+    meta = F.Meta(32768, 4, 80, 32)  # long-document capacity: needs 320 MiB of scratch
     import torch
     x = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(F.ForkError) as e:

@@ -27,7 +27,7 @@ __global__ void rope_tables_kernel(float2* hi, int hi_rows, float2* lo, int half
     const int64_t e = is_hi ? idx : idx - n_hi;
     const int i = static_cast<int>(e % half);
     const int64_t t = is_hi ? (e / half) * 64 : e / half;
-    const double f = pow(theta, -2.0 * i / (2.0 * half));
+    const double f = exp2(-2.0 * i / (2.0 * half) * log2(theta));
     const double ang = static_cast<double>(t) * f;
     double sn, cs;
     sincos(ang, &sn, &cs);
@@ -36,10 +36,11 @@ __global__ void rope_tables_kernel(float2* hi, int hi_rows, float2* lo, int half
   }
 }
 
-// Rotate every key row of the stream (position from the metadata) and of the
-// prefix (position = row index inside its request's prefix).
+// Rotate every row of a stream tensor [T_cap, heads, D] (position from the
+// metadata) and of a prefix tensor [prefix_rows, heads, D] (position = row
+// index inside its request's prefix) into the workspace.
 template <int D>
-__global__ void rope_keys_kernel(const int32_t* __restrict__ meta, MetaLayout L,
+__global__ void rope_rows_kernel(const int32_t* __restrict__ meta, MetaLayout L,
                                  const uint16_t* __restrict__ k, const uint16_t* __restrict__ pk,
                                  uint16_t* __restrict__ kr, uint16_t* __restrict__ pkr,
                                  int prefix_rows, int Hkv, const float2* __restrict__ hi,
@@ -120,13 +121,14 @@ static bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t
 }
 
 struct AttnWs {
-  size_t kr, pkr, hi, lo, total;
+  size_t qr, kr, pkr, hi, lo, total;
 };
 
-static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hkv, int64_t d) {
+static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hkv, int64_t d) {
   AttnWs w;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  w.kr = 0;
+  w.qr = 0;
+  w.kr = al(w.qr + static_cast<size_t>(T_cap) * Hq * d * 2);
   w.pkr = al(w.kr + static_cast<size_t>(T_cap) * Hkv * d * 2);
   w.hi = al(w.pkr + static_cast<size_t>(prefix_rows) * Hkv * d * 2);
   w.lo = al(w.hi + static_cast<size_t>(rope_hi_rows(T_cap + prefix_rows)) * (d / 2) * 8);
@@ -138,11 +140,11 @@ static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hkv, int64_t d
 
 using namespace fork;
 
-extern "C" size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hkv,
-                                            int32_t d, float rope_theta) {
-  if (T_cap < 1 || prefix_rows < 0 || Hkv < 1 || (d != 64 && d != 128)) return 0;
+extern "C" size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq,
+                                            int32_t Hkv, int32_t d, float rope_theta) {
+  if (T_cap < 1 || prefix_rows < 0 || Hkv < 1 || Hq < Hkv || (d != 64 && d != 128)) return 0;
   if (rope_theta == 0.f) return 0;
-  return attn_ws(T_cap, prefix_rows, Hkv, d).total;
+  return attn_ws(T_cap, prefix_rows, Hq, Hkv, d).total;
 }
 
 extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k,
@@ -186,24 +188,31 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   p.scale_log2 = scale * 1.4426950408889634f;
 
   if (rope_theta != 0.f) {
-    const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hkv, d);
+    const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hq, Hkv, d);
     if (!workspace || ws_bytes < w.total || !is_aligned16(workspace)) return FORK_EINVAL;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
+    uint16_t* qr = reinterpret_cast<uint16_t*>(ws + w.qr);
     uint16_t* kr = reinterpret_cast<uint16_t*>(ws + w.kr);
     uint16_t* pkr = reinterpret_cast<uint16_t*>(ws + w.pkr);
     float2* hi = reinterpret_cast<float2*>(ws + w.hi);
     float2* lo = reinterpret_cast<float2*>(ws + w.lo);
     const int hi_rows = static_cast<int>(rope_hi_rows(static_cast<int64_t>(L.T_cap) + prefix_rows));
-    rope_tables_kernel<<<64, 256, 0, s>>>(hi, hi_rows, lo, d / 2, static_cast<double>(rope_theta));
-    const int blocks = 4 * 152;
-    if (d == 64)
-      rope_keys_kernel<64><<<blocks, 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows, Hkv, hi, lo, hi_rows);
-    else
-      rope_keys_kernel<128><<<blocks, 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows, Hkv, hi, lo, hi_rows);
+    rope_tables_kernel<<<2 * 152, 128, 0, s>>>(hi, hi_rows, lo, d / 2, static_cast<double>(rope_theta));
+    const int blocks = 8 * 152;
+    // keys of the stream and of the prefix, then the queries of the stream
+    if (d == 64) {
+      rope_rows_kernel<64><<<blocks, 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows, Hkv, hi, lo, hi_rows);
+      rope_rows_kernel<64><<<blocks, 256, 0, s>>>(p.meta, L, q, nullptr, qr, nullptr, 0, Hq, hi, lo, hi_rows);
+    } else {
+      rope_rows_kernel<128><<<blocks, 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows, Hkv, hi, lo, hi_rows);
+      rope_rows_kernel<128><<<blocks, 256, 0, s>>>(p.meta, L, q, nullptr, qr, nullptr, 0, Hq, hi, lo, hi_rows);
+    }
+    p.q = qr;
     p.k = kr;
     p.prefix_k = pkr;
     p.rope_hi = hi;
     p.rope_lo = lo;
+    p.rope_theta = 0.f;  // queries are already rotated
   }
   if (cudaGetLastError() != cudaSuccess) return FORK_ECUDA;
   const int grid_x = static_cast<int>(std::min<int64_t>(
@@ -214,7 +223,7 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   const uint16_t* pk = p.prefix_rows > 0 ? p.prefix_k : p.k;
   const uint16_t* pv = p.prefix_rows > 0 ? p.prefix_v : p.v;
   const int prow = p.prefix_rows > 0 ? p.prefix_rows : L.T_cap;
-  if (!make_map(&maps[0], q, d, Hq, L.T_cap, G, m->tile_tokens) ||
+  if (!make_map(&maps[0], p.q, d, Hq, L.T_cap, G, m->tile_tokens) ||
       !make_map(&maps[1], p.k, d, Hkv, L.T_cap, 1, 128) || !make_map(&maps[2], v, d, Hkv, L.T_cap, 1, 128) ||
       !make_map(&maps[3], pk, d, Hkv, prow, 1, 128) || !make_map(&maps[4], pv, d, Hkv, prow, 1, 128))
     return FORK_ECUDA;
@@ -265,7 +274,7 @@ extern "C" int fork_attn_noalloc(const fork_meta* m, const uint16_t* q, const ui
   int rc = check_meta(m, &L);
   if (rc != FORK_OK) return rc;
   if (prefix_rows < 0 || Hkv < 1 || (d != 64 && d != 128)) return FORK_EINVAL;
-  const size_t need = fork_attn_workspace_bytes(L.T_cap, prefix_rows, Hkv, d, rope_theta);
+  const size_t need = fork_attn_workspace_bytes(L.T_cap, prefix_rows, Hq, Hkv, d, rope_theta);
   if (need > FORK_NOALLOC_SCRATCH_BYTES) return FORK_ECAPACITY;
   void* scratch = nullptr;
   if (need > 0 && (rc = noalloc_scratch(&scratch)) != FORK_OK) return rc;

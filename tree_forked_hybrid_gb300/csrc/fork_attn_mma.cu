@@ -172,20 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   cp_async_wait<0>();
   __syncthreads();
 
-  // rotary embedding of the query tile at the isolated positions
-  if (p.rope_theta != 0.f) {
-    for (int idx = tid; idx < kRows * (D / 2); idx += kThreads) {
-      const int r = idx / (D / 2), i = idx % (D / 2);
-      const int tpos = tx_min + r / G;
-      float cs, sn;
-      rope_cs(p.rope_hi, p.rope_lo, D / 2, tpos, i, &cs, &sn);
-      const float a = bf2f(sm.q[r * LD + i]), b = bf2f(sm.q[r * LD + i + D / 2]);
-      sm.q[r * LD + i] = f2bf(a * cs - b * sn);
-      sm.q[r * LD + i + D / 2] = f2bf(b * cs + a * sn);
-    }
-    __syncthreads();
-  }
-
   // Q fragments of this warp's 16 rows
   uint32_t qf[D / 16][4];
   {

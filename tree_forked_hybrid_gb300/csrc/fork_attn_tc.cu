@@ -48,12 +48,19 @@ struct TcLayout {
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);  // one CTA per SM
 };
 
-enum Bar { B_QFULL = 0, B_QREADY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_SFULL0, B_SFULL1,
+enum Bar { B_QFULL = 0, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_SFULL0, B_SFULL1,
            B_SFREE0, B_SFREE1, B_PFULL, B_ODONE, B_FIN, B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x on the SFU (flush-to-zero; 2^-inf = 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // byte offset of element e (0 <= e < D) of row r inside a [128 x D] K-major
@@ -69,9 +76,7 @@ struct TcParams {
   const int32_t* meta;
   MetaLayout L;
   uint16_t* o;
-  const float2* rope_hi;
-  const float2* rope_lo;
-  int Hq, Hkv, G, prefix_rows, window, rope;
+  int Hq, Hkv, G, prefix_rows, window;
   float scale_log2;
 };
 
@@ -105,41 +110,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tx_min = seg_pos0 + off;
   const int tx_max = seg_pos0 + off + n - 1;
 
-  // ---- key ranges (prefix rows, trunk, own branch) ------------------------------
-  int r_row0[3], r_len[3], r_pos0[3], r_pref[3], lo[3], cnt[3];
-  int nr = 0, total = 0;
+  // ---- key ranges in fixed slots: 0 prefix rows, 1 trunk, 2 own branch --------------
+  // (an absent range has length 0; fixed slots keep every range variable in registers)
   const int pl = meta[L.req_prefix_len + j];
-  if (pl > 0) {
-    const int poff = meta[L.req_prefix_off + j];
-    if (poff + pl > p.prefix_rows) {
-      if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
-      return;
-    }
-    r_row0[nr] = poff; r_len[nr] = pl; r_pos0[nr] = 0; r_pref[nr] = 1; ++nr;
+  const int poff = pl > 0 ? meta[L.req_prefix_off + j] : 0;
+  if (pl > 0 && poff + pl > p.prefix_rows) {
+    if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
+    return;
   }
-  r_row0[nr] = meta[L.seg_trunk_start + s]; r_len[nr] = meta[L.seg_trunk_len + s]; r_pos0[nr] = pl;
-  r_pref[nr] = 0; ++nr;
-  if (c > 0) { r_row0[nr] = seg_start; r_len[nr] = seg_len; r_pos0[nr] = seg_pos0; r_pref[nr] = 0; ++nr; }
-#pragma unroll
-  for (int r = 0; r < 3; ++r) {
-    lo[r] = 0;
-    cnt[r] = 0;
-    if (r < nr) {
-      const int umax = min(r_len[r] - 1, tx_max - r_pos0[r]);
-      const int umin = p.window > 0 ? max(0, tx_min - p.window + 1 - r_pos0[r]) : 0;
-      if (umax >= umin) {
-        lo[r] = umin / kKeys;
-        cnt[r] = umax / kKeys - lo[r] + 1;
-      }
+  const int r_row0_0 = poff, r_len_0 = pl, r_pos0_0 = 0;
+  const int r_row0_1 = meta[L.seg_trunk_start + s], r_len_1 = meta[L.seg_trunk_len + s], r_pos0_1 = pl;
+  const int r_row0_2 = seg_start, r_len_2 = c > 0 ? seg_len : 0, r_pos0_2 = seg_pos0;
+  auto tiles = [&](int len, int pos0, int& lo_t, int& cnt_t) {
+    lo_t = 0;
+    cnt_t = 0;
+    if (len <= 0) return;
+    const int umax = min(len - 1, tx_max - pos0);
+    const int umin = p.window > 0 ? max(0, tx_min - p.window + 1 - pos0) : 0;
+    if (umax >= umin) {
+      lo_t = umin / kKeys;
+      cnt_t = umax / kKeys - lo_t + 1;
     }
-    total += cnt[r];
-  }
+  };
+  int lo0, cnt0, lo1, cnt1, lo2, cnt2;
+  tiles(r_len_0, r_pos0_0, lo0, cnt0);
+  tiles(r_len_1, r_pos0_1, lo1, cnt1);
+  tiles(r_len_2, r_pos0_2, lo2, cnt2);
+  const int total = cnt0 + cnt1 + cnt2;
   if (total == 0) return;  // cannot happen for a valid tile (a token sees itself)
-  // flat key-tile index f -> (range, tile)
-  auto key_tile = [&](int f, int& r, int& t) {
-    r = 0;
-    if (f >= cnt[0]) { f -= cnt[0]; r = 1; if (f >= cnt[1]) { f -= cnt[1]; r = 2; } }
-    t = lo[r] + f;
+  // flat key-tile index f -> range slot r, first key row, length, first position, tile t
+  struct KT {
+    int r, row0, len, pos0, t;
+  };
+  auto key_tile = [&](int f) -> KT {
+    if (f < cnt0) return {0, r_row0_0, r_len_0, r_pos0_0, lo0 + f};
+    f -= cnt0;
+    if (f < cnt1) return {1, r_row0_1, r_len_1, r_pos0_1, lo1 + f};
+    f -= cnt1;
+    return {2, r_row0_2, r_len_2, r_pos0_2, lo2 + f};
   };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR);
@@ -149,7 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     tc::mbar_init(&bars[B_QFULL], 1);
-    tc::mbar_init(&bars[B_QREADY], 128);
     tc::mbar_init(&bars[B_KVFULL0], 1);
     tc::mbar_init(&bars[B_KVFULL1], 1);
     tc::mbar_init(&bars[B_KVEMPTY0], 1);
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_s[2] = {tmem, tmem + 128};
+  auto tm_s = [&](int st) -> uint32_t { return tmem + static_cast<uint32_t>(st) * 128u; };
   const uint32_t tm_o = tmem + 256;
   unsigned char* sQ = smem + LY::Q;
   unsigned char* sK = smem + LY::K;
@@ -195,11 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int f = 0; f < total; ++f) {
         const int st = f & 1;
         if (f >= 2 && !tc::mbar_wait(&bars[B_KVEMPTY0 + st], ((f >> 1) - 1) & 1, abort)) break;
-        int r, t;
-        key_tile(f, r, t);
-        const CUtensorMap* km = r_pref[r] ? &pkmap : &kmap;
-        const CUtensorMap* vm = r_pref[r] ? &pvmap : &vmap;
-        const int row = r_row0[r] + t * kKeys;
+        const KT kt = key_tile(f);
+        const CUtensorMap* km = kt.r == 0 ? &pkmap : &kmap;
+        const CUtensorMap* vm = kt.r == 0 ? &pvmap : &vmap;
+        const int row = kt.row0 + kt.t * kKeys;
         tc::mbar_expect_tx(&bars[B_KVFULL0 + st], 2 * NB * kBox);
         for (int b = 0; b < NB; ++b) {
           tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KVFULL0 + st], b * 64, g, row);
@@ -218,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, 0, 1);
       const uint32_t q_addr = tc::smem_u32(sQ), k_addr = tc::smem_u32(sK), v_addr = tc::smem_u32(sV),
                      p_addr = tc::smem_u32(sP);
-      bool ok = tc::mbar_wait(&bars[p.rope ? B_QREADY : B_QFULL], 0, abort);
+      bool ok = tc::mbar_wait(&bars[B_QFULL], 0, abort);
       auto issue_pv = [&](int f) {
         const int st = f & 1;
         for (int step = 0; step < kKeys / 16; ++step) {
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) {
             const uint64_t a = tc::sdesc_sw128(q_addr + b * kBox + k * 32, 16, 1024);
             const uint64_t bd = tc::sdesc_sw128(k_addr + (st * NB + b) * kBox + k * 32, 16, 1024);
-            tc::mma_bf16(tm_s[st], a, bd, idesc_qk, (b | k) ? 1u : 0u);
+            tc::mma_bf16(tm_s(st), a, bd, idesc_qk, (b | k) ? 1u : 0u);
           }
         tc::mma_commit(&bars[B_SFULL0 + st]);
         if (f >= 1) {
@@ -262,22 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tx = tx_min + tok;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok = true;
-    if (p.rope) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_QFULL], 0, abort));
-      if (ok) {
-        for (int i = 0; i < D / 2; ++i) {
-          float cs, sn;
-          rope_cs(p.rope_hi, p.rope_lo, D / 2, tx, i, &cs, &sn);
-          uint16_t* a = reinterpret_cast<uint16_t*>(sQ + sw128_off(row, i));
-          uint16_t* b = reinterpret_cast<uint16_t*>(sQ + sw128_off(row, i + D / 2));
-          const float x0 = bf2f(*a), x1 = bf2f(*b);
-          *a = f2bf(x0 * cs - x1 * sn);
-          *b = f2bf(x1 * cs + x0 * sn);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&bars[B_QREADY]);
-    }
     float m_used = -INFINITY, l = 0.f;
     const float sl2 = p.scale_log2;
     for (int f = 0; ok && f < total; ++f) {
@@ -289,46 +279,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t rawv[kKeys];
 #pragma unroll
-        for (int i = 0; i < kKeys / 32; ++i) tc::tmem_ld32(tm_s[st] + lane_base + i * 32, rawv + i * 32);
+        for (int i = 0; i < kKeys / 32; ++i) tc::tmem_ld32(tm_s(st) + lane_base + i * 32, rawv + i * 32);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int cc = 0; cc < kKeys; ++cc) sv[cc] = __uint_as_float(rawv[cc]);
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&bars[B_SFREE0 + st]);
-      int r, t;
-      key_tile(f, r, t);
-      const int u0 = t * kKeys;
-      const int len = r_len[r], p0 = r_pos0[r];
+      const KT kt = key_tile(f);
+      const int u0 = kt.t * kKeys;
+      const int len = kt.len, p0 = kt.pos0;
       const bool need_mask = (u0 + kKeys > len) || (p0 + u0 + kKeys - 1 > tx_min) ||
                              (p.window > 0 && tx_max - (p0 + u0) >= p.window);
-      float mt = -INFINITY;
       if (need_mask) {
+        // key u0+cc visible iff inside the range, not after the query, inside the window
+        const int lim_len = len - u0;          // cc < lim_len
+        const int lim_causal = tx - p0 - u0;   // cc <= lim_causal
+        const int lim_win = p.window > 0 ? tx - p0 - u0 - p.window : -0x40000000;  // cc > lim_win
 #pragma unroll
-        for (int cc = 0; cc < kKeys; ++cc) {
-          const int ku = u0 + cc, ty = p0 + ku;
-          const bool vis = ku < len && ty <= tx && (p.window == 0 || tx - ty < p.window);
-          sv[cc] = vis ? sv[cc] * sl2 : -INFINITY;
-          mt = fmaxf(mt, sv[cc]);
-        }
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < kKeys; ++cc) {
-          sv[cc] *= sl2;
-          mt = fmaxf(mt, sv[cc]);
-        }
+        for (int cc = 0; cc < kKeys; ++cc)
+          if (cc >= lim_len || cc > lim_causal || cc <= lim_win) sv[cc] = -INFINITY;
       }
+      // row maximum (raw scores; the scale is positive)
+      float mx[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx[e] = sv[e];
+#pragma unroll
+      for (int cc = 8; cc < kKeys; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], sv[cc]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
       const bool resc = mt > m_used + kRescale;
       const float m_new = resc ? mt : m_used;
       const float base = (m_new == -INFINITY) ? 0.f : m_new;
       const float factor = resc ? exp2f(m_used - base) : 1.f;  // 0 when nothing was accumulated
-      // probabilities (bf16) written as this row of the K-major SW128 P tile
-      float rs = 0.f;
+      // p = 2^(s*scale*log2e - base), summed with independent partial sums
+      float ps[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ps[e] = 0.f;
 #pragma unroll
       for (int cc = 0; cc < kKeys; ++cc) {
-        sv[cc] = exp2f(sv[cc] - base);
-        rs += sv[cc];
+        sv[cc] = fast_exp2(fmaf(sv[cc], sl2, -base));
+        ps[cc & 7] += sv[cc];
       }
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * factor + rs;
       m_used = m_new;
       if (f >= 1) {
@@ -418,14 +411,11 @@ int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, cud
   p.meta = a.meta;
   p.L = a.L;
   p.o = a.o;
-  p.rope_hi = a.rope_hi;
-  p.rope_lo = a.rope_lo;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.G = a.G;
   p.prefix_rows = a.prefix_rows;
   p.window = a.window;
-  p.rope = a.rope_theta != 0.f ? 1 : 0;
   p.scale_log2 = a.scale_log2;
   dim3 grid(grid_x, a.Hkv);
   attn_tc_kernel<D><<<grid, kThreads, LY::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);

@@ -55,7 +55,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fork_meta_init": (ctypes.c_int, [MP, vp, sz, i32, i32, i32, i32]),
         "fork_build_meta": (ctypes.c_int, [MP, vp, i32, i32, u32, vp]),
         "fork_read_status": (ctypes.c_int, [MP, ctypes.POINTER(i32), vp]),
-        "fork_attn_workspace_bytes": (sz, [i32, i32, i32, i32, f32]),
+        "fork_attn_workspace_bytes": (sz, [i32, i32, i32, i32, i32, f32]),
         "fork_attn": (ctypes.c_int, [MP, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, vp, vp, i32, vp,
                                      sz, u32, vp]),
         "fork_attn_noalloc": (ctypes.c_int, [MP, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, vp, vp, i32,
@@ -128,8 +128,8 @@ def fork_read_status(meta: Meta, stream=None) -> int:
     return out.value
 
 
-def fork_attn_workspace_bytes(T_cap: int, prefix_rows: int, Hkv: int, d: int, rope_theta: float) -> int:
-    return load().fork_attn_workspace_bytes(T_cap, prefix_rows, Hkv, d, rope_theta)
+def fork_attn_workspace_bytes(T_cap: int, prefix_rows: int, Hq: int, Hkv: int, d: int, rope_theta: float) -> int:
+    return load().fork_attn_workspace_bytes(T_cap, prefix_rows, Hq, Hkv, d, rope_theta)
 
 
 def fork_attn(meta: Meta, q, k, v, o, Hq: int, Hkv: int, d: int, window: int, rope_theta: float,

@@ -68,7 +68,7 @@ class DeviceRound:
                          for a in rnd.attn_shapes}
         self.attn_ws = {}
         for a in rnd.attn_shapes:
-            nb = F.fork_attn_workspace_bytes(T_cap, self.prefix_rows, a.Hkv, a.d, a.rope_theta)
+            nb = F.fork_attn_workspace_bytes(T_cap, self.prefix_rows, a.Hq, a.Hkv, a.d, a.rope_theta)
             self.attn_ws[a.name] = torch.empty(max(nb, 16), dtype=torch.uint8, device=device) if nb else None
         g = rnd.gdn_shape
         if g.dk != g.dv:
@@ -135,5 +135,5 @@ class DeviceRound:
     def launches_per_round(self) -> int:
         n = 2  # metadata: tables + tokens
         for a in self.rnd.attn_shapes:
-            n += 3 if a.rope_theta else 1  # rotary tables + keys + attention
+            n += 4 if a.rope_theta else 1  # rotary tables + keys + queries + attention
         return n + 3  # gdn trunk, gdn branches, readout
