@@ -23,28 +23,11 @@
 // T = (I + A)^{-1} is formed by blocked forward substitution in float32.
 // Chunks are aligned to the segment start, so a question's result never
 // depends on the rest of the round.
-#include "fork_common.cuh"
+#include "fork_gdn.cuh"
 
 namespace fork {
 
-struct GdnParams {
-  const int32_t* meta;
-  MetaLayout L;
-  const uint16_t* q;
-  const uint16_t* k;
-  const uint16_t* v;
-  const float* alpha;
-  const float* eta;
-  const float* conv_w;      // [3, H, D, K]
-  int H, K;
-  const float* state_in;    // trunk: init_state (resume) or null; branch: S_P
-  const uint16_t* hist_in;  // trunk: init_conv or null; branch: conv_win
-  float* S_P;               // trunk output
-  uint16_t* conv_win;       // trunk output
-  float* S_ckpt;
-  uint16_t* conv_ckpt;
-  uint16_t* o;
-};
+
 
 namespace {
 constexpr int C = 64;         // chunk length
@@ -545,7 +528,6 @@ extern "C" int fork_gdn_trunk(const fork_meta* m, const uint16_t* q, const uint1
                               const float* init_state, const uint16_t* init_conv, float* S_P,
                               uint16_t* conv_win, float* S_ckpt, uint16_t* conv_ckpt, uint16_t* o,
                               uint32_t flags, void* stream) {
-  (void)flags;
   MetaLayout L;
   int rc = gdn_common_checks(m, &L, q, k, v, alpha, eta, conv_w, H, d, K, chunk, o);
   if (rc != FORK_OK) return rc;
@@ -573,6 +555,7 @@ extern "C" int fork_gdn_trunk(const fork_meta* m, const uint16_t* q, const uint1
   p.conv_ckpt = conv_ckpt;
   p.o = o;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128 && !(flags & FORK_WARP_MMA)) return launch_gdn_tc(p, false, m->max_req, s);
   return d == 64 ? launch_gdn<64, false>(p, m->max_req, s) : launch_gdn<128, false>(p, m->max_req, s);
 }
 
@@ -581,7 +564,6 @@ extern "C" int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const ui
                                  const float* conv_w, int32_t H, int32_t d, int32_t K,
                                  int32_t chunk, const float* S_P, const uint16_t* conv_win,
                                  uint16_t* o, uint32_t flags, void* stream) {
-  (void)flags;
   MetaLayout L;
   int rc = gdn_common_checks(m, &L, q, k, v, alpha, eta, conv_w, H, d, K, chunk, o);
   if (rc != FORK_OK) return rc;
@@ -607,5 +589,6 @@ extern "C" int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const ui
   p.conv_ckpt = nullptr;
   p.o = o;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128 && !(flags & FORK_WARP_MMA)) return launch_gdn_tc(p, true, m->max_q, s);
   return d == 64 ? launch_gdn<64, true>(p, m->max_q, s) : launch_gdn<128, true>(p, m->max_q, s);
 }
