@@ -173,34 +173,39 @@ __global__ void __launch_bounds__(NT, 1) gdn_tc_kernel(const GdnParams p) {
   const int half = warp >> 2;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-  const uint16_t* xsrc[3] = {p.q, p.k, p.v};
+  auto xsrc_of = [&](int st) -> const uint16_t* { return st == 0 ? p.q : (st == 1 ? p.k : p.v); };
   auto raw = [&](int o_seg, int s, int c) -> float {
-    if (o_seg >= 0) return bf2f(xsrc[s][(static_cast<int64_t>(start + o_seg) * H + h) * D + c]);
+    if (o_seg >= 0) return bf2f(xsrc_of(s)[(static_cast<int64_t>(start + o_seg) * H + h) * D + c]);
     const int r = KW - 1 + o_seg;
     if (r < 0 || hist == nullptr) return 0.f;
     return bf2f(hist[((static_cast<int64_t>(j * (KW - 1) + r) * 3 + s) * H + h) * D + c]);
   };
+  // stage raw rows c0n-3 .. c0n+C-1 (zero beyond the segment) and the gates of a chunk:
+  // thread = (16-byte piece, first row); rows step by NT/16
   auto prefetch = [&](int c0n) {
-    constexpr int CPR = D / 8;
-    for (int e = tid; e < 3 * HR * CPR; e += NT) {
-      const int s = e / (HR * CPR), r = (e / CPR) % HR, ch = e % CPR;
-      const int o_seg = c0n - (KW - 1) + r;
-      const uint16_t* src = p.q;
-      bool valid = false;
-      if (o_seg >= 0 && o_seg < len) {
-        src = xsrc[s] + (static_cast<int64_t>(start + o_seg) * H + h) * D + ch * 8;
-        valid = true;
-      } else if (o_seg < 0 && hist != nullptr) {
-        src = hist + ((static_cast<int64_t>(j * (KW - 1) + (KW - 1) + o_seg) * 3 + s) * H + h) * D + ch * 8;
-        valid = true;
+    const int ch = tid & 15, r0 = tid >> 4;
+#pragma unroll
+    for (int st = 0; st < 3; ++st) {
+      for (int r = r0; r < HR; r += NT / 16) {
+        const int o_seg = c0n - (KW - 1) + r;
+        const uint16_t* src = p.q;
+        bool valid = false;
+        if (o_seg >= 0 && o_seg < len) {
+          src = xsrc_of(st) + (static_cast<int64_t>(start + o_seg) * H + h) * D + ch * 8;
+          valid = true;
+        } else if (o_seg < 0 && hist != nullptr) {
+          src = hist + ((static_cast<int64_t>(j * (KW - 1) + (KW - 1) + o_seg) * 3 + st) * H + h) * D + ch * 8;
+          valid = true;
+        }
+        cp_async16(&raw_st[(st * HR + r) * D + ch * 8], src, valid);
       }
-      cp_async16(&raw_st[(s * HR + r) * D + ch * 8], src, valid);
     }
-    for (int u = tid; u < 2 * C; u += NT) {
-      const int o_seg = c0n + (u % C);
+    if (tid < 2 * C) {
+      const int u = tid & (C - 1);
+      const int o_seg = c0n + u;
       const bool valid = o_seg < len;
-      const float* src = (u < C ? p.alpha : p.eta) + (static_cast<int64_t>(start + (valid ? o_seg : 0)) * H + h);
-      cp_async4(u < C ? &ga[u] : &ge[u - C], src, valid);
+      const float* src = (tid < C ? p.alpha : p.eta) + (static_cast<int64_t>(start + (valid ? o_seg : 0)) * H + h);
+      cp_async4(tid < C ? &ga[u] : &ge[u], src, valid);
     }
     asm volatile("cp.async.commit_group;\n" ::);
   };
@@ -235,6 +240,10 @@ __global__ void __launch_bounds__(NT, 1) gdn_tc_kernel(const GdnParams p) {
 
   unsigned char* ktg = sm + Lay::AM;  // 128 x 64 fp32 (2 boxes), over the inverse's buffers
   const uint32_t xqk_a = smem_u32(xqk), tb_a = smem_u32(tb), pb_a = smem_u32(pb), ktg_a = smem_u32(ktg);
+  for (int e = tid; e < C * C; e += NT) {  // blocks of T above the diagonal stay zero
+    const int t = e >> 6, sidx = e & 63;
+    if ((sidx >> 4) > (t >> 4)) *reinterpret_cast<uint32_t*>(tb + swz(64, t, sidx)) = 0u;
+  }
   bool ok = true;
   if (len > 0) prefetch(0);
   int ci = 0;
@@ -330,15 +339,18 @@ __global__ void __launch_bounds__(NT, 1) gdn_tc_kernel(const GdnParams p) {
       tc::tc_fence_after();
       constexpr uint32_t id1 = tc::idesc_tf32(128, 64, 0, 0);
       constexpr uint32_t id3 = tc::idesc_tf32(128, 128, 0, 0);
+      // the start-address field is in 16-byte units: +2 per 32-byte k step, +1024 per box
+      const uint64_t dq = tc::sdesc_sw128(xqk_a, 16, 1024), dk = tc::sdesc_sw128(xqk_a + C * 128, 16, 1024);
+#pragma unroll
       for (int ks = 0; ks < D / 8; ++ks) {
-        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-        tc::mma_tf32_ss(tmem + TD1, tc::sdesc_sw128(xqk_a + off, 16, 1024),
-                        tc::sdesc_sw128(xqk_a + off + C * 128, 16, 1024), id1, ks > 0);
+        const uint64_t off = static_cast<uint64_t>((ks >> 2) * 1024 + (ks & 3) * 2);
+        tc::mma_tf32_ss(tmem + TD1, dq + off, dk + off, id1, ks > 0);
       }
       tc::mma_commit(&bars[B_M1]);
+#pragma unroll
       for (int ks = 0; ks < D / 8; ++ks) {
-        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-        tc::mma_tf32_ts(tmem + TD3, tmem + TS + ks * 8, tc::sdesc_sw128(xqk_a + off, 16, 1024), id3, ks > 0);
+        const uint64_t off = static_cast<uint64_t>((ks >> 2) * 1024 + (ks & 3) * 2);
+        tc::mma_tf32_ts(tmem + TD3, tmem + TS + ks * 8, dq + off, id3, ks > 0);
       }
       tc::mma_commit(&bars[B_M3]);
     }
@@ -360,19 +372,26 @@ __global__ void __launch_bounds__(NT, 1) gdn_tc_kernel(const GdnParams p) {
       }
     }
     __syncthreads();
-    // ---- T = (I + A)^{-1} (fp32): diagonal 16x16 blocks, then the others ----------
+    // ---- T = (I + A)^{-1} (fp32): diagonal 16x16 blocks, then the others; each
+    //      finished block also goes (rounded) into the B-operand tile -------------
     if (tid < 64) {
       const int bi = tid >> 4, c = tid & 15, base = bi * 16;
       float x[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        float acc = (r == c) ? 1.f : 0.f;
+        float a0 = (r == c) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < r; ++m) acc -= am[(base + r) * LDC + base + m] * x[m];
-        x[r] = r < c ? 0.f : acc;
+        for (int m = 0; m < r; m += 2) {
+          a0 -= am[(base + r) * LDC + base + m] * x[m];
+          if (m + 1 < r) a1 -= am[(base + r) * LDC + base + m + 1] * x[m + 1];
+        }
+        x[r] = r < c ? 0.f : a0 + a1;
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) tm[(base + r) * LDC + base + c] = x[r];
+      for (int r = 0; r < 16; ++r) {
+        tm[(base + r) * LDC + base + c] = x[r];
+        *reinterpret_cast<uint32_t*>(tb + swz(64, base + r, base + c)) = tf32_bits(x[r]);
+      }
     }
     __syncthreads();
     for (int dist = 1; dist < 4; ++dist) {
@@ -380,32 +399,42 @@ __global__ void __launch_bounds__(NT, 1) gdn_tc_kernel(const GdnParams p) {
       for (int e = tid; e < npair * 256; e += NT) {
         const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
         const int bi = dist + pr, bj = pr;
-        float acc = 0.f;
-        for (int m = bj * 16; m < bi * 16; ++m) acc += am[(bi * 16 + r) * LDC + m] * tm[m * LDC + bj * 16 + c];
-        xs[e] = acc;
+        const float* arow = am + (bi * 16 + r) * LDC;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int m = bj * 16; m < bi * 16; m += 4) {
+          a0 += arow[m] * tm[m * LDC + bj * 16 + c];
+          a1 += arow[m + 1] * tm[(m + 1) * LDC + bj * 16 + c];
+          a2 += arow[m + 2] * tm[(m + 2) * LDC + bj * 16 + c];
+          a3 += arow[m + 3] * tm[(m + 3) * LDC + bj * 16 + c];
+        }
+        xs[e] = (a0 + a1) + (a2 + a3);
       }
       __syncthreads();
       for (int e = tid; e < npair * 256; e += NT) {
         const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
         const int bi = dist + pr, bj = pr;
-        float acc = 0.f;
+        const float* trow = tm + (bi * 16 + r) * LDC + bi * 16;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc += tm[(bi * 16 + r) * LDC + bi * 16 + m] * xs[(pr << 8) + m * 16 + c];
-        tm[(bi * 16 + r) * LDC + bj * 16 + c] = -acc;
+        for (int m = 0; m < 16; m += 4) {
+          a0 += trow[m] * xs[(pr << 8) + m * 16 + c];
+          a1 += trow[m + 1] * xs[(pr << 8) + (m + 1) * 16 + c];
+          a2 += trow[m + 2] * xs[(pr << 8) + (m + 2) * 16 + c];
+          a3 += trow[m + 3] * xs[(pr << 8) + (m + 3) * 16 + c];
+        }
+        const float v = -((a0 + a1) + (a2 + a3));
+        tm[(bi * 16 + r) * LDC + bj * 16 + c] = v;
+        *reinterpret_cast<uint32_t*>(tb + swz(64, bi * 16 + r, bj * 16 + c)) = tf32_bits(v);
       }
       __syncthreads();
     }
-    // T as the B operand (row t, column s; zero above the diagonal), rounded
-    for (int e = tid; e < C * C; e += NT) {
-      const int t = e >> 6, s = e & 63;
-      *reinterpret_cast<uint32_t*>(tb + swz(64, t, s)) = s <= t ? tf32_bits(tm[t * LDC + s]) : 0u;
-    }
-    __syncthreads();  // the inverse's buffers are free from here on
+    // the inverse's buffers are free from here on (the last loop ended with a barrier)
     // K^T diag(Gamma_last) as the B operand of the state update (row c, column s),
     // written over the inverse's buffers
     if (need_state) {
-      for (int e = tid; e < D * C; e += NT) {
-        const int cch = e / C, sidx = e % C;
+      const int cch = tid >> 1, s0 = (tid & 1) * 32;
+#pragma unroll 8
+      for (int sidx = s0; sidx < s0 + 32; ++sidx) {
         const float kv = *reinterpret_cast<const float*>(xqk + swz(128, C + sidx, cch));
         *reinterpret_cast<uint32_t*>(ktg + swz(128, cch, sidx)) = tf32_bits(GL[sidx] * kv);
       }
