@@ -89,7 +89,8 @@ typedef struct fork_meta {
  * > 1<<18). */
 size_t fork_meta_bytes(int32_t T_cap, int32_t max_req, int32_t max_q);
 
-/* Fill *m (host only, no CUDA call).  tile_tokens in {8,16,32,64,128}.
+/* Fill *m (host only, no CUDA call).  tile_tokens in {8,16,32,64,128} (256 is accepted
+ * for metadata that no attention call will use).
  * Errors: FORK_EINVAL (null, invalid capacity, buffer too small or not
  * 16-byte aligned). */
 int fork_meta_init(fork_meta* m, void* d_buf, size_t bytes, int32_t T_cap, int32_t max_req,
@@ -113,6 +114,10 @@ int fork_meta_init(fork_meta* m, void* d_buf, size_t bytes, int32_t T_cap, int32
  * (R > max_req, Nq > max_q). */
 int fork_build_meta(const fork_meta* m, const int32_t* d_desc, int32_t R, int32_t Nq,
                     uint32_t flags, void* stream);
+
+/* cudaError_t value of the most recent CUDA runtime call of this library that
+ * failed on the calling host thread (0 if none): the detail behind FORK_ECUDA. */
+int fork_last_cuda_error(void);
 
 /* Copy the device status word of a metadata buffer to *h_status.  Enqueues a
  * device-to-host copy on `stream` and synchronises that stream. */

@@ -214,7 +214,7 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     p.rope_lo = lo;
     p.rope_theta = 0.f;  // queries are already rotated
   }
-  if (cudaGetLastError() != cudaSuccess) return FORK_ECUDA;
+  if (cuda_rc(cudaGetLastError()) != FORK_OK) return FORK_ECUDA;
   const int grid_x = static_cast<int>(std::min<int64_t>(
       L.max_work, (L.T_cap + m->tile_tokens - 1) / m->tile_tokens + L.max_seg));
   if (flags & FORK_WARP_MMA)
@@ -253,12 +253,12 @@ void* g_noalloc_ptr[kMaxDevices] = {};  // device address of the array, per devi
 // device with that device current (this also loads the module on that device).
 static int noalloc_scratch(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FORK_ECUDA;
+  if (cuda_rc(cudaGetDevice(&dev)) != FORK_OK) return FORK_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return FORK_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FORK_ECUDA;
+    if (cuda_rc(cudaGetSymbolAddress(&p, g_noalloc_scratch)) != FORK_OK || p == nullptr) return FORK_ECUDA;
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];

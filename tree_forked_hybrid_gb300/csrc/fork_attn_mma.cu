@@ -307,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
 template <int D>
 int launch_attn_mma(const AttnParams& p, int grid_x, cudaStream_t s) {
   const size_t smem = sizeof(Smem<D>);
-  if (cudaFuncSetAttribute(attn_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
+  if (cuda_rc(cudaFuncSetAttribute(attn_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem))) != FORK_OK)
     return FORK_ECUDA;
   dim3 grid(grid_x, p.Hkv);
   attn_mma_kernel<D><<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? FORK_OK : FORK_ECUDA;
+  return cuda_rc(cudaGetLastError());
 }
 
 template int launch_attn_mma<64>(const AttnParams&, int, cudaStream_t);

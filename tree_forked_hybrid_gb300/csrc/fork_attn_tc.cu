@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, cudaStream_t s) {
   using LY = TcLayout<D>;
-  if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM) != cudaSuccess)
+  if (cuda_rc(cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM)) != FORK_OK)
     return FORK_ECUDA;
   TcParams p;
   p.meta = a.meta;
@@ -419,7 +419,7 @@ int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, cud
   p.scale_log2 = a.scale_log2;
   dim3 grid(grid_x, a.Hkv);
   attn_tc_kernel<D><<<grid, kThreads, LY::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
-  return cudaGetLastError() == cudaSuccess ? FORK_OK : FORK_ECUDA;
+  return cuda_rc(cudaGetLastError());
 }
 
 template int launch_attn_tc<64>(const AttnParams&, const CUtensorMap*, int, cudaStream_t);

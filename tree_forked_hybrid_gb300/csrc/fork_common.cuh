@@ -84,6 +84,10 @@ inline bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p)
 
 int check_device();  // FORK_OK on an sm_103 device, else FORK_EUNSUPPORTED/FORK_ECUDA
 
+// Record a failing CUDA runtime result for fork_last_cuda_error (per host thread);
+// returns FORK_ECUDA when e is an error, FORK_OK otherwise.
+int cuda_rc(cudaError_t e);
+
 __device__ __forceinline__ float bf2f(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }

@@ -498,12 +498,12 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
 template <int D, bool BRANCH>
 static int launch_gdn(const GdnParams& p, int grid_x, cudaStream_t s) {
   const size_t smem = sizeof(GdnSmem<D>);
-  if (cudaFuncSetAttribute(gdn_chunk_kernel<D, BRANCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
+  if (cuda_rc(cudaFuncSetAttribute(gdn_chunk_kernel<D, BRANCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem))) != FORK_OK)
     return FORK_ECUDA;
   dim3 grid(grid_x, p.H);
   gdn_chunk_kernel<D, BRANCH><<<grid, NT, smem, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? FORK_OK : FORK_ECUDA;
+  return cuda_rc(cudaGetLastError());
 }
 
 static int gdn_common_checks(const fork_meta* m, MetaLayout* L, const uint16_t* q, const uint16_t* k,

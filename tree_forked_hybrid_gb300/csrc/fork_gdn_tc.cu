@@ -614,7 +614,7 @@ int launch_gdn_tc(const GdnParams& p, bool branch, int grid_x, cudaStream_t s) {
       return FORK_ECUDA;
     gdn_tc_kernel<false><<<grid, NT, Lay::SMEM, s>>>(p);
   }
-  return cudaGetLastError() == cudaSuccess ? FORK_OK : FORK_ECUDA;
+  return cuda_rc(cudaGetLastError());
 }
 
 }  // namespace fork

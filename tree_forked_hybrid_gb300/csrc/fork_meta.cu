@@ -13,12 +13,20 @@
 
 namespace fork {
 
+static thread_local int t_last_cuda_error = 0;
+
+int cuda_rc(cudaError_t e) {
+  if (e == cudaSuccess) return FORK_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return FORK_ECUDA;
+}
+
 int check_device() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FORK_ECUDA;
+  if (cuda_rc(cudaGetDevice(&dev)) != FORK_OK) return FORK_ECUDA;
   int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+  if (cuda_rc(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != FORK_OK ||
+      cuda_rc(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != FORK_OK)
     return FORK_ECUDA;
   return (major == 10 && minor == 3) ? FORK_OK : FORK_EUNSUPPORTED;
 }
@@ -32,7 +40,7 @@ int check_meta(const fork_meta* m, MetaLayout* out) {
   if (!m || !m->d_buf || !is_aligned16(m->d_buf)) return FORK_EINVAL;
   if (!valid_caps(m->T_cap, m->max_req, m->max_q)) return FORK_EINVAL;
   int t = m->tile_tokens;
-  if (t != 8 && t != 16 && t != 32 && t != 64 && t != 128) return FORK_EINVAL;
+  if (t != 8 && t != 16 && t != 32 && t != 64 && t != 128 && t != 256) return FORK_EINVAL;
   MetaLayout L = meta_layout(m->T_cap, m->max_req, m->max_q);
   if (m->bytes < static_cast<size_t>(L.total) * 4) return FORK_EINVAL;
   *out = L;
@@ -265,8 +273,10 @@ extern "C" int fork_build_meta(const fork_meta* m, const int32_t* d_desc, int32_
   int32_t* meta = static_cast<int32_t*>(m->d_buf);
   meta_tables_kernel<<<1, 1024, 0, s>>>(d_desc, R, Nq, meta, L, m->tile_tokens);
   meta_tokens_kernel<<<L.max_seg + 1, 256, 0, s>>>(meta, L);
-  return cudaGetLastError() == cudaSuccess ? FORK_OK : FORK_ECUDA;
+  return cuda_rc(cudaGetLastError());
 }
+
+extern "C" int fork_last_cuda_error(void) { return t_last_cuda_error; }
 
 extern "C" int fork_read_status(const fork_meta* m, int32_t* h_status, void* stream) {
   MetaLayout L;
@@ -275,8 +285,7 @@ extern "C" int fork_read_status(const fork_meta* m, int32_t* h_status, void* str
   if (!h_status) return FORK_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int32_t* meta = static_cast<const int32_t*>(m->d_buf);
-  if (cudaMemcpyAsync(h_status, meta + H_STATUS, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
-      cudaSuccess)
+  if (cuda_rc(cudaMemcpyAsync(h_status, meta + H_STATUS, sizeof(int32_t), cudaMemcpyDeviceToHost, s)) != FORK_OK)
     return FORK_ECUDA;
-  return cudaStreamSynchronize(s) == cudaSuccess ? FORK_OK : FORK_ECUDA;
+  return cuda_rc(cudaStreamSynchronize(s));
 }

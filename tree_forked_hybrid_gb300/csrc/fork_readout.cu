@@ -70,5 +70,5 @@ extern "C" int fork_readout(const fork_meta* m, const uint16_t* h, int32_t D, co
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   readout_kernel<<<m->max_q, 256, 0, s>>>(static_cast<const int32_t*>(m->d_buf), L, h, D, w_opt,
                                          opt_off, p);
-  return cudaGetLastError() == cudaSuccess ? FORK_OK : FORK_ECUDA;
+  return cuda_rc(cudaGetLastError());
 }

@@ -25,9 +25,11 @@ _lib = None
 
 
 class ForkError(RuntimeError):
-    def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+    def __init__(self, fn: str, code: int, cuda_error: int = 0):
+        extra = f" (CUDA error {cuda_error})" if code == 4 and cuda_error else ""
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}{extra}")
         self.code = code
+        self.cuda_error = cuda_error
 
 
 class fork_meta(ctypes.Structure):
@@ -55,6 +57,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fork_meta_init": (ctypes.c_int, [MP, vp, sz, i32, i32, i32, i32]),
         "fork_build_meta": (ctypes.c_int, [MP, vp, i32, i32, u32, vp]),
         "fork_read_status": (ctypes.c_int, [MP, ctypes.POINTER(i32), vp]),
+        "fork_last_cuda_error": (ctypes.c_int, []),
         "fork_attn_workspace_bytes": (sz, [i32, i32, i32, i32, i32, f32]),
         "fork_attn": (ctypes.c_int, [MP, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, vp, vp, i32, vp,
                                      sz, u32, vp]),
@@ -92,7 +95,7 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def _check(fn: str, rc: int):
     if rc != 0:
-        raise ForkError(fn, rc)
+        raise ForkError(fn, rc, load().fork_last_cuda_error() if rc == 4 else 0)
 
 
 class Meta:
