@@ -49,11 +49,12 @@ __global__ void rope_rows_kernel(const int32_t* __restrict__ meta, MetaLayout L,
   const int T = meta[H_T];
   const int R = meta[H_R];
   constexpr int HALF = D / 2;
-  const int64_t rows = static_cast<int64_t>(T + prefix_rows) * Hkv;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-       idx < rows * HALF; idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(idx % HALF);
-    const int64_t rh = idx / HALF;  // row * Hkv + head
+  constexpr int GRP = HALF / 8;  // 8 pairs per thread: one 16-byte load from each half
+  const int64_t items = static_cast<int64_t>(T + prefix_rows) * Hkv * GRP;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < items;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i0 = static_cast<int>(idx % GRP) * 8;
+    const int64_t rh = idx / GRP;  // row * heads + head
     const int64_t row = rh / Hkv;
     const uint16_t* src;
     uint16_t* dst;
@@ -80,11 +81,31 @@ __global__ void rope_rows_kernel(const int32_t* __restrict__ meta, MetaLayout L,
       atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
       continue;
     }
-    float cs, sn;
-    rope_cs(hi, lo, HALF, t, i, &cs, &sn);
-    const float x0 = bf2f(src[i]), x1 = bf2f(src[i + HALF]);
-    dst[i] = f2bf(x0 * cs - x1 * sn);
-    dst[i + HALF] = f2bf(x1 * cs + x0 * sn);
+    const uint4 xa = *reinterpret_cast<const uint4*>(src + i0);
+    const uint4 xb = *reinterpret_cast<const uint4*>(src + i0 + HALF);
+    const float4* A = reinterpret_cast<const float4*>(hi + static_cast<int64_t>(t >> 6) * HALF + i0);
+    const float4* B = reinterpret_cast<const float4*>(lo + static_cast<int64_t>(t & 63) * HALF + i0);
+    const uint32_t aw[4] = {xa.x, xa.y, xa.z, xa.w}, bw[4] = {xb.x, xb.y, xb.z, xb.w};
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // pairs i0+2q, i0+2q+1
+      const float4 a4 = A[q], b4 = B[q];  // (cos, sin) of the two pairs for 64*(t>>6) and t&63
+      float ya[2], yb[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float ac = e ? a4.z : a4.x, as = e ? a4.w : a4.y;
+        const float bc = e ? b4.z : b4.x, bs = e ? b4.w : b4.y;
+        const float cs = ac * bc - as * bs, sn = as * bc + ac * bs;
+        const float x0 = bf2f(static_cast<uint16_t>(e ? aw[q] >> 16 : aw[q] & 0xffffu));
+        const float x1 = bf2f(static_cast<uint16_t>(e ? bw[q] >> 16 : bw[q] & 0xffffu));
+        ya[e] = x0 * cs - x1 * sn;
+        yb[e] = x1 * cs + x0 * sn;
+      }
+      oa[q] = static_cast<uint32_t>(f2bf(ya[0])) | (static_cast<uint32_t>(f2bf(ya[1])) << 16);
+      ob[q] = static_cast<uint32_t>(f2bf(yb[0])) | (static_cast<uint32_t>(f2bf(yb[1])) << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + i0) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *reinterpret_cast<uint4*>(dst + i0 + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
   }
 }
 

@@ -48,8 +48,8 @@ struct TcLayout {
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);  // one CTA per SM
 };
 
-enum Bar { B_QFULL = 0, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_SFULL0, B_SFULL1,
-           B_SFREE0, B_SFREE1, B_PFULL, B_ODONE, B_FIN, B_COUNT };
+enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
+           B_VEMPTY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL, B_ODONE, B_FIN, B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -157,10 +157,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     tc::mbar_init(&bars[B_QFULL], 1);
-    tc::mbar_init(&bars[B_KVFULL0], 1);
-    tc::mbar_init(&bars[B_KVFULL1], 1);
-    tc::mbar_init(&bars[B_KVEMPTY0], 1);
-    tc::mbar_init(&bars[B_KVEMPTY1], 1);
+    for (int k = 0; k < 2; ++k) {
+      tc::mbar_init(&bars[B_KFULL0 + k], 1);
+      tc::mbar_init(&bars[B_VFULL0 + k], 1);
+      tc::mbar_init(&bars[B_KEMPTY0 + k], 1);
+      tc::mbar_init(&bars[B_VEMPTY0 + k], 1);
+    }
     tc::mbar_init(&bars[B_SFULL0], 1);
     tc::mbar_init(&bars[B_SFULL1], 1);
     tc::mbar_init(&bars[B_SFREE0], 128);
@@ -198,65 +200,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::mbar_expect_tx(&bars[B_QFULL], NB * kBox);
       for (int b = 0; b < NB; ++b) tc::tma_load_3d(sQ + b * kBox, &qmap, &bars[B_QFULL], b * 64, g * G, seg_start + off);
+      // K_f waits for QK_{f-2} (its slot's previous reader), V_f for PV_{f-2}
       int issued = 0;
       for (int f = 0; f < total; ++f) {
         const int st = f & 1;
-        if (f >= 2 && !tc::mbar_wait(&bars[B_KVEMPTY0 + st], ((f >> 1) - 1) & 1, abort)) break;
         const KT kt = key_tile(f);
         const CUtensorMap* km = kt.r == 0 ? &pkmap : &kmap;
         const CUtensorMap* vm = kt.r == 0 ? &pvmap : &vmap;
         const int row = kt.row0 + kt.t * kKeys;
-        tc::mbar_expect_tx(&bars[B_KVFULL0 + st], 2 * NB * kBox);
-        for (int b = 0; b < NB; ++b) {
-          tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KVFULL0 + st], b * 64, g, row);
-          tc::tma_load_3d(sV + (st * NB + b) * kBox, vm, &bars[B_KVFULL0 + st], b * 64, g, row);
-        }
+        if (f >= 2 && !tc::mbar_wait(&bars[B_KEMPTY0 + st], ((f >> 1) - 1) & 1, abort)) break;
+        tc::mbar_expect_tx(&bars[B_KFULL0 + st], NB * kBox);
+        for (int b = 0; b < NB; ++b) tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KFULL0 + st], b * 64, g, row);
+        if (f >= 2 && !tc::mbar_wait(&bars[B_VEMPTY0 + st], ((f >> 1) - 1) & 1, abort)) break;
+        tc::mbar_expect_tx(&bars[B_VFULL0 + st], NB * kBox);
+        for (int b = 0; b < NB; ++b) tc::tma_load_3d(sV + (st * NB + b) * kBox, vm, &bars[B_VFULL0 + st], b * 64, g, row);
         issued = f + 1;
       }
       // drain: the last loads issued complete by themselves
       tc::mbar_wait(&bars[B_QFULL], 0, abort);
-      for (int f = max(0, issued - 2); f < issued; ++f) tc::mbar_wait(&bars[B_KVFULL0 + (f & 1)], (f >> 1) & 1, abort);
+      for (int f = max(0, issued - 2); f < issued; ++f) {
+        tc::mbar_wait(&bars[B_KFULL0 + (f & 1)], (f >> 1) & 1, abort);
+        tc::mbar_wait(&bars[B_VFULL0 + (f & 1)], (f >> 1) & 1, abort);
+      }
     }
   } else if (warp == 5) {
     // ===================== MMA issuer =====================
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16(128, kKeys, 0, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, 0, 1);
-      const uint32_t q_addr = tc::smem_u32(sQ), k_addr = tc::smem_u32(sK), v_addr = tc::smem_u32(sV),
-                     p_addr = tc::smem_u32(sP);
+      // descriptors are built once; the start-address field (16-byte units) is then
+      // advanced by constants: +2 per 32-byte k step, +kBox/16 per box
+      const uint64_t dq = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
+      const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
+      const uint64_t dp = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);
+      const uint64_t dv = tc::sdesc_sw128(tc::smem_u32(sV), kBox, 1024);
+      constexpr uint64_t kBoxU = kBox / 16, kStageU = NB * kBox / 16;
       bool ok = tc::mbar_wait(&bars[B_QFULL], 0, abort);
-      auto issue_pv = [&](int f) {
+      auto issue_pv = [&](int f) -> bool {
         const int st = f & 1;
-        for (int step = 0; step < kKeys / 16; ++step) {
-          const uint64_t a = tc::sdesc_sw128(p_addr + (step >> 2) * kBox + (step & 3) * 32, 16, 1024);
-          const uint64_t b = tc::sdesc_sw128(v_addr + st * NB * kBox + step * 2048, kBox, 1024);
-          tc::mma_bf16(tm_o, a, b, idesc_pv, (f > 0 || step > 0) ? 1u : 0u);
-        }
+        if (!tc::mbar_wait(&bars[B_VFULL0 + st], (f >> 1) & 1, abort)) return false;
+        if (!tc::mbar_wait(&bars[B_PFULL], f & 1, abort)) return false;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int step = 0; step < kKeys / 16; ++step)
+          tc::mma_bf16(tm_o, dp + (step >> 2) * kBoxU + (step & 3) * 2, dv + st * kStageU + step * (2048 / 16),
+                       idesc_pv, (f > 0 || step > 0) ? 1u : 0u);
         tc::mma_commit(&bars[B_ODONE]);
-        tc::mma_commit(&bars[B_KVEMPTY0 + st]);
+        tc::mma_commit(&bars[B_VEMPTY0 + st]);
+        return true;
       };
       for (int f = 0; ok && f < total; ++f) {
         const int st = f & 1;
-        if (!tc::mbar_wait(&bars[B_KVFULL0 + st], (f >> 1) & 1, abort)) { ok = false; break; }
+        if (!tc::mbar_wait(&bars[B_KFULL0 + st], (f >> 1) & 1, abort)) { ok = false; break; }
         if (f >= 2 && !tc::mbar_wait(&bars[B_SFREE0 + st], ((f >> 1) - 1) & 1, abort)) { ok = false; break; }
         tc::tc_fence_after();
+#pragma unroll
         for (int b = 0; b < NB; ++b)
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = tc::sdesc_sw128(q_addr + b * kBox + k * 32, 16, 1024);
-            const uint64_t bd = tc::sdesc_sw128(k_addr + (st * NB + b) * kBox + k * 32, 16, 1024);
-            tc::mma_bf16(tm_s(st), a, bd, idesc_qk, (b | k) ? 1u : 0u);
-          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16(tm_s(st), dq + b * kBoxU + k * 2, dk + st * kStageU + b * kBoxU + k * 2, idesc_qk,
+                         (b | k) ? 1u : 0u);
         tc::mma_commit(&bars[B_SFULL0 + st]);
-        if (f >= 1) {
-          if (!tc::mbar_wait(&bars[B_PFULL], (f - 1) & 1, abort)) { ok = false; break; }
-          tc::tc_fence_after();
-          issue_pv(f - 1);
-        }
+        tc::mma_commit(&bars[B_KEMPTY0 + st]);
+        if (f >= 1 && !issue_pv(f - 1)) { ok = false; break; }
       }
-      if (ok && tc::mbar_wait(&bars[B_PFULL], (total - 1) & 1, abort)) {
-        tc::tc_fence_after();
-        issue_pv(total - 1);
-      }
+      if (ok) issue_pv(total - 1);
       // every MMA issued by this thread has completed before TMEM is released
       tc::mma_commit(&bars[B_FIN]);
       tc::mbar_wait(&bars[B_FIN], 0, abort);
@@ -343,6 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // key rows past the range end may be pad rows of the stream: zero them in V
       if (u0 + kKeys > len) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_VFULL0 + st], (f >> 1) & 1, abort));
+        if (!ok) break;
         const int valid_rows = max(0, len - u0);
         if (row >= valid_rows) {
           unsigned char* vrow = sV + st * NB * kBox + row * 128;
