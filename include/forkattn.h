@@ -80,7 +80,8 @@ typedef struct fork_meta {
   int32_t T_cap;       /* stream capacity in tokens */
   int32_t max_req;     /* most requests a round may hold */
   int32_t max_q;       /* most questions a round may hold */
-  int32_t tile_tokens; /* attention query-tile length in tokens: 128 / (Hq / Hkv) */
+  int32_t tile_tokens; /* tokens per attention work item: 256 / (Hq / Hkv) (two 128-row
+                          query tiles per CTA), or 128 / (Hq / Hkv) (one tile) */
 } fork_meta;
 
 /* Bytes of the metadata buffer for a stream capacity T_cap (tokens), at most
@@ -89,8 +90,7 @@ typedef struct fork_meta {
  * > 1<<18). */
 size_t fork_meta_bytes(int32_t T_cap, int32_t max_req, int32_t max_q);
 
-/* Fill *m (host only, no CUDA call).  tile_tokens in {8,16,32,64,128} (256 is accepted
- * for metadata that no attention call will use).
+/* Fill *m (host only, no CUDA call).  tile_tokens in {8,16,32,64,128,256}.
  * Errors: FORK_EINVAL (null, invalid capacity, buffer too small or not
  * 16-byte aligned). */
 int fork_meta_init(fork_meta* m, void* d_buf, size_t bytes, int32_t T_cap, int32_t max_req,
@@ -138,7 +138,9 @@ size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq,
 /* o_x = sum_y softmax_y(<R(q_x,t_x), R(k_y,t_y)> * scale) v_y over visible y.
  *   q [T_cap, Hq, d], k and v [T_cap, Hkv, d] bf16 (stream rows; pad rows
  *   ignored); o [T_cap, Hq, d] bf16 (pad rows not written).  q-head h reads
- *   kv-head h / (Hq / Hkv).  d in {64, 128}; Hq / Hkv * tile_tokens == 128.
+ *   kv-head h / (Hq / Hkv).  d in {64, 128}; Hq / Hkv * tile_tokens is 256
+ *   (each work item is two 128-row query tiles sharing every key tile: the fast
+ *   configuration) or 128; FORK_WARP_MMA needs 128.
  *   window 0 = full attention, else W > 0.  rope_theta 0 = no rotary
  *   embedding, else rotate-half pairs (i, i + d/2) by t * theta^(-2i/d).
  *   scale: score scale (1/sqrt(d) in the workloads).

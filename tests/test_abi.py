@@ -74,7 +74,10 @@ def test_argument_errors_return_before_any_launch(lib):
     # attention: null tensors, bad head dim, GQA group not matching the tile, misalignment
     assert lib.fork_attn(ref, None, fake, fake, fake, 4, 1, 128, 0, 0.0, 0.1, None, None, 0, None, 0, 0, None) == 1
     assert lib.fork_attn(ref, fake, fake, fake, fake, 4, 1, 96, 0, 0.0, 0.1, None, None, 0, None, 0, 0, None) == 1
-    assert lib.fork_attn(ref, fake, fake, fake, fake, 8, 1, 128, 0, 0.0, 0.1, None, None, 0, None, 0, 0, None) == 1
+    # 16 q-heads per kv head x 32-token tiles = 512 rows: neither one nor two 128-row tiles
+    assert lib.fork_attn(ref, fake, fake, fake, fake, 16, 1, 128, 0, 0.0, 0.1, None, None, 0, None, 0, 0, None) == 1
+    # two 128-row tiles per work item are for the tcgen05 kernel only
+    assert lib.fork_attn(ref, fake, fake, fake, fake, 8, 1, 128, 0, 0.0, 0.1, None, None, 0, None, 0, 4, None) == 1
     assert lib.fork_attn(ref, fake, fake, fake, fake, 6, 4, 128, 0, 0.0, 0.1, None, None, 0, None, 0, 0, None) == 1
     odd = ctypes.c_void_p(0x1002)
     assert lib.fork_attn(ref, odd, fake, fake, fake, 4, 1, 128, 0, 0.0, 0.1, None, None, 0, None, 0, 0, None) == 1

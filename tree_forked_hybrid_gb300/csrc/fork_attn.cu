@@ -181,7 +181,9 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   if (d != 64 && d != 128) return FORK_EINVAL;
   if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0) return FORK_EINVAL;
   const int G = Hq / Hkv;
-  if (G * m->tile_tokens != 128) return FORK_EINVAL;
+  // a work item is one 128-row query tile, or two for the tcgen05 kernel
+  const bool warp_mma = (flags & FORK_WARP_MMA) != 0;
+  if (G * m->tile_tokens != 128 && (warp_mma || G * m->tile_tokens != 256)) return FORK_EINVAL;
   if (window < 0 || prefix_rows < 0 || !(scale > 0.f) || !std::isfinite(scale)) return FORK_EINVAL;
   if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return FORK_EINVAL;
   if (prefix_rows > 0 && (!prefix_k || !prefix_v || !is_aligned16(prefix_k) || !is_aligned16(prefix_v)))
@@ -238,17 +240,19 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   if (cuda_rc(cudaGetLastError()) != FORK_OK) return FORK_ECUDA;
   const int grid_x = static_cast<int>(std::min<int64_t>(
       L.max_work, (L.T_cap + m->tile_tokens - 1) / m->tile_tokens + L.max_seg));
-  if (flags & FORK_WARP_MMA)
+  if (warp_mma)
     return d == 64 ? launch_attn_mma<64>(p, grid_x, s) : launch_attn_mma<128>(p, grid_x, s);
   alignas(128) CUtensorMap maps[5];
   const uint16_t* pk = p.prefix_rows > 0 ? p.prefix_k : p.k;
   const uint16_t* pv = p.prefix_rows > 0 ? p.prefix_v : p.v;
   const int prow = p.prefix_rows > 0 ? p.prefix_rows : L.T_cap;
-  if (!make_map(&maps[0], p.q, d, Hq, L.T_cap, G, m->tile_tokens) ||
+  const bool two = G * m->tile_tokens == 256;
+  const int tile = 128 / G;  // tokens of one 128-row query tile
+  if (!make_map(&maps[0], p.q, d, Hq, L.T_cap, G, tile) ||
       !make_map(&maps[1], p.k, d, Hkv, L.T_cap, 1, 128) || !make_map(&maps[2], v, d, Hkv, L.T_cap, 1, 128) ||
       !make_map(&maps[3], pk, d, Hkv, prow, 1, 128) || !make_map(&maps[4], pv, d, Hkv, prow, 1, 128))
     return FORK_ECUDA;
-  return d == 64 ? launch_attn_tc<64>(p, maps, grid_x, s) : launch_attn_tc<128>(p, maps, grid_x, s);
+  return d == 64 ? launch_attn_tc<64>(p, maps, grid_x, two, s) : launch_attn_tc<128>(p, maps, grid_x, two, s);
 }
 
 // ---- fork_attn_noalloc: fork_attn with the library's own scratch area -------------

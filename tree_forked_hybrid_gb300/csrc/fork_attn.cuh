@@ -49,6 +49,6 @@ int launch_attn_mma(const AttnParams& p, int grid_x, cudaStream_t s);
 
 // maps: q, k, v, prefix k, prefix v (CUtensorMap, 128-byte aligned)
 template <int D>
-int launch_attn_tc(const AttnParams& p, const CUtensorMap* maps, int grid_x, cudaStream_t s);
+int launch_attn_tc(const AttnParams& p, const CUtensorMap* maps, int grid_x, bool two_tiles, cudaStream_t s);
 
 }  // namespace fork

@@ -2,26 +2,35 @@
 //
 // Visibility (rainbus summary "方法步骤详情" step 2; onedev "무엇과 다른가"):
 // key y is visible to query x iff j_y = j_x, c_y in {0, c_x}, t_y <= t_x and,
-// for a sliding-window layer, t_x - t_y < W.  A query tile (128 rows =
-// tile_tokens tokens x the Hq/Hkv heads that share one kv head) reads at most
-// three contiguous key ranges: the request's prefix rows kept outside the
-// stream, its trunk segment, and for a question its own branch.  Inside a
-// range, key u (position p0 + u) is visible to query position t iff u < len,
-// p0 + u <= t and (W == 0 or t - p0 - u < W).  Key tiles are aligned to the
-// range start and query tiles to the segment start: every output element is
-// produced by the same sequence of operations whatever else the round holds.
+// for a sliding-window layer, t_x - t_y < W.  The queries of one work item
+// (tile_tokens tokens of one segment x the Hq/Hkv heads that share a kv head)
+// read at most three contiguous key ranges: the request's prefix rows kept
+// outside the stream, its trunk segment, and for a question its own branch.
+// Inside a range, key u (position p0 + u) is visible to query position t iff
+// u < len, p0 + u <= t and (W == 0 or t - p0 - u < W).  Key tiles are aligned
+// to the range start and query tiles to the segment start: every output
+// element is produced by the same sequence of operations whatever else the
+// round holds.
 //
-// One CTA = one query tile x one kv head, 6 warps:
-//   warp 4 (one lane)  TMA producer: Q once, then K/V tiles into a 2-stage ring;
-//   warp 5 (one lane)  MMA issuer: S = Q K^T into one of two TMEM buffers,
-//                      O += P V into a TMEM accumulator; TMEM owner;
-//   warps 0-3          one query row per thread: S from TMEM, mask, online
-//                      softmax in the log2 domain (the running maximum is only
-//                      moved when it grows by more than 2^8, so O is rescaled
-//                      rarely), P (bf16) into shared memory, final O / l.
-// Operands are bf16 in 128-byte-swizzled shared memory, accumulation f32 in
-// TMEM.  Every wait is bounded; on a timeout the CTA raises the status bit,
-// drains its own copies and MMAs, frees TMEM and exits.
+// One CTA = one work item x one kv head = up to two 128-row query tiles
+// (rows = token x grouped head) that share every K/V tile, 10 warps:
+//   warp 8 (one lane)   TMA producer: both Q tiles once, then K and V tiles
+//                       into two 2-stage rings (K and V slots are freed by
+//                       their own readers);
+//   warp 9              MMA issuer (lane 0) and TMEM owner.  Per key tile j,
+//                       for each query tile t: O_t += P_t(j-1) V(j-1), then
+//                       S_t = Q_t K(j)^T; the two tiles alternate so one
+//                       tile's softmax overlaps the other tile's products;
+//   warps 0-3 / 4-7     softmax of tile 0 / tile 1, one query row per thread:
+//                       S from TMEM, mask, online softmax in the log2 domain
+//                       (the running maximum only moves when it grows by more
+//                       than 2^8, so O is rescaled rarely), P as bf16 written
+//                       back into the TMEM columns of S, where the PV product
+//                       reads it as its A operand; at the end O / l.
+// TMEM: S/P of tile t at columns 128t, O_t at 256 + t*D (512 columns).
+// Operands are bf16, accumulation f32 in TMEM.  Every wait is bounded; on a
+// timeout the CTA raises the status bit, drains its own copies and MMAs,
+// frees TMEM and exits.
 #include "fork_attn.cuh"
 #include "tc_ptx.cuh"
 
@@ -29,27 +38,26 @@ namespace fork {
 
 namespace {
 
-constexpr int kRows = 128;   // query rows per CTA
+constexpr int kRows = 128;   // query rows per MMA tile
 constexpr int kKeys = 128;   // keys per tile
 constexpr int kBox = 128 * 128;  // bytes of one 128-row x 64-element bf16 box
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescale = 8.f;  // move the running max only when it grows by > 2^8
 
 template <int D>
 struct TcLayout {
   static constexpr int NB = D / 64;  // 64-element boxes per row
-  static constexpr int Q = 0;
-  static constexpr int K = Q + NB * kBox;           // 2 stages
-  static constexpr int V = K + 2 * NB * kBox;       // 2 stages
-  static constexpr int P = V + 2 * NB * kBox;       // 2 boxes (128 keys)
-  static constexpr int BAR = P + 2 * kBox;
+  static constexpr int Q = 0;                        // 2 query tiles
+  static constexpr int K = Q + 2 * NB * kBox;        // 2 stages
+  static constexpr int V = K + 2 * NB * kBox;        // 2 stages
+  static constexpr int BAR = V + 2 * NB * kBox;
   static constexpr int BYTES = BAR + 256;
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);  // one CTA per SM
 };
 
 enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
-           B_VEMPTY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL, B_ODONE, B_FIN, B_COUNT };
+           B_VEMPTY1, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -63,11 +71,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// byte offset of element e (0 <= e < D) of row r inside a [128 x D] K-major
-// SW128 tile made of D/64 boxes
-__device__ __forceinline__ int sw128_off(int r, int e) {
-  const int b = e >> 6, ce = e & 63;
-  return b * kBox + r * 128 + ((((ce >> 3) ^ (r & 7))) << 4) + ((ce & 7) << 1);
+// tcgen05.mma kind::f16 with A (bf16, 2 per 32-bit column) read from TMEM
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 }  // namespace
@@ -76,7 +87,7 @@ struct TcParams {
   const int32_t* meta;
   MetaLayout L;
   uint16_t* o;
-  int Hq, Hkv, G, prefix_rows, window;
+  int Hq, Hkv, G, prefix_rows, window, two_tiles;
   float scale_log2;
 };
 
@@ -98,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (w >= meta[H_NWORK]) return;
   const int g = blockIdx.y;
   const int G = p.G;
-  const int tile = kRows / G;
+  const int tile = kRows / G;  // tokens per MMA tile
   const int s = meta[L.work_seg + w];
   const int off = meta[L.work_off + w];
   const int seg_start = meta[L.seg_start + s];
@@ -106,9 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int seg_pos0 = meta[L.seg_pos0 + s];
   const int j = meta[L.seg_req + s];
   const int c = meta[L.seg_branch + s];
-  const int n = min(tile, seg_len - off);
+  const int n_all = min(p.two_tiles ? 2 * tile : tile, seg_len - off);  // tokens of this work item
+  const int ntiles = n_all > tile ? 2 : 1;
   const int tx_min = seg_pos0 + off;
-  const int tx_max = seg_pos0 + off + n - 1;
+  const int tx_max = seg_pos0 + off + n_all - 1;
 
   // ---- key ranges in fixed slots: 0 prefix rows, 1 trunk, 2 own branch --------------
   // (an absent range has length 0; fixed slots keep every range variable in registers)
@@ -153,6 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::BAR + B_COUNT * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + LY::BAR + B_COUNT * 8 + 8);
+  // per range slot: first tile, tile count, length, first position (read by the softmax
+  // warps, which keep no range variables in registers)
+  int* rtab = reinterpret_cast<int*>(smem + LY::BAR + B_COUNT * 8 + 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -162,18 +177,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars[B_VFULL0 + k], 1);
       tc::mbar_init(&bars[B_KEMPTY0 + k], 1);
       tc::mbar_init(&bars[B_VEMPTY0 + k], 1);
+      tc::mbar_init(&bars[B_SFULL0 + k], 1);
+      tc::mbar_init(&bars[B_PFULL0 + k], 128);
+      tc::mbar_init(&bars[B_OFULL0 + k], 1);
     }
-    tc::mbar_init(&bars[B_SFULL0], 1);
-    tc::mbar_init(&bars[B_SFULL1], 1);
-    tc::mbar_init(&bars[B_SFREE0], 128);
-    tc::mbar_init(&bars[B_SFREE1], 128);
-    tc::mbar_init(&bars[B_PFULL], 128);
-    tc::mbar_init(&bars[B_ODONE], 1);
     tc::mbar_init(&bars[B_FIN], 1);
     *abort = 0;
+    const int tab[12] = {lo0, cnt0, r_len_0, r_pos0_0, lo1, cnt1, r_len_1, r_pos0_1, lo2, cnt2, r_len_2, r_pos0_2};
+    for (int i = 0; i < 12; ++i) rtab[i] = tab[i];
     tc::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -181,14 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  auto tm_s = [&](int st) -> uint32_t { return tmem + static_cast<uint32_t>(st) * 128u; };
-  const uint32_t tm_o = tmem + 256;
+  auto tm_s = [&](int t) -> uint32_t { return tmem + static_cast<uint32_t>(t) * 128u; };
+  auto tm_o = [&](int t) -> uint32_t { return tmem + 256u + static_cast<uint32_t>(t * D); };
   unsigned char* sQ = smem + LY::Q;
   unsigned char* sK = smem + LY::K;
   unsigned char* sV = smem + LY::V;
-  unsigned char* sP = smem + LY::P;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ===================== TMA producer =====================
     if (lane == 0) {
       tc::prefetch_tmap(&qmap);
@@ -198,9 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::prefetch_tmap(&pkmap);
         tc::prefetch_tmap(&pvmap);
       }
-      tc::mbar_expect_tx(&bars[B_QFULL], NB * kBox);
-      for (int b = 0; b < NB; ++b) tc::tma_load_3d(sQ + b * kBox, &qmap, &bars[B_QFULL], b * 64, g * G, seg_start + off);
-      // K_f waits for QK_{f-2} (its slot's previous reader), V_f for PV_{f-2}
+      tc::mbar_expect_tx(&bars[B_QFULL], ntiles * NB * kBox);
+      for (int t = 0; t < ntiles; ++t)
+        for (int b = 0; b < NB; ++b)
+          tc::tma_load_3d(sQ + (t * NB + b) * kBox, &qmap, &bars[B_QFULL], b * 64, g * G,
+                          seg_start + off + t * tile);
+      // K_f waits for the QK^T products of K_{f-2} (its slot's previous reader), V_f for
+      // the PV products of V_{f-2}
       int issued = 0;
       for (int f = 0; f < total; ++f) {
         const int st = f & 1;
@@ -223,177 +240,218 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_wait(&bars[B_VFULL0 + (f & 1)], (f >> 1) & 1, abort);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ===================== MMA issuer =====================
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_bf16(128, kKeys, 0, 0);
-      constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, 0, 1);
-      // descriptors are built once; the start-address field (16-byte units) is then
-      // advanced by constants: +2 per 32-byte k step, +kBox/16 per box
-      const uint64_t dq = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
-      const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
-      const uint64_t dp = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);
-      const uint64_t dv = tc::sdesc_sw128(tc::smem_u32(sV), kBox, 1024);
-      constexpr uint64_t kBoxU = kBox / 16, kStageU = NB * kBox / 16;
-      bool ok = tc::mbar_wait(&bars[B_QFULL], 0, abort);
-      auto issue_pv = [&](int f) -> bool {
-        const int st = f & 1;
-        if (!tc::mbar_wait(&bars[B_VFULL0 + st], (f >> 1) & 1, abort)) return false;
-        if (!tc::mbar_wait(&bars[B_PFULL], f & 1, abort)) return false;
-        tc::tc_fence_after();
-#pragma unroll
-        for (int step = 0; step < kKeys / 16; ++step)
-          tc::mma_bf16(tm_o, dp + (step >> 2) * kBoxU + (step & 3) * 2, dv + st * kStageU + step * (2048 / 16),
-                       idesc_pv, (f > 0 || step > 0) ? 1u : 0u);
-        tc::mma_commit(&bars[B_ODONE]);
-        tc::mma_commit(&bars[B_VEMPTY0 + st]);
-        return true;
-      };
-      for (int f = 0; ok && f < total; ++f) {
-        const int st = f & 1;
-        if (!tc::mbar_wait(&bars[B_KFULL0 + st], (f >> 1) & 1, abort)) { ok = false; break; }
-        if (f >= 2 && !tc::mbar_wait(&bars[B_SFREE0 + st], ((f >> 1) - 1) & 1, abort)) { ok = false; break; }
-        tc::tc_fence_after();
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc::mma_bf16(tm_s(st), dq + b * kBoxU + k * 2, dk + st * kStageU + b * kBoxU + k * 2, idesc_qk,
-                         (b | k) ? 1u : 0u);
-        tc::mma_commit(&bars[B_SFULL0 + st]);
-        tc::mma_commit(&bars[B_KEMPTY0 + st]);
-        if (f >= 1 && !issue_pv(f - 1)) { ok = false; break; }
+    constexpr uint32_t idesc_qk = tc::idesc_bf16(128, kKeys, 0, 0);
+    constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, 0, 1);
+    // descriptors are built once; the start-address field (16-byte units) is then
+    // advanced by constants: +2 per 32-byte k step, +kBox/16 per box
+    const uint64_t dq = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
+    const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
+    const uint64_t dv = tc::sdesc_sw128(tc::smem_u32(sV), kBox, 1024);
+    constexpr uint64_t kBoxU = kBox / 16, kStageU = NB * kBox / 16;
+    // every lane waits; the warp proceeds only if all of them saw the phase complete
+    auto wwait = [&](int b, uint32_t par) -> bool {
+      return __all_sync(0xffffffffu, tc::mbar_wait(&bars[b], par, abort)) != 0;
+    };
+    bool ok = wwait(B_QFULL, 0);
+    const int last_tile = total - 1;
+    // V tile f ready for the PV products; a range that ends inside the tile is followed by
+    // rows that may be pad rows of the stream (any bits), zeroed here: their p is 0 but
+    // 0 * NaN would not be
+    auto v_ready = [&](int f) -> bool {
+      const int st = f & 1;
+      if (!wwait(B_VFULL0 + st, (f >> 1) & 1)) return false;
+      const KT kt = key_tile(f);
+      const int valid_rows = kt.len - kt.t * kKeys;
+      if (kt.r != 0 && valid_rows < kKeys && kt.row0 + kt.t * kKeys + kKeys > meta[H_T]) {
+        // rows [valid_rows, 128) of this slot
+        for (int e = lane; e < (kKeys - valid_rows) * NB * 8; e += 32) {
+          const int r = valid_rows + e / (NB * 8), b = (e / 8) % NB, q = e % 8;
+          *reinterpret_cast<uint4*>(sV + (st * NB + b) * kBox + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+        }
+        tc::fence_proxy_async_smem();
       }
-      if (ok) issue_pv(total - 1);
-      // every MMA issued by this thread has completed before TMEM is released
-      tc::mma_commit(&bars[B_FIN]);
-      tc::mbar_wait(&bars[B_FIN], 0, abort);
-    }
-  } else {
-    // ===================== softmax warps (row = tid) =====================
-    const int row = tid;
-    const int tok = row / G, hl = row % G;
-    const int tx = tx_min + tok;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    bool ok = true;
-    float m_used = -INFINITY, l = 0.f;
-    const float sl2 = p.scale_log2;
+      __syncwarp();
+      return true;
+    };
+    auto issue_pv = [&](int t, int f) {
+      const int st = f & 1;
+      const uint32_t a = tm_s(t);
+#pragma unroll
+      for (int step = 0; step < kKeys / 16; ++step)
+        mma_bf16_ts(tm_o(t), a + step * 8, dv + st * kStageU + step * (2048 / 16), idesc_pv,
+                    (f > 0 || step > 0) ? 1u : 0u);
+    };
+    auto issue_qk = [&](int t, int f) {
+      const int st = f & 1;
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tm_s(t), dq + (t * NB + b) * kBoxU + k * 2, dk + st * kStageU + b * kBoxU + k * 2,
+                       idesc_qk, (b | k) ? 1u : 0u);
+    };
     for (int f = 0; ok && f < total; ++f) {
       const int st = f & 1;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SFULL0 + st], (f >> 1) & 1, abort));
+      if (!wwait(B_KFULL0 + st, (f >> 1) & 1)) { ok = false; break; }
+      if (f > 0 && !v_ready(f - 1)) { ok = false; break; }
+      for (int t = 0; t < ntiles; ++t) {
+        // P_t(f-1) is in the TMEM columns of S_t: the products read it before S_t is rewritten
+        // (tcgen05 MMAs of one thread execute in issue order)
+        if (f > 0) {
+          if (!wwait(B_PFULL0 + t, (f - 1) & 1)) { ok = false; break; }
+          tc::tc_fence_after();
+          if (lane == 0) issue_pv(t, f - 1);
+        }
+        if (lane == 0) {
+          issue_qk(t, f);
+          tc::mma_commit(&bars[B_SFULL0 + t]);
+        }
+        __syncwarp();
+      }
       if (!ok) break;
-      tc::tc_fence_after();
-      float sv[kKeys];
-      {
-        uint32_t rawv[kKeys];
-#pragma unroll
-        for (int i = 0; i < kKeys / 32; ++i) tc::tmem_ld32(tm_s(st) + lane_base + i * 32, rawv + i * 32);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < kKeys; ++cc) sv[cc] = __uint_as_float(rawv[cc]);
+      if (lane == 0) {
+        tc::mma_commit(&bars[B_KEMPTY0 + st]);
+        if (f > 0) tc::mma_commit(&bars[B_VEMPTY0 + (st ^ 1)]);
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&bars[B_SFREE0 + st]);
-      const KT kt = key_tile(f);
-      const int u0 = kt.t * kKeys;
-      const int len = kt.len, p0 = kt.pos0;
-      const bool need_mask = (u0 + kKeys > len) || (p0 + u0 + kKeys - 1 > tx_min) ||
-                             (p.window > 0 && tx_max - (p0 + u0) >= p.window);
-      if (need_mask) {
-        // key u0+cc visible iff inside the range, not after the query, inside the window
-        const int lim_len = len - u0;          // cc < lim_len
-        const int lim_causal = tx - p0 - u0;   // cc <= lim_causal
-        const int lim_win = p.window > 0 ? tx - p0 - u0 - p.window : -0x40000000;  // cc > lim_win
-#pragma unroll
-        for (int cc = 0; cc < kKeys; ++cc)
-          if (cc >= lim_len || cc > lim_causal || cc <= lim_win) sv[cc] = -INFINITY;
+      __syncwarp();
+    }
+    if (ok && v_ready(last_tile)) {
+      for (int t = 0; t < ntiles; ++t) {
+        if (!wwait(B_PFULL0 + t, last_tile & 1)) break;
+        tc::tc_fence_after();
+        if (lane == 0) {
+          issue_pv(t, last_tile);
+          tc::mma_commit(&bars[B_OFULL0 + t]);
+        }
+        __syncwarp();
       }
-      // row maximum (raw scores; the scale is positive)
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = sv[e];
-#pragma unroll
-      for (int cc = 8; cc < kKeys; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], sv[cc]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
-      const bool resc = mt > m_used + kRescale;
-      const float m_new = resc ? mt : m_used;
-      const float base = (m_new == -INFINITY) ? 0.f : m_new;
-      const float factor = resc ? exp2f(m_used - base) : 1.f;  // 0 when nothing was accumulated
-      // p = 2^(s*scale*log2e - base), summed with independent partial sums
-      float ps[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ps[e] = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < kKeys; ++cc) {
-        sv[cc] = fast_exp2(fmaf(sv[cc], sl2, -base));
-        ps[cc & 7] += sv[cc];
-      }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      l = l * factor + rs;
-      m_used = m_new;
-      if (f >= 1) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_ODONE], (f - 1) & 1, abort));
+    }
+    // every MMA issued by this warp has completed before TMEM is released
+    if (lane == 0) tc::mma_commit(&bars[B_FIN]);
+    __syncwarp();
+    wwait(B_FIN, 0);
+  } else {
+    // ===================== softmax warpgroups (tile t = warp / 4, row = tid % 128) ==========
+    const int t = warp >> 2;
+    if (t < ntiles) {
+      const int row = tid & 127;
+      const int tok = row / G, hl = row % G;
+      const int n_t = min(tile, n_all - t * tile);  // valid tokens of this tile
+      const int txm = tx_min + t * tile;            // first position of this tile
+      const int txM = txm + n_t - 1;                // last valid position of this tile
+      const int tx = txm + tok;
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t ts = tm_s(t) + lane_base, to = tm_o(t) + lane_base;
+      bool ok = true;
+      float m_used = -INFINITY, l = 0.f;
+      const float sl2 = p.scale_log2;
+      for (int f = 0; ok && f < total; ++f) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SFULL0 + t], f & 1, abort));
         if (!ok) break;
         tc::tc_fence_after();
-        if (__any_sync(0xffffffffu, factor != 1.f)) {
+        float sv[kKeys];
+        {
+          uint32_t rawv[kKeys];
+#pragma unroll
+          for (int i = 0; i < kKeys / 32; ++i) tc::tmem_ld32(ts + i * 32, rawv + i * 32);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int cc = 0; cc < kKeys; ++cc) sv[cc] = __uint_as_float(rawv[cc]);
+        }
+        int len, p0, u0;
+        {
+          const int c0 = rtab[1], c1 = rtab[5];
+          const int r = f < c0 ? 0 : (f < c0 + c1 ? 1 : 2);
+          const int fr = f - (r == 0 ? 0 : (r == 1 ? c0 : c0 + c1));
+          u0 = (rtab[4 * r] + fr) * kKeys;
+          len = rtab[4 * r + 2];
+          p0 = rtab[4 * r + 3];
+        }
+        const bool need_mask = (u0 + kKeys > len) || (p0 + u0 + kKeys - 1 > txm) ||
+                               (p.window > 0 && txM - (p0 + u0) >= p.window);
+        if (need_mask) {
+          // key u0+cc visible iff inside the range, not after the query, inside the window
+          const int lim_len = len - u0;          // cc < lim_len
+          const int lim_causal = tx - p0 - u0;   // cc <= lim_causal
+          const int lim_win = p.window > 0 ? tx - p0 - u0 - p.window : -0x40000000;  // cc > lim_win
+#pragma unroll
+          for (int cc = 0; cc < kKeys; ++cc)
+            if (cc >= lim_len || cc > lim_causal || cc <= lim_win) sv[cc] = -INFINITY;
+        }
+        // row maximum (raw scores; the scale is positive)
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = sv[e];
+#pragma unroll
+        for (int cc = 8; cc < kKeys; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], sv[cc]);
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        const bool resc = mt > m_used + kRescale;
+        const float m_new = resc ? mt : m_used;
+        const float base = (m_new == -INFINITY) ? 0.f : m_new;
+        const float factor = resc ? exp2f(m_used - base) : 1.f;  // 0 when nothing was accumulated
+        // p = 2^(s*scale*log2e - base), summed with independent partial sums, packed to
+        // bf16 pairs (key order) into the first 64 columns of S_t
+        float ps[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 4; ++h2) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int cc = h2 * 32 + 2 * e;
+            const float a = fast_exp2(fmaf(sv[cc], sl2, -base));
+            const float b = fast_exp2(fmaf(sv[cc + 1], sl2, -base));
+            ps[(2 * e) & 7] += a;
+            ps[(2 * e + 1) & 7] += b;
+            pk[e] = pack_bf16(a, b);
+          }
+          tc::tmem_st16(ts + h2 * 16, pk);
+        }
+        const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        l = l * factor + rs;
+        m_used = m_new;
+        // O_t holds the products of key tiles < f (all complete: S_t(f) was committed after
+        // them) and no product writes it until P_t(f) is published; rescaled after the
+        // exponentials, when the scores no longer occupy registers
+        if (f >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll
           for (int i = 0; i < D / 32; ++i) {
             uint32_t ov[32];
-            tc::tmem_ld32(tm_o + lane_base + i * 32, ov);
+            tc::tmem_ld32(to + i * 32, ov);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
-            tc::tmem_st32(tm_o + lane_base + i * 32, ov);
+            tc::tmem_st32(to + i * 32, ov);
           }
-          tc::tmem_wait_st();
         }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars[B_PFULL0 + t]);
       }
-      // key rows past the range end may be pad rows of the stream: zero them in V
-      if (u0 + kKeys > len) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_VFULL0 + st], (f >> 1) & 1, abort));
-        if (!ok) break;
-        const int valid_rows = max(0, len - u0);
-        if (row >= valid_rows) {
-          unsigned char* vrow = sV + st * NB * kBox + row * 128;
+      if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OFULL0 + t], 0, abort));
+      if (ok) {
+        tc::tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint16_t* orow = p.o + (static_cast<int64_t>(seg_start + off + t * tile + tok) * p.Hq + g * G + hl) * D;
 #pragma unroll
-          for (int b = 0; b < NB; ++b)
+        for (int i = 0; i < D / 32; ++i) {
+          uint32_t ov[32];
+          tc::tmem_ld32(to + i * 32, ov);
+          tc::tmem_wait_ld();
+          if (tok < n_t) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + b * kBox + q * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kKeys / 8; ++q) {
-        uint4 v4;
-        v4.x = pack_bf16(sv[q * 8 + 0], sv[q * 8 + 1]);
-        v4.y = pack_bf16(sv[q * 8 + 2], sv[q * 8 + 3]);
-        v4.z = pack_bf16(sv[q * 8 + 4], sv[q * 8 + 5]);
-        v4.w = pack_bf16(sv[q * 8 + 6], sv[q * 8 + 7]);
-        *reinterpret_cast<uint4*>(sP + sw128_off(row, q * 8)) = v4;
-      }
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_before();
-      tc::mbar_arrive(&bars[B_PFULL]);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_ODONE], (total - 1) & 1, abort));
-    if (ok) {
-      tc::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = p.o + (static_cast<int64_t>(seg_start + off + tok) * p.Hq + g * G + hl) * D;
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        uint32_t ov[32];
-        tc::tmem_ld32(tm_o + lane_base + i * 32, ov);
-        tc::tmem_wait_ld();
-        if (tok < n) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v4;
-            v4.x = pack_bf16(__uint_as_float(ov[q * 8 + 0]) * inv, __uint_as_float(ov[q * 8 + 1]) * inv);
-            v4.y = pack_bf16(__uint_as_float(ov[q * 8 + 2]) * inv, __uint_as_float(ov[q * 8 + 3]) * inv);
-            v4.z = pack_bf16(__uint_as_float(ov[q * 8 + 4]) * inv, __uint_as_float(ov[q * 8 + 5]) * inv);
-            v4.w = pack_bf16(__uint_as_float(ov[q * 8 + 6]) * inv, __uint_as_float(ov[q * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + i * 32 + q * 8) = v4;
+            for (int q = 0; q < 4; ++q) {
+              uint4 v4;
+              v4.x = pack_bf16(__uint_as_float(ov[q * 8 + 0]) * inv, __uint_as_float(ov[q * 8 + 1]) * inv);
+              v4.y = pack_bf16(__uint_as_float(ov[q * 8 + 2]) * inv, __uint_as_float(ov[q * 8 + 3]) * inv);
+              v4.z = pack_bf16(__uint_as_float(ov[q * 8 + 4]) * inv, __uint_as_float(ov[q * 8 + 5]) * inv);
+              v4.w = pack_bf16(__uint_as_float(ov[q * 8 + 6]) * inv, __uint_as_float(ov[q * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + i * 32 + q * 8) = v4;
+            }
           }
         }
       }
@@ -403,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   if (*abort && tid == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_TIMEOUT);
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -413,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---- host side -------------------------------------------------------------------
 
 template <int D>
-int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, cudaStream_t s) {
+int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, bool two_tiles, cudaStream_t s) {
   using LY = TcLayout<D>;
   if (cuda_rc(cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM)) != FORK_OK)
     return FORK_ECUDA;
@@ -426,13 +484,14 @@ int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, cud
   p.G = a.G;
   p.prefix_rows = a.prefix_rows;
   p.window = a.window;
+  p.two_tiles = two_tiles ? 1 : 0;
   p.scale_log2 = a.scale_log2;
   dim3 grid(grid_x, a.Hkv);
   attn_tc_kernel<D><<<grid, kThreads, LY::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cuda_rc(cudaGetLastError());
 }
 
-template int launch_attn_tc<64>(const AttnParams&, const CUtensorMap*, int, cudaStream_t);
-template int launch_attn_tc<128>(const AttnParams&, const CUtensorMap*, int, cudaStream_t);
+template int launch_attn_tc<64>(const AttnParams&, const CUtensorMap*, int, bool, cudaStream_t);
+template int launch_attn_tc<128>(const AttnParams&, const CUtensorMap*, int, bool, cudaStream_t);
 
 }  // namespace fork

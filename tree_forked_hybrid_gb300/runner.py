@@ -45,7 +45,9 @@ class DeviceRound:
         for a in rnd.attn_shapes:
             if a.Hq // a.Hkv != G:
                 raise ValueError("attention layers of one round share the GQA group size")
-        self.tile_tokens = 128 // G
+        # a work item of the tcgen05 attention kernel is two 128-row query tiles
+        # (tokens x grouped heads) that share every key tile; the warp-MMA kernel takes one
+        self.tile_tokens = (128 if flags & F.FORK_WARP_MMA else 256) // G
         self.max_req = max_req or rnd.R
         self.max_q = rnd.Nq if max_q is None else max_q
         self.meta = F.Meta(rnd.T_cap, self.max_req, self.max_q, self.tile_tokens, device)
