@@ -125,20 +125,26 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 3-D bf16 tensor [rows][heads][d] read in boxes of {64 elements, box_heads, box_rows},
-// 128-byte swizzle, zero fill outside the tensor.
-static bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int box_heads,
-                     int box_rows) {
+// 3-D bf16 tensor [rows][heads][d] read in boxes of {box_d elements, box_heads, box_rows}
+// (128-byte swizzle or none), zero fill outside the tensor.
+bool encode_map_3d(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int box_d, int box_heads,
+                   int box_rows, bool swizzle128) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
-  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_d), static_cast<cuuint32_t>(box_heads),
+                       static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[3] = {1u, 1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int box_heads,
+                     int box_rows) {
+  return encode_map_3d(m, base, d, heads, rows, 64, box_heads, box_rows, true);
 }
 
 struct AttnWs {

@@ -44,6 +44,10 @@ __device__ __forceinline__ void rope_cs(const float2* hi, const float2* lo, int 
   *sn = A.y * B.x + A.x * B.y;
 }
 
+// TMA descriptor of a bf16 tensor [rows][heads][d] (fork_attn.cu)
+bool encode_map_3d(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int box_d, int box_heads,
+                   int box_rows, bool swizzle128);
+
 template <int D>
 int launch_attn_mma(const AttnParams& p, int grid_x, cudaStream_t s);
 
