@@ -69,7 +69,7 @@ static_assert(Lay::SMEM <= 232448, "shared memory budget");
 static_assert(3 * kQG * 4 <= 64, "segment table");
 static_assert(Lay::RAW % 128 == 0 && Lay::RAWS % 128 == 0, "TMA destinations");
 
-enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_FINP, B_FINC, B_N };
+enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_OUT, B_FINP, B_FINC, B_N };
 
 // SFU approximations (relative error ~2^-22): 2^x, 1/x, 1/sqrt(x)
 __device__ __forceinline__ float ex2f(float x) {
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(NT, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(sm + Lay::BAR + B_N * 8 + 8);
 
   if (tid == 0) {
-    for (int b = 0; b < B_N; ++b) tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1) ? NCH : 1);
+    for (int b = 0; b < B_N; ++b) tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1 || b == B_OUT) ? NCH : 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -420,8 +420,9 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc::mma_commit(&bars[B_M1]);
       }
-      // P and diag(Gamma_last) K^T are read by the chain's products of chunk k-1
-      if (k >= 1 && !(ok = pwait(B_MB, (k - 1) & 1))) break;
+      // P and diag(Gamma_last) K^T are read by the chain's products of chunk k-1, and the
+      // K^T tile then stages that chunk's output rows until the chain has written them out
+      if (k >= 1 && !(ok = pwait(B_OUT, (k - 1) & 1))) break;
       {
         uint32_t kv4[32];
 #pragma unroll
@@ -735,22 +736,46 @@ __global__ void __launch_bounds__(NT, 1)
                             tc::sdesc_sw128(kt_a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id6, 1u);
         tc::mma_commit(&bars[B_MB]);
       }
-      // ---- C3: output rows (thread = v, one bf16 per token) ----------------------------
+      // ---- C3: output rows.  Thread v holds column v of the chunk's 64 x 128 output; the
+      //      columns are staged as bf16 rows (token-major, 256 bytes each) in the K^T tile,
+      //      free now that the products of this chunk are complete, then written out as
+      //      coalesced 16-byte stores.  Lane pairs swap values so that each shared-memory
+      //      store carries two neighbouring columns of one token; odd rows are rotated by
+      //      64 bytes so that the two tokens of one store instruction use different banks.
       if (!(ok = cwait(B_MB, k & 1))) break;
       tc::tc_fence_after();
       {
-        uint32_t v32[32];
+        const bool odd = lane & 1;
+        const int v0 = v & ~1;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
+          uint32_t v32[32];
           tc::tmem_ld32(tmem + t_x(slot) + q * 32 + lb, v32);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int t = q * 32 + e;
-            if (t < n) p.o[(static_cast<int64_t>(start + c0 + t) * H + h) * D + v] = f2bf(__uint_as_float(v32[e]));
+          for (int e = 0; e < 32; e += 2) {
+            // even lane: (token t, columns v, v+1); odd lane: (token t+1, columns v-1, v)
+            const float mine_t = __uint_as_float(v32[e]), mine_t1 = __uint_as_float(v32[e + 1]);
+            const float other = __shfl_xor_sync(0xffffffffu, odd ? mine_t : mine_t1, 1);
+            const int t = q * 32 + e + (odd ? 1 : 0);
+            const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine_t1) : __floats2bfloat162_rn(mine_t, other);
+            *reinterpret_cast<__nv_bfloat162*>(kt + t * (D * 2) + ((v0 * 2 + (t & 1) * 64) & (D * 2 - 1))) = pr;
           }
         }
       }
+      role_sync(2, NCH);
+      {
+        const int cq = ct & 15;  // 16-byte piece of a 256-byte row
+#pragma unroll
+        for (int pass = 0; pass < C / 8; ++pass) {
+          const int t = pass * 8 + (ct >> 4);
+          if (t < n) {
+            const uint4 val = *reinterpret_cast<const uint4*>(kt + t * (D * 2) + ((cq * 16 + (t & 1) * 64) & (D * 2 - 1)));
+            *reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(start + c0 + t) * H + h) * D + cq * 8) = val;
+          }
+        }
+      }
+      tc::mbar_arrive(&bars[B_OUT]);
       tc::tc_fence_before();
       tc::mbar_arrive(&bars[B_EPI0 + slot]);
       ++k;
