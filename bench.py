@@ -30,6 +30,29 @@ sys.path.insert(0, ROOT)
 WORKLOAD_ID = 3
 METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one call of the full-
+# attention layer on this workload, summed over the call's launches (rotary tables, key and
+# query rotation, attention), from one ncu capture of this bench's command.  Keyed by the
+# SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
+TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
+                       "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
+           "sha256": None, "bytes": None}
+
+
+def _sources_sha256(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic():
+    if TRAFFIC["sha256"] is None or TRAFFIC["bytes"] is None:
+        return None
+    return TRAFFIC["bytes"] if _sources_sha256(TRAFFIC["sources"]) == TRAFFIC["sha256"] else None
+
 
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -241,6 +264,7 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     per_call = {name: statistics.mean(a.elapsed_time(b) for a, b in lst) for name, lst in ev.items()}
+    kernel_alone = attn_kernel_alone(torch, dr, rnd, stream)
     tokens_all = rnd.T * ws
     value = tokens_all * args.steps / (elapsed_ms / 1e3)
     ms_per_step = elapsed_ms / args.steps
@@ -253,10 +277,20 @@ def main():
     if top.startswith("attn_"):
         f = work["attn"][top[5:]]["flops"]
         ach = f / (per_call[top] / 1e3) / 1e12
-        roof = {"kernel": f"fork_attn ({top[5:]}): rotary tables + key rotation + attention",
+        traffic = _traffic() if top == "attn_attn" else None
+        roof = {"kernel": f"fork_attn ({top[5:]}): rotary tables, key and query rotation, attn_tc_kernel",
                 "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"], "traffic": None,
-                "peak_note": f"bf16 dense sustained ({peaks['source']}); kernel timed inside a long step"}
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"], "traffic": traffic,
+                "traffic_unit": "bytes per call (all launches of the call)",
+                "peak_note": f"bf16 dense sustained ({peaks['source']}); call timed inside a long step"}
+        if top == "attn_attn" and kernel_alone:
+            ka = f / (kernel_alone / 1e3) / 1e12
+            roof["kernel_alone"] = {"kernel": "attn_tc_kernel (same round, queries and keys not rotated: the "
+                                              "same visible pairs and FLOPs)",
+                                    "ms": kernel_alone, "achieved": ka, "peak": peaks["bf16_tflops"],
+                                    "frac": ka / peaks["bf16_tflops"],
+                                    "peak_note": f"bf16 dense burst ({peaks['source']}); timed alone after the "
+                                                 "timed region"}
     else:
         key = "gdn" if top.startswith("gdn") else "readout"
         b = work[key]["bytes"] if key != "gdn" else work["gdn"]["bytes"]
@@ -289,6 +323,37 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def attn_kernel_alone(torch, dr, rnd, stream, reps=10):
+    """Mean duration (ms) of the attention kernel alone for the full-attention layer:
+    fork_attn with the rotation off launches only attn_tc_kernel, which does the same
+    visible-pair work as in the step.  Writes a scratch output."""
+    import math
+    from tree_forked_hybrid_gb300 import fork as F
+    a = [x for x in rnd.attn_shapes if x.window == 0]
+    if not a:
+        return None
+    a = a[0]
+    inp = dr.inputs[a.name]
+    out = torch.empty_like(dr.attn_out[a.name])
+
+    def call():
+        F.fork_attn(dr.meta, inp["q"], inp["k"], inp["v"], out, a.Hq, a.Hkv, a.d, a.window, 0.0,
+                    1.0 / math.sqrt(a.d), None, None, None, dr.flags, stream)
+
+    for _ in range(3):
+        call()
+    evs = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(x.elapsed_time(y) for x, y in evs)
 
 
 def e2e(torch, dr, rnd, args, stream, dist, local, ws):

@@ -44,6 +44,7 @@ constexpr int kBox = 128 * 128;  // bytes of one 128-row x 64-element bf16 box
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescale = 8.f;  // move the running max only when it grows by > 2^8
+constexpr int kVStages = 2;      // V ring depth (a third slot measured no faster)
 
 template <int D>
 struct TcLayout {
@@ -51,13 +52,13 @@ struct TcLayout {
   static constexpr int Q = 0;                        // 2 query tiles
   static constexpr int K = Q + 2 * NB * kBox;        // 2 stages
   static constexpr int V = K + 2 * NB * kBox;        // 2 stages
-  static constexpr int BAR = V + 2 * NB * kBox;
+  static constexpr int BAR = V + kVStages * NB * kBox;
   static constexpr int BYTES = BAR + 256;
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);  // one CTA per SM
 };
 
-enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
-           B_VEMPTY1, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_COUNT };
+enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_VFULL2, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
+           B_VEMPTY1, B_VEMPTY2, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -172,11 +173,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     tc::mbar_init(&bars[B_QFULL], 1);
+    for (int k = 0; k < kVStages; ++k) {
+      tc::mbar_init(&bars[B_VFULL0 + k], 1);
+      tc::mbar_init(&bars[B_VEMPTY0 + k], 1);
+    }
     for (int k = 0; k < 2; ++k) {
       tc::mbar_init(&bars[B_KFULL0 + k], 1);
-      tc::mbar_init(&bars[B_VFULL0 + k], 1);
       tc::mbar_init(&bars[B_KEMPTY0 + k], 1);
-      tc::mbar_init(&bars[B_VEMPTY0 + k], 1);
       tc::mbar_init(&bars[B_SFULL0 + k], 1);
       tc::mbar_init(&bars[B_PFULL0 + k], 128);
       tc::mbar_init(&bars[B_OFULL0 + k], 1);
@@ -217,10 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_load_3d(sQ + (t * NB + b) * kBox, &qmap, &bars[B_QFULL], b * 64, g * G,
                           seg_start + off + t * tile);
       // K_f waits for the QK^T products of K_{f-2} (its slot's previous reader), V_f for
-      // the PV products of V_{f-2}
+      // the PV products of V_{f-kVStages}
       int issued = 0;
       for (int f = 0; f < total; ++f) {
-        const int st = f & 1;
+        const int st = f & 1, vs = f % kVStages;
         const KT kt = key_tile(f);
         const CUtensorMap* km = kt.r == 0 ? &pkmap : &kmap;
         const CUtensorMap* vm = kt.r == 0 ? &pvmap : &vmap;
@@ -228,17 +231,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (f >= 2 && !tc::mbar_wait(&bars[B_KEMPTY0 + st], ((f >> 1) - 1) & 1, abort)) break;
         tc::mbar_expect_tx(&bars[B_KFULL0 + st], NB * kBox);
         for (int b = 0; b < NB; ++b) tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KFULL0 + st], b * 64, g, row);
-        if (f >= 2 && !tc::mbar_wait(&bars[B_VEMPTY0 + st], ((f >> 1) - 1) & 1, abort)) break;
-        tc::mbar_expect_tx(&bars[B_VFULL0 + st], NB * kBox);
-        for (int b = 0; b < NB; ++b) tc::tma_load_3d(sV + (st * NB + b) * kBox, vm, &bars[B_VFULL0 + st], b * 64, g, row);
+        if (f >= kVStages && !tc::mbar_wait(&bars[B_VEMPTY0 + vs], ((f / kVStages) - 1) & 1, abort)) break;
+        tc::mbar_expect_tx(&bars[B_VFULL0 + vs], NB * kBox);
+        for (int b = 0; b < NB; ++b) tc::tma_load_3d(sV + (vs * NB + b) * kBox, vm, &bars[B_VFULL0 + vs], b * 64, g, row);
         issued = f + 1;
       }
       // drain: the last loads issued complete by themselves
       tc::mbar_wait(&bars[B_QFULL], 0, abort);
-      for (int f = max(0, issued - 2); f < issued; ++f) {
-        tc::mbar_wait(&bars[B_KFULL0 + (f & 1)], (f >> 1) & 1, abort);
-        tc::mbar_wait(&bars[B_VFULL0 + (f & 1)], (f >> 1) & 1, abort);
-      }
+      for (int f = max(0, issued - 2); f < issued; ++f) tc::mbar_wait(&bars[B_KFULL0 + (f & 1)], (f >> 1) & 1, abort);
+      for (int f = max(0, issued - kVStages); f < issued; ++f)
+        tc::mbar_wait(&bars[B_VFULL0 + f % kVStages], (f / kVStages) & 1, abort);
     }
   } else if (warp == 9) {
     // ===================== MMA issuer =====================
@@ -260,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows that may be pad rows of the stream (any bits), zeroed here: their p is 0 but
     // 0 * NaN would not be
     auto v_ready = [&](int f) -> bool {
-      const int st = f & 1;
-      if (!wwait(B_VFULL0 + st, (f >> 1) & 1)) return false;
+      const int st = f % kVStages;
+      if (!wwait(B_VFULL0 + st, (f / kVStages) & 1)) return false;
       const KT kt = key_tile(f);
       const int valid_rows = kt.len - kt.t * kKeys;
       if (kt.r != 0 && valid_rows < kKeys && kt.row0 + kt.t * kKeys + kKeys > meta[H_T]) {
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     auto issue_pv = [&](int t, int f) {
-      const int st = f & 1;
+      const int st = f % kVStages;
       const uint32_t a = tm_s(t);
 #pragma unroll
       for (int step = 0; step < kKeys / 16; ++step)
@@ -302,7 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (f > 0) {
           if (!wwait(B_PFULL0 + t, (f - 1) & 1)) { ok = false; break; }
           tc::tc_fence_after();
-          if (lane == 0) issue_pv(t, f - 1);
+          if (lane == 0) {
+            issue_pv(t, f - 1);
+            // V_{f-1} has no reader after the last tile's PV products: its slot is
+            // released before the next QK^T products are queued behind them
+            if (t == ntiles - 1) tc::mma_commit(&bars[B_VEMPTY0 + (f - 1) % kVStages]);
+          }
         }
         if (lane == 0) {
           issue_qk(t, f);
@@ -311,10 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) {
-        tc::mma_commit(&bars[B_KEMPTY0 + st]);
-        if (f > 0) tc::mma_commit(&bars[B_VEMPTY0 + (st ^ 1)]);
-      }
+      if (lane == 0) tc::mma_commit(&bars[B_KEMPTY0 + st]);
       __syncwarp();
     }
     if (ok && v_ready(last_tile)) {

@@ -111,6 +111,17 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid
 __device__ __forceinline__ float bf_at(const unsigned char* p) {
   return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
 }
+// 32 consecutive fp32 values (16-byte aligned) into registers with 8 vector loads
+__device__ __forceinline__ void ld32f(const float* src, float* dst) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 v = reinterpret_cast<const float4*>(src)[q];
+    dst[4 * q] = v.x;
+    dst[4 * q + 1] = v.y;
+    dst[4 * q + 2] = v.z;
+    dst[4 * q + 3] = v.w;
+  }
+}
 // barrier over the `n` threads of one role; returns true iff every one of them passed ok
 __device__ __forceinline__ bool role_and(int id, int n, bool ok) {
   uint32_t r;
@@ -264,10 +275,12 @@ __global__ void __launch_bounds__(NT, 1)
       tc::prefetch_tmap(&kmap);
       tc::prefetch_tmap(&vmap);
     }
-    // blocks of T above the diagonal stay zero
+    // blocks of T above the diagonal stay zero (the operand tile, and the blocks (0,1) and
+    // (2,3) of the fp32 copy, which the two-level products read)
     for (int e = tid; e < C * C; e += NP) {
       const int t = e >> 6, s = e & 63;
       if ((s >> 4) > (t >> 4)) *reinterpret_cast<uint32_t*>(tb + swz(64, t, s)) = 0u;
+      if ((s >> 4) == (t >> 4) + 1 && (t >> 4) % 2 == 0) tm[t * LDC + s] = 0.f;
     }
     bool ok = true;
     int si = first_seg(seg_first), c0 = 0, k = 0;
@@ -326,11 +339,13 @@ __global__ void __launch_bounds__(NT, 1)
         const unsigned char* col = raw + 2 * Lay::RAWS + ch * 2;
         float x0 = bf_at(col + (u0 + 0) * D * 2), x1 = bf_at(col + (u0 + 1) * D * 2), x2 = bf_at(col + (u0 + 2) * D * 2);
         uint32_t av[32];
+        float etv[32];
+        ld32f(ETA + u0, etv);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float x3 = bf_at(col + (u0 + e + 3) * D * 2);
           const float y = silu(wv[0] * x0 + wv[1] * x1 + wv[2] * x2 + wv[3] * x3);
-          av[e] = (u0 + e < n) ? tf32_bits(ETA[u0 + e] * y) : 0u;
+          av[e] = (u0 + e < n) ? tf32_bits(etv[e] * y) : 0u;
           x0 = x1;
           x1 = x2;
           x2 = x3;
@@ -384,26 +399,42 @@ __global__ void __launch_bounds__(NT, 1)
       role_sync(1, NP);
       // ---- P5: next chunk's loads (the raw buffer is free); L2 norm of the 128 rows ----
       if (nsi < seg_end) issue_loads(nsi, nc0);
-      // 8 threads per row, 16 channels (four 16-byte chunks) each
-      for (int r = tid >> 3; r < 2 * C; r += NP / 8) {
-        const int l8 = tid & 7;
-        unsigned char* base = qk + (l8 >> 1) * 16384 + r * 128;
-        float4 xv[4];
-        float ss = 0.f;
+      // 8 threads per row, one 16-byte chunk of each of the 4 column boxes: the 8 lanes of
+      // a 16-byte access phase then touch 8 different chunks of one box row (all 32 banks).
+      // A thread's 4 rows (r, r + 32, r + 64, r + 96) are processed two at a time.
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          xv[q] = *reinterpret_cast<const float4*>(base + ((((l8 & 1) * 4 + q) ^ (r & 7)) << 4));
-          ss += xv[q].x * xv[q].x + xv[q].y * xv[q].y + xv[q].z * xv[q].z + xv[q].w * xv[q].w;
+      for (int half = 0; half < 2; ++half) {
+        const int l8 = tid & 7, r0 = (tid >> 3) + 64 * half;
+        float4 xv[2][4];
+        float ss[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = r0 + 32 * i;
+          const unsigned char* base = qk + r * 128 + ((l8 ^ (r & 7)) << 4);
+          ss[i] = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            xv[i][q] = *reinterpret_cast<const float4*>(base + q * 16384);
+            ss[i] += xv[i][q].x * xv[i][q].x + xv[i][q].y * xv[i][q].y + xv[i][q].z * xv[i][q].z + xv[i][q].w * xv[i][q].w;
+          }
         }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-        const float inv = rsqrtf_(ss + 1e-6f);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(base + ((((l8 & 1) * 4 + q) ^ (r & 7)) << 4)) =
-              make_uint4(tf32_bits(xv[q].x * inv), tf32_bits(xv[q].y * inv), tf32_bits(xv[q].z * inv),
-                         tf32_bits(xv[q].w * inv));
+        for (int i = 0; i < 2; ++i) {
+          ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], 1);
+          ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], 2);
+          ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], 4);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = r0 + 32 * i;
+          unsigned char* base = qk + r * 128 + ((l8 ^ (r & 7)) << 4);
+          const float inv = rsqrtf_(ss[i] + 1e-6f);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(base + q * 16384) =
+                make_uint4(tf32_bits(xv[i][q].x * inv), tf32_bits(xv[i][q].y * inv), tf32_bits(xv[i][q].z * inv),
+                           tf32_bits(xv[i][q].w * inv));
+        }
       }
       tc::fence_proxy_async_smem();
       role_sync(1, NP);
@@ -425,11 +456,13 @@ __global__ void __launch_bounds__(NT, 1)
       if (k >= 1 && !(ok = pwait(B_OUT, (k - 1) & 1))) break;
       {
         uint32_t kv4[32];
+        float glv[32];
+        ld32f(GL + u0, glv);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int t = u0 + e;
           const float kv = *reinterpret_cast<const float*>(qk + swz(128, C + t, ch));
-          kv4[e] = tf32_bits(GL[t] * kv);
+          kv4[e] = tf32_bits(glv[e] * kv);
         }
         unsigned char* row = kt + hf * 16384 + ch * 128;
 #pragma unroll
@@ -450,13 +483,22 @@ __global__ void __launch_bounds__(NT, 1)
         // chunk), else 2^{(G_t - G_s) log2 e} per element
         const bool prod = G[C - 1] > -80.f;
         float vals[32];
+        if (prod) {
+          ld32f(IG + u0, vals);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) vals[e] *= egt;
+        } else {
+          ld32f(G + u0, vals);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) vals[e] = ex2f(gt - vals[e] * kLog2e);
+        }
+        // vals = Gamma_{t, u0+e}; masked and scaled by the products
+        const float scale = ch < C ? 1.f : et;
+        const int lim = ch < C ? t : t - 1;  // P keeps s <= t, A keeps s < t
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int s = u0 + e;
-          const float val = __uint_as_float(v32[e]);
-          const float gam = prod ? egt * IG[s] : ex2f(gt - G[s] * kLog2e);
-          if (ch < C) vals[e] = s <= t ? gam * val : 0.f;
-          else vals[e] = s < t ? et * gam * val : 0.f;
+          vals[e] = s <= lim ? scale * vals[e] * __uint_as_float(v32[e]) : 0.f;
         }
         if (ch < C) {
           unsigned char* row = pb + hf * 8192 + t * 128;
@@ -478,10 +520,13 @@ __global__ void __launch_bounds__(NT, 1)
       // (eta e^G K)^T into the TMEM columns of Q K^T, now read by everyone
       {
         uint32_t aw[32];
+        float etv[32], egv[32];
+        ld32f(ETA + u0, etv);
+        ld32f(EG + u0, egv);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int t = u0 + e;
-          aw[e] = tf32_bits(ETA[t] * EG[t] * *reinterpret_cast<const float*>(qk + swz(128, C + t, ch)));
+          aw[e] = tf32_bits(etv[e] * egv[e] * *reinterpret_cast<const float*>(qk + swz(128, C + t, ch)));
         }
         tc::tmem_st32(tmem + T_M1 + u0 + lb, aw);
       }
@@ -507,58 +552,61 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       role_sync(1, NP);
-      // block (bi, bj) = (bj + dist, bj): X = A[bi, bj..bi) T[bj..bi, bj], then T_ij = -T_ii X.
-      // thread = (block, row r, four columns): one float4 of T (or X) per term, so each
-      // shared-memory load feeds four products
+      // Off-diagonal blocks of T in two levels (T_ij = -T_ii A_ij T_jj for a 2 x 2 block
+      // lower-triangular matrix): first the 16 x 16 blocks (1,0) and (3,2), then the 32 x 32
+      // block T_BA = -T_BB (A_BA T_AA) with T_AA, T_BB the two 32 x 32 diagonal blocks.
+      // Thread = (row, four columns): one float4 of T per term, so each shared-memory load
+      // feeds four products.  T's upper blocks (0,1) and (2,3) hold zeros (set at the
+      // start), so the sums run over whole blocks; Y = A_BA T_AA goes to T's unused
+      // upper-right quarter.
+      auto dot16 = [&](const float* arow, const float* bcol, int ldb, float4& acc) {
 #pragma unroll
-      for (int dist = 1; dist < 4; ++dist) {
-        const int npair = 4 - dist;
-        const int pr = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        if (pr < npair) {
-          const int bi = dist + pr, bj = pr;
-          const float* arow = am + (bi * 16 + r) * LDC + bj * 16;
-          const float* tcol = tm + (bj * 16) * LDC + bj * 16 + c4;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m4 = 0; m4 < 16; m4 += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(arow + m4);
+          const float av4[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-          for (int m4 = 0; m4 < 16 * dist; m4 += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(arow + m4);
-            const float av4[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 t4 = *reinterpret_cast<const float4*>(tcol + (m4 + i) * LDC);
-              acc.x += av4[i] * t4.x;
-              acc.y += av4[i] * t4.y;
-              acc.z += av4[i] * t4.z;
-              acc.w += av4[i] * t4.w;
-            }
+          for (int i = 0; i < 4; ++i) {
+            const float4 t4 = *reinterpret_cast<const float4*>(bcol + (m4 + i) * ldb);
+            acc.x += av4[i] * t4.x;
+            acc.y += av4[i] * t4.y;
+            acc.z += av4[i] * t4.z;
+            acc.w += av4[i] * t4.w;
           }
+        }
+      };
+      auto put_t = [&](int row, int col4, const float4& acc) {  // T(row, col4..+3) = -acc
+        const float v4[4] = {-acc.x, -acc.y, -acc.z, -acc.w};
+        *reinterpret_cast<float4*>(tm + row * LDC + col4) = make_float4(v4[0], v4[1], v4[2], v4[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(tb + swz(64, row, col4 + i)) = tf32_bits(v4[i]);
+      };
+      {
+        const int pr = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        const int bi = 2 * pr + 1, bj = 2 * pr;
+        if (tid < 128) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          dot16(am + (bi * 16 + r) * LDC + bj * 16, tm + (bj * 16) * LDC + bj * 16 + c4, LDC, acc);
           *reinterpret_cast<float4*>(xs + (pr << 8) + r * 16 + c4) = acc;
         }
         role_sync(1, NP);
-        if (pr < npair) {
-          const int bi = dist + pr, bj = pr;
-          const float* trow = tm + (bi * 16 + r) * LDC + bi * 16;
-          const float* xcol = xs + (pr << 8) + c4;
+        if (tid < 128) {
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int m4 = 0; m4 < 16; m4 += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(trow + m4);
-            const float av4[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 x4 = *reinterpret_cast<const float4*>(xcol + (m4 + i) * 16);
-              acc.x += av4[i] * x4.x;
-              acc.y += av4[i] * x4.y;
-              acc.z += av4[i] * x4.z;
-              acc.w += av4[i] * x4.w;
-            }
-          }
-          const float v4[4] = {-acc.x, -acc.y, -acc.z, -acc.w};
-          *reinterpret_cast<float4*>(tm + (bi * 16 + r) * LDC + bj * 16 + c4) = make_float4(v4[0], v4[1], v4[2], v4[3]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint32_t*>(tb + swz(64, bi * 16 + r, bj * 16 + c4 + i)) = tf32_bits(v4[i]);
+          dot16(tm + (bi * 16 + r) * LDC + bi * 16, xs + (pr << 8) + c4, 16, acc);
+          put_t(bi * 16 + r, bj * 16 + c4, acc);
         }
+        role_sync(1, NP);
+      }
+      {
+        const int i = tid >> 3, c4 = (tid & 7) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        dot16(am + (32 + i) * LDC, tm + c4, LDC, acc);
+        dot16(am + (32 + i) * LDC + 16, tm + 16 * LDC + c4, LDC, acc);
+        *reinterpret_cast<float4*>(tm + i * LDC + 32 + c4) = acc;
+        role_sync(1, NP);
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        dot16(tm + (32 + i) * LDC + 32, tm + 32 + c4, LDC, acc);
+        dot16(tm + (32 + i) * LDC + 48, tm + 16 * LDC + 32 + c4, LDC, acc);
+        put_t(32 + i, c4, acc);
         role_sync(1, NP);
       }
       // ---- P9: W^T into the X columns of this slot (free once the chain has written out
