@@ -36,7 +36,7 @@ METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 # SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
 TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
                        "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
-           "sha256": None, "bytes": None}
+           "sha256": "ea25ac3eb4f110a6abbff49fc1fc384eed5754927fc447506a0d0bebb08ba388", "bytes": 460163328}
 
 
 def _sources_sha256(paths):
@@ -240,6 +240,7 @@ def main():
         dist.barrier()
     sampler = ClockSampler(_gpu_uuid(torch, local))
     time.sleep(0.3)
+    dr.run()  # one more untimed step after the idle wait for the sampler
     ev = {name: [] for name, _ in calls}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)

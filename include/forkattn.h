@@ -130,8 +130,10 @@ int fork_read_status(const fork_meta* m, int32_t* h_status, void* stream);
  * rotary positions they would have alone).
  * ------------------------------------------------------------------------ */
 
-/* Workspace bytes fork_attn needs: rotated queries and keys of the stream,
- * rotated prefix keys and two small rotary tables (0 when rope_theta == 0). */
+/* Workspace bytes fork_attn needs: rotated keys of the stream, rotated prefix
+ * keys, two small rotary tables, and room for rotated queries (written only
+ * with FORK_WARP_MMA: the default kernel rotates its query tiles in shared
+ * memory).  0 when rope_theta == 0. */
 size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq, int32_t Hkv,
                                  int32_t d, float rope_theta);
 

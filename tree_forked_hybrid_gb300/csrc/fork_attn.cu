@@ -38,75 +38,104 @@ __global__ void rope_tables_kernel(float2* hi, int hi_rows, float2* lo, int half
 
 // Rotate every row of a stream tensor [T_cap, heads, D] (position from the
 // metadata) and of a prefix tensor [prefix_rows, heads, D] (position = row
-// index inside its request's prefix) into the workspace.
+// index inside its request's prefix) into the workspace.  A thread rotates 8
+// pairs (one 16-byte piece of each half) of one head in kRopeRows rows; a block
+// of 256 threads covers kRopeRows * max(1, 256 / (heads * D / 16)) whole rows,
+// so the rows, head and pair group of each thread are fixed (no index division in
+// a loop), and all of a thread's loads are issued before its arithmetic.
+constexpr int kRopeRows = 4;
+
 template <int D>
-__global__ void rope_rows_kernel(const int32_t* __restrict__ meta, MetaLayout L,
+__global__ void __launch_bounds__(256) rope_rows_kernel(const int32_t* __restrict__ meta, MetaLayout L,
                                  const uint16_t* __restrict__ k, const uint16_t* __restrict__ pk,
                                  uint16_t* __restrict__ kr, uint16_t* __restrict__ pkr,
                                  int prefix_rows, int Hkv, const float2* __restrict__ hi,
                                  const float2* __restrict__ lo, int hi_rows) {
   if (meta[H_VALID] == 0) return;
-  const int T = meta[H_T];
-  const int R = meta[H_R];
   constexpr int HALF = D / 2;
   constexpr int GRP = HALF / 8;  // 8 pairs per thread: one 16-byte load from each half
-  const int64_t items = static_cast<int64_t>(T + prefix_rows) * Hkv * GRP;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < items;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int i0 = static_cast<int>(idx % GRP) * 8;
-    const int64_t rh = idx / GRP;  // row * heads + head
-    const int64_t row = rh / Hkv;
-    const uint16_t* src;
-    uint16_t* dst;
-    int t;
-    if (row < T) {
-      t = meta[L.tok_pos + row];
-      src = k + rh * D;
-      dst = kr + rh * D;
-    } else {
-      const int pr = static_cast<int>(row - T);
-      // request owning prefix row pr: last j with prefix_off[j] <= pr
-      int a = 0, b = R;
-      while (b - a > 1) {
-        const int mid = (a + b) >> 1;
-        if (meta[L.req_prefix_off + mid] <= pr) a = mid; else b = mid;
-      }
-      t = pr - meta[L.req_prefix_off + a];
-      src = pk + (rh - static_cast<int64_t>(T) * Hkv) * D;
-      dst = pkr + (rh - static_cast<int64_t>(T) * Hkv) * D;
-    }
-    if (t < 0 || (t >> 6) >= hi_rows) {
-      // position beyond the rotary table: the prefix buffers given to fork_attn are
-      // shorter than the descriptor's prefix lengths
-      atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
-      continue;
-    }
-    const uint4 xa = *reinterpret_cast<const uint4*>(src + i0);
-    const uint4 xb = *reinterpret_cast<const uint4*>(src + i0 + HALF);
-    const float4* A = reinterpret_cast<const float4*>(hi + static_cast<int64_t>(t >> 6) * HALF + i0);
-    const float4* B = reinterpret_cast<const float4*>(lo + static_cast<int64_t>(t & 63) * HALF + i0);
-    const uint32_t aw[4] = {xa.x, xa.y, xa.z, xa.w}, bw[4] = {xb.x, xb.y, xb.z, xb.w};
-    uint32_t oa[4], ob[4];
+  const int per_row = Hkv * GRP;
+  const int nr = per_row >= 256 ? 1 : 256 / per_row;  // rows per block and step
+  const int T = meta[H_T];
+  const int R = meta[H_R];
+  const int64_t rows = static_cast<int64_t>(T) + prefix_rows;
+  for (int item = threadIdx.x; item < nr * per_row; item += blockDim.x) {
+    const int r_local = item / per_row, rem = item - r_local * per_row;
+    const int head = rem / GRP, i0 = (rem % GRP) * 8;
+    int tpos[kRopeRows];
+    uint4 xa[kRopeRows], xb[kRopeRows];
+    uint16_t* dst[kRopeRows];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {  // pairs i0+2q, i0+2q+1
-      const float4 a4 = A[q], b4 = B[q];  // (cos, sin) of the two pairs for 64*(t>>6) and t&63
-      float ya[2], yb[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float ac = e ? a4.z : a4.x, as = e ? a4.w : a4.y;
-        const float bc = e ? b4.z : b4.x, bs = e ? b4.w : b4.y;
-        const float cs = ac * bc - as * bs, sn = as * bc + ac * bs;
-        const float x0 = bf2f(static_cast<uint16_t>(e ? aw[q] >> 16 : aw[q] & 0xffffu));
-        const float x1 = bf2f(static_cast<uint16_t>(e ? bw[q] >> 16 : bw[q] & 0xffffu));
-        ya[e] = x0 * cs - x1 * sn;
-        yb[e] = x1 * cs + x0 * sn;
+    for (int j = 0; j < kRopeRows; ++j) {
+      const int64_t row = (static_cast<int64_t>(blockIdx.x) * kRopeRows + j) * nr + r_local;
+      dst[j] = nullptr;
+      tpos[j] = -1;
+      if (row >= rows) continue;
+      const int64_t rh = row * Hkv + head;  // row * heads + head
+      const uint16_t* src;
+      if (row < T) {
+        tpos[j] = meta[L.tok_pos + row];
+        src = k + rh * D;
+        dst[j] = kr + rh * D;
+      } else {
+        const int pr = static_cast<int>(row - T);
+        // request owning prefix row pr: last j with prefix_off[j] <= pr
+        int a = 0, b = R;
+        while (b - a > 1) {
+          const int mid = (a + b) >> 1;
+          if (meta[L.req_prefix_off + mid] <= pr) a = mid; else b = mid;
+        }
+        tpos[j] = pr - meta[L.req_prefix_off + a];
+        src = pk + (rh - static_cast<int64_t>(T) * Hkv) * D;
+        dst[j] = pkr + (rh - static_cast<int64_t>(T) * Hkv) * D;
       }
-      oa[q] = static_cast<uint32_t>(f2bf(ya[0])) | (static_cast<uint32_t>(f2bf(ya[1])) << 16);
-      ob[q] = static_cast<uint32_t>(f2bf(yb[0])) | (static_cast<uint32_t>(f2bf(yb[1])) << 16);
+      xa[j] = *reinterpret_cast<const uint4*>(src + i0);
+      xb[j] = *reinterpret_cast<const uint4*>(src + i0 + HALF);
     }
-    *reinterpret_cast<uint4*>(dst + i0) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-    *reinterpret_cast<uint4*>(dst + i0 + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+#pragma unroll
+    for (int j = 0; j < kRopeRows; ++j) {
+      if (dst[j] == nullptr) continue;
+      const int t = tpos[j];
+      if (t < 0 || (t >> 6) >= hi_rows) {
+        // position beyond the rotary table: the prefix buffers given to fork_attn are
+        // shorter than the descriptor's prefix lengths
+        atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
+        continue;
+      }
+      const float4* A = reinterpret_cast<const float4*>(hi + static_cast<int64_t>(t >> 6) * HALF + i0);
+      const float4* B = reinterpret_cast<const float4*>(lo + static_cast<int64_t>(t & 63) * HALF + i0);
+      const uint32_t aw[4] = {xa[j].x, xa[j].y, xa[j].z, xa[j].w}, bw[4] = {xb[j].x, xb[j].y, xb[j].z, xb[j].w};
+      uint32_t oa[4], ob[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // pairs i0+2q, i0+2q+1
+        const float4 a4 = A[q], b4 = B[q];  // (cos, sin) of the two pairs for 64*(t>>6) and t&63
+        float ya[2], yb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float ac = e ? a4.z : a4.x, as = e ? a4.w : a4.y;
+          const float bc = e ? b4.z : b4.x, bs = e ? b4.w : b4.y;
+          const float cs = ac * bc - as * bs, sn = as * bc + ac * bs;
+          const float x0 = bf2f(static_cast<uint16_t>(e ? aw[q] >> 16 : aw[q] & 0xffffu));
+          const float x1 = bf2f(static_cast<uint16_t>(e ? bw[q] >> 16 : bw[q] & 0xffffu));
+          ya[e] = x0 * cs - x1 * sn;
+          yb[e] = x1 * cs + x0 * sn;
+        }
+        oa[q] = static_cast<uint32_t>(f2bf(ya[0])) | (static_cast<uint32_t>(f2bf(ya[1])) << 16);
+        ob[q] = static_cast<uint32_t>(f2bf(yb[0])) | (static_cast<uint32_t>(f2bf(yb[1])) << 16);
+      }
+      *reinterpret_cast<uint4*>(dst[j] + i0) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+      *reinterpret_cast<uint4*>(dst[j] + i0 + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    }
   }
+}
+
+// blocks of rope_rows_kernel for rows_cap rows of `heads` heads
+template <int D>
+static int rope_blocks(int64_t rows_cap, int heads) {
+  const int per_row = heads * (D / 16);
+  const int nr = per_row >= 256 ? 1 : 256 / per_row;
+  const int64_t per_block = static_cast<int64_t>(nr) * kRopeRows;
+  return static_cast<int>((rows_cap + per_block - 1) / per_block);
 }
 
 // cuTensorMapEncodeTiled, fetched once through the runtime (no link-time
@@ -215,6 +244,8 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   p.window = window;
   p.rope_theta = rope_theta;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.rope_hi_rows = 0;
+  p.rotate_q = 0;
 
   if (rope_theta != 0.f) {
     const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hq, Hkv, d);
@@ -227,21 +258,31 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     float2* lo = reinterpret_cast<float2*>(ws + w.lo);
     const int hi_rows = static_cast<int>(rope_hi_rows(static_cast<int64_t>(L.T_cap) + prefix_rows));
     rope_tables_kernel<<<2 * 152, 128, 0, s>>>(hi, hi_rows, lo, d / 2, static_cast<double>(rope_theta));
-    const int blocks = 8 * 152;
-    // keys of the stream and of the prefix, then the queries of the stream
+    // keys of the stream and of the prefix (grids from the capacities: blocks past the
+    // round's rows return); the queries here only for the warp-MMA kernel: the tcgen05
+    // kernel rotates each query tile in shared memory once it has landed
+    const int64_t krows = static_cast<int64_t>(L.T_cap) + prefix_rows;
     if (d == 64) {
-      rope_rows_kernel<64><<<blocks, 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows, Hkv, hi, lo, hi_rows);
-      rope_rows_kernel<64><<<blocks, 256, 0, s>>>(p.meta, L, q, nullptr, qr, nullptr, 0, Hq, hi, lo, hi_rows);
+      rope_rows_kernel<64><<<rope_blocks<64>(krows, Hkv), 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows,
+                                                                        Hkv, hi, lo, hi_rows);
+      if (warp_mma)
+        rope_rows_kernel<64><<<rope_blocks<64>(L.T_cap, Hq), 256, 0, s>>>(p.meta, L, q, nullptr, qr, nullptr, 0, Hq,
+                                                                           hi, lo, hi_rows);
     } else {
-      rope_rows_kernel<128><<<blocks, 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows, Hkv, hi, lo, hi_rows);
-      rope_rows_kernel<128><<<blocks, 256, 0, s>>>(p.meta, L, q, nullptr, qr, nullptr, 0, Hq, hi, lo, hi_rows);
+      rope_rows_kernel<128><<<rope_blocks<128>(krows, Hkv), 256, 0, s>>>(p.meta, L, k, prefix_k, kr, pkr, prefix_rows,
+                                                                          Hkv, hi, lo, hi_rows);
+      if (warp_mma)
+        rope_rows_kernel<128><<<rope_blocks<128>(L.T_cap, Hq), 256, 0, s>>>(p.meta, L, q, nullptr, qr, nullptr, 0,
+                                                                             Hq, hi, lo, hi_rows);
     }
-    p.q = qr;
+    if (warp_mma) p.q = qr;
     p.k = kr;
     p.prefix_k = pkr;
     p.rope_hi = hi;
     p.rope_lo = lo;
-    p.rope_theta = 0.f;  // queries are already rotated
+    p.rope_hi_rows = hi_rows;
+    p.rotate_q = warp_mma ? 0 : 1;
+    p.rope_theta = 0.f;  // keys rotated; queries rotated above or by the attention kernel
   }
   if (cuda_rc(cudaGetLastError()) != FORK_OK) return FORK_ECUDA;
   const int grid_x = static_cast<int>(std::min<int64_t>(

@@ -32,6 +32,8 @@ struct AttnParams {
   int window;
   float rope_theta;          // 0 = off
   float scale_log2;          // scale * log2(e)
+  int rope_hi_rows;          // rows of rope_hi
+  int rotate_q;              // queries are rotated by the attention kernel (tcgen05 path)
 };
 
 // (cos, sin) of t * f_i from the two-level table: t = 64 a + b,

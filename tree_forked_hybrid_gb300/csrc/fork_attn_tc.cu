@@ -58,7 +58,8 @@ struct TcLayout {
 };
 
 enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_VFULL2, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
-           B_VEMPTY1, B_VEMPTY2, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_COUNT };
+           B_VEMPTY1, B_VEMPTY2, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_QROT,
+           B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -88,9 +89,51 @@ struct TcParams {
   const int32_t* meta;
   MetaLayout L;
   uint16_t* o;
-  int Hq, Hkv, G, prefix_rows, window, two_tiles;
+  const float2* rope_hi;  // (cos, sin) tables of the rotary embedding (rotate_q)
+  const float2* rope_lo;
+  int Hq, Hkv, G, prefix_rows, window, two_tiles, rotate_q, rope_hi_rows;
   float scale_log2;
 };
+
+// Rotary embedding of one query row held in a 128-byte-swizzled tile (boxes of 64
+// elements, 128 bytes per row): pairs (i, i + D/2) at position tpos, 8 pairs per step
+// (one 16-byte piece of each half; both pieces sit at the same swizzled chunk when D =
+// 128).  (cos, sin) by angle addition from the two-level table, as in the rotation pass.
+template <int D>
+__device__ __forceinline__ void rotate_q_row(unsigned char* tile, int row, int tpos, const float2* __restrict__ hi,
+                                             const float2* __restrict__ lo) {
+  constexpr int HALF = D / 2;
+  const float4* A = reinterpret_cast<const float4*>(hi + static_cast<int64_t>(tpos >> 6) * HALF);
+  const float4* B = reinterpret_cast<const float4*>(lo + static_cast<int64_t>(tpos & 63) * HALF);
+#pragma unroll 2
+  for (int c = 0; c < HALF / 8; ++c) {
+    const int ea = 8 * c, eb = ea + HALF;
+    uint4* pa = reinterpret_cast<uint4*>(tile + (ea >> 6) * kBox + row * 128 + ((((ea & 63) >> 3) ^ (row & 7)) << 4));
+    uint4* pb = reinterpret_cast<uint4*>(tile + (eb >> 6) * kBox + row * 128 + ((((eb & 63) >> 3) ^ (row & 7)) << 4));
+    const uint4 xa = *pa, xb = *pb;
+    const uint32_t aw[4] = {xa.x, xa.y, xa.z, xa.w}, bw[4] = {xb.x, xb.y, xb.z, xb.w};
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // pairs ea+2q, ea+2q+1
+      const float4 a4 = A[c * 4 + q], b4 = B[c * 4 + q];
+      float ya[2], yb[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float ac = e ? a4.z : a4.x, as = e ? a4.w : a4.y;
+        const float bc = e ? b4.z : b4.x, bs = e ? b4.w : b4.y;
+        const float cs = ac * bc - as * bs, sn = as * bc + ac * bs;
+        const float x0 = bf2f(static_cast<uint16_t>(e ? aw[q] >> 16 : aw[q] & 0xffffu));
+        const float x1 = bf2f(static_cast<uint16_t>(e ? bw[q] >> 16 : bw[q] & 0xffffu));
+        ya[e] = x0 * cs - x1 * sn;
+        yb[e] = x1 * cs + x0 * sn;
+      }
+      oa[q] = static_cast<uint32_t>(f2bf(ya[0])) | (static_cast<uint32_t>(f2bf(ya[1])) << 16);
+      ob[q] = static_cast<uint32_t>(f2bf(yb[0])) | (static_cast<uint32_t>(f2bf(yb[1])) << 16);
+    }
+    *pa = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *pb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -185,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars[B_OFULL0 + k], 1);
     }
     tc::mbar_init(&bars[B_FIN], 1);
+    tc::mbar_init(&bars[B_QROT], 256);
     *abort = 0;
     const int tab[12] = {lo0, cnt0, r_len_0, r_pos0_0, lo1, cnt1, r_len_1, r_pos0_1, lo2, cnt2, r_len_2, r_pos0_2};
     for (int i = 0; i < 12; ++i) rtab[i] = tab[i];
@@ -256,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wwait = [&](int b, uint32_t par) -> bool {
       return __all_sync(0xffffffffu, tc::mbar_wait(&bars[b], par, abort)) != 0;
     };
-    bool ok = wwait(B_QFULL, 0);
+    bool ok = wwait(p.rotate_q ? B_QROT : B_QFULL, 0);
     const int last_tile = total - 1;
     // V tile f ready for the PV products; a range that ends inside the tile is followed by
     // rows that may be pad rows of the stream (any bits), zeroed here: their p is 0 but
@@ -339,6 +383,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ===================== softmax warpgroups (tile t = warp / 4, row = tid % 128) ==========
     const int t = warp >> 2;
+    if (p.rotate_q) {
+      // rotary embedding of the query tiles in shared memory, thread = row, once they have
+      // landed; the products read them after every thread's fence and arrival
+      const bool okq = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_QFULL], 0, abort));
+      if (okq && t < ntiles) {
+        const int row = tid & 127, tok = row / G;
+        if (tok < min(tile, n_all - t * tile)) {
+          const int tpos = tx_min + t * tile + tok;
+          if (tpos >> 6 < p.rope_hi_rows) rotate_q_row<D>(sQ + t * NB * kBox, row, tpos, p.rope_hi, p.rope_lo);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars[B_QROT]);
+    }
     if (t < ntiles) {
       const int row = tid & 127;
       const int tok = row / G, hl = row % G;
@@ -489,6 +547,10 @@ int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, boo
   p.prefix_rows = a.prefix_rows;
   p.window = a.window;
   p.two_tiles = two_tiles ? 1 : 0;
+  p.rotate_q = a.rotate_q;
+  p.rope_hi = a.rope_hi;
+  p.rope_lo = a.rope_lo;
+  p.rope_hi_rows = a.rope_hi_rows;
   p.scale_log2 = a.scale_log2;
   dim3 grid(grid_x, a.Hkv);
   attn_tc_kernel<D><<<grid, kThreads, LY::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
