@@ -36,7 +36,7 @@ METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 # SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
 TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
                        "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
-           "sha256": "ea25ac3eb4f110a6abbff49fc1fc384eed5754927fc447506a0d0bebb08ba388", "bytes": 460163328}
+           "sha256": "05bcebf9af2dfac67abbafe77c15605bf0cef673b97c45a9fd9f89aa8f79e9cf", "bytes": 459936000}
 
 
 def _sources_sha256(paths):

@@ -105,7 +105,7 @@ __device__ __forceinline__ void rotate_q_row(unsigned char* tile, int row, int t
   constexpr int HALF = D / 2;
   const float4* A = reinterpret_cast<const float4*>(hi + static_cast<int64_t>(tpos >> 6) * HALF);
   const float4* B = reinterpret_cast<const float4*>(lo + static_cast<int64_t>(tpos & 63) * HALF);
-#pragma unroll 2
+#pragma unroll
   for (int c = 0; c < HALF / 8; ++c) {
     const int ea = 8 * c, eb = ea + HALF;
     uint4* pa = reinterpret_cast<uint4*>(tile + (ea >> 6) * kBox + row * 128 + ((((ea & 63) >> 3) ^ (row & 7)) << 4));
@@ -385,7 +385,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;
     if (p.rotate_q) {
       // rotary embedding of the query tiles in shared memory, thread = row, once they have
-      // landed; the products read them after every thread's fence and arrival
+      // landed; the products read them after every thread's fence and arrival.  The row's
+      // two table rows (512 bytes each) are prefetched into L1 while the tiles load.
+      if (t < ntiles) {
+        const int tok = (tid & 127) / G;
+        const int tpos = tx_min + t * tile + min(tok, tile - 1);
+        if (tpos >> 6 < p.rope_hi_rows) {
+          const char* ha = reinterpret_cast<const char*>(p.rope_hi + static_cast<int64_t>(tpos >> 6) * (D / 2));
+          const char* la = reinterpret_cast<const char*>(p.rope_lo + static_cast<int64_t>(tpos & 63) * (D / 2));
+#pragma unroll
+          for (int o = 0; o < D * 4; o += 128) {
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(ha + o));
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(la + o));
+          }
+        }
+      }
       const bool okq = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_QFULL], 0, abort));
       if (okq && t < ntiles) {
         const int row = tid & 127, tok = row / G;
