@@ -205,6 +205,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the short-request round eagerly and as one CUDA graph replay")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -313,6 +315,11 @@ def main():
 
     if not args.no_e2e:
         out["e2e"] = e2e(torch, dr, rnd, args, stream, dist, local, ws)
+    if args.graph:
+        try:
+            out["graph_replay"] = graph_timing(torch, args, local)
+        except Exception as exc:  # reported, never fatal for the main line
+            out["graph_replay"] = {"error": f"{type(exc).__name__}: {exc}"}
     if rank == 0 and ws == 1 and not args.no_cpu:
         n, dt = oracle_sample(rnd, None, 1)
         out["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
@@ -324,6 +331,37 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def graph_timing(torch, args, local, wid=1):
+    """Round latency of the short-request round (32 requests, 14.9k tokens): the layer's
+    calls launched one by one, and the same calls replayed from one CUDA graph."""
+    from tree_forked_hybrid_gb300 import workloads as wl
+    from tree_forked_hybrid_gb300.runner import DeviceRound, GraphRound
+    rnd = wl.make_round(wid)
+    dr = DeviceRound(rnd, device=f"cuda:{local}")
+    g = GraphRound(DeviceRound(rnd, device=f"cuda:{local}"))
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    eager = timed(dr.run)
+    graph = timed(g.replay)
+    if g.dr.status() != 0 or dr.status() != 0:
+        raise RuntimeError("device status set")
+    return {"workload": f"short requests: R={rnd.R}, T={rnd.T}, T_cap={rnd.T_cap}", "eager_ms": eager,
+            "graph_ms": graph, "launches_per_round": dr.launches_per_round()}
 
 
 def attn_kernel_alone(torch, dr, rnd, stream, reps=10):

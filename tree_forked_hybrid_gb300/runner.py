@@ -137,5 +137,54 @@ class DeviceRound:
     def launches_per_round(self) -> int:
         n = 2  # metadata: tables + tokens
         for a in self.rnd.attn_shapes:
-            n += 4 if a.rope_theta else 1  # rotary tables + keys + queries + attention
+            # rotary tables + keys (+ queries for the warp-MMA kernel) + attention
+            n += (4 if self.flags & F.FORK_WARP_MMA else 3) if a.rope_theta else 1
         return n + 3  # gdn trunk, gdn branches, readout
+
+
+class GraphRound:
+    """The whole layer of one round captured as a single CUDA graph.
+
+    Launch shapes depend only on the capacities and the shape arguments, and
+    no call reads the device back, so ``DeviceRound.run`` captures as is: the
+    metadata build reads the descriptor from device memory, and every later
+    kernel takes its segments from the metadata.  A new round with the same
+    request and question counts (other lengths, other values) replays the
+    graph after ``load`` has copied its descriptor and inputs into the
+    captured buffers.  The onedev summary ("어떻게 쓰나") captures one graph
+    per capacity bucket the same way.
+    """
+
+    def __init__(self, dr: DeviceRound):
+        self.dr = dr
+        side = torch.cuda.Stream(device=dr.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # first calls outside capture (function attributes, entry points)
+            dr.run()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
+            dr.run()
+        torch.cuda.synchronize()
+
+    def load(self, rnd: Round):
+        """Copy another round's descriptor and inputs into the captured buffers."""
+        dr = self.dr
+        if rnd.R != dr.rnd.R or rnd.Nq != dr.rnd.Nq or rnd.T_cap != dr.rnd.T_cap:
+            raise ValueError("the graph was captured for another request/question count or capacity")
+        if int(rnd.opt_off[-1]) > dr.p.numel() or rnd.w_opt.shape[0] > dr.w_opt.shape[0]:
+            raise ValueError("more options than the captured buffers hold")
+        if int(rnd.prefix_len.sum()) != dr.prefix_rows:
+            raise ValueError("the graph was captured for another number of prefix rows")
+        dr.desc.copy_(torch.from_numpy(rnd.desc()))
+        for name, lay in rnd.layers.items():
+            for k, v in lay.items():
+                src = _bf16(v, "cpu") if v.dtype == np.uint16 else _f32(v, "cpu")
+                dr.inputs[name][k].copy_(src)
+        dr.w_opt[:rnd.w_opt.shape[0]].copy_(_bf16(rnd.w_opt, "cpu"))
+        dr.opt_off.copy_(torch.from_numpy(rnd.opt_off.astype(np.int32)))
+        dr.rnd = rnd
+
+    def replay(self):
+        self.graph.replay()
