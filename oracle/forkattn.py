@@ -360,6 +360,46 @@ def readout(h: np.ndarray, w: np.ndarray, off: np.ndarray, dtype=np.float32) -> 
     return p
 
 
+# ----------------------------------------------------------------------------
+# Selective readout with the final pointwise block on the question rows only
+# (onedev "어떻게 쓰나": in the last layer the MLP and what follows run only on
+# each question's last-token row, which changes no output).  The pages give no
+# form for the block; reading R10: pre-norm SwiGLU MLP with a residual, then a
+# final RMSNorm, then eq. (1); RMSNorm x * (mean x^2 + 1e-6)^(-1/2) * g; the
+# two GEMM inputs (normalised row, gated activation) are stored as bfloat16
+# as in a bf16 model; everything else in `dtype`.
+# ----------------------------------------------------------------------------
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 values rounded to the nearest bfloat16 (ties to even), as float32."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    keep = (u >> 16) & 1
+    r = ((u + 0x7FFF + keep) >> 16) << 16
+    return (r & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+
+
+def rms_norm(x: np.ndarray, g: np.ndarray, eps: float = 1e-6, dtype=np.float32) -> np.ndarray:
+    x = x.astype(dtype)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + dtype(eps)) * g.astype(dtype)
+
+
+def mlp_block(h: np.ndarray, g1, w_gate, w_up, w_down, dtype=np.float32) -> np.ndarray:
+    """y = h + W_down (silu(W_gate n) * (W_up n)), n = bf16(rms_norm(h, g1)); rows independent."""
+    n = round_to_bf16(rms_norm(h, g1, dtype=np.float32)).astype(dtype)
+    gate = n @ w_gate.astype(dtype).T
+    up = n @ w_up.astype(dtype).T
+    a = round_to_bf16((silu(gate) * up).astype(np.float32)).astype(dtype)
+    return h.astype(dtype) + a @ w_down.astype(dtype).T
+
+
+def readout_mlp(h: np.ndarray, g1, w_gate, w_up, w_down, g2, w: np.ndarray, off: np.ndarray,
+                dtype=np.float32) -> np.ndarray:
+    """Eq. (1) on z = rms_norm(mlp_block(h), g2), h [Nq, D] the questions' last-token rows."""
+    y = mlp_block(h, g1, w_gate, w_up, w_down, dtype)
+    return readout(rms_norm(y, g2, dtype=dtype), w, off, dtype)
+
+
 def total_variation(p: np.ndarray, r: np.ndarray, off: np.ndarray) -> np.ndarray:
     """TV(P, Q) = 1/2 sum |p - q| per question (rainbus "前置知识")."""
     return np.array([0.5 * np.abs(p[off[i]:off[i + 1]] - r[off[i]:off[i + 1]]).sum()
@@ -515,4 +555,8 @@ PINS = {
     "causal_conv": "numpy.convolve per channel",
     "gdn_sequence": "literal matrix form, eta=0, delta-rule recall, orthonormal keys, resume==scratch",
     "readout": "scipy.special.softmax, |O|=1, equal logits, sum to one",
+    "round_to_bf16": "bit patterns of hand-picked ties and carries; idempotent; exact for bf16 values",
+    "rms_norm": "constant rows map to sign * g; unit mean square; scale invariance",
+    "mlp_block": "W_down = 0 gives h; literal per-row loop in fp64; rows independent (selective = full)",
+    "readout_mlp": "W_down = 0 and g2 = 1 reduce to eq. (1) on rms_norm(h)",
 }
