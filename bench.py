@@ -205,6 +205,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--readout-mlp", action="store_true",
+                    help="also time the selective-readout block (norm, SwiGLU MLP, final norm, eq. (1))")
     ap.add_argument("--graph", action="store_true",
                     help="also time the short-request round eagerly and as one CUDA graph replay")
     args = ap.parse_args()
@@ -315,6 +317,11 @@ def main():
 
     if not args.no_e2e:
         out["e2e"] = e2e(torch, dr, rnd, args, stream, dist, local, ws)
+    if args.readout_mlp:
+        try:
+            out["readout_mlp"] = readout_mlp_timing(torch, dr, rnd, stream, peaks)
+        except Exception as exc:  # reported, never fatal for the main line
+            out["readout_mlp"] = {"error": f"{type(exc).__name__}: {exc}"}
     if args.graph:
         try:
             out["graph_replay"] = graph_timing(torch, args, local)
@@ -331,6 +338,41 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def readout_mlp_timing(torch, dr, rnd, stream, peaks, reps=20):
+    """The selective-readout block on this round's question rows (D = H*dv, F = 2D):
+    mean CUDA-event time, against the HBM roofline of its weight bytes."""
+    import numpy as np
+    from tree_forked_hybrid_gb300 import fork as F
+    from tree_forked_hybrid_gb300 import workloads as wl
+    D = rnd.D
+    Fw = 2 * D
+    wts = wl.readout_block_weights(D, Fw)
+    dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dr.device)
+    W = {k: dev(v) for k, v in wts.items()}
+    ws = torch.empty(F.fork_readout_mlp_workspace_bytes(dr.max_q, D, Fw), dtype=torch.uint8, device=dr.device)
+    p = torch.empty_like(dr.p)
+
+    def call():
+        F.fork_readout_mlp(dr.meta, dr.gdn_out, D, Fw, W["g1"], W["w_gate"], W["w_up"], W["w_down"], W["g2"],
+                           dr.w_opt, dr.opt_off, p, ws, 0, stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = 3 * D * Fw * 2 + rnd.Nq * D * 2 + int(rnd.opt_off[-1]) * D * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"block": f"Nq={rnd.Nq} rows, D={D}, F={Fw}", "ms": ms, "bytes": nbytes, "achieved_gbs": gbs,
+            "frac_hbm": gbs / peaks["hbm_gbs"], "flops": 6 * rnd.Nq * D * Fw}
 
 
 def graph_timing(torch, args, local, wid=1):

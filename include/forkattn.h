@@ -236,6 +236,33 @@ int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const uint16_t* k, 
 int fork_readout(const fork_meta* m, const uint16_t* h, int32_t D, const uint16_t* w_opt,
                  const int32_t* opt_off, float* p, uint32_t flags, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Selective readout with the last layer's pointwise block on the question
+ * rows only (onedev "어떻게 쓰나": the MLP and what follows run only on each
+ * question's last-token row, which changes no output).  The pages give no
+ * form for the block; this one is a pre-norm SwiGLU MLP with a residual and a
+ * final RMSNorm, rmsnorm(x) = x * (mean x^2 + 1e-6)^(-1/2):
+ *   n_i = bf16(rmsnorm(h_i) * g1),  a_i = bf16(silu(W_gate n_i) * (W_up n_i)),
+ *   y_i = h_i + W_down a_i,  z_i = rmsnorm(y_i) * g2,
+ *   p_i(o) = exp(w_o . z_i) / sum_{o' in O_i} exp(w_o' . z_i).
+ *   h [T_cap, D] bf16 (rows read at each question's last token); g1, g2 [D]
+ *   float32; w_gate, w_up [F, D] and w_down [D, F] bf16, row-major; w_opt,
+ *   opt_off, p as for fork_readout.  D a multiple of 64, at most 8192; F a
+ *   multiple of 64, at most 65536.  Products on the tensor cores with bf16
+ *   operands and float32 accumulation; norms, SiLU and eq. (1) in float32.
+ *   workspace: device buffer of fork_readout_mlp_workspace_bytes(max_q, D,
+ *   F) bytes, 16-byte aligned, owned by the caller (the normalised rows
+ *   [Mpad, D] bf16, the activations [Mpad, F] bf16 and y [Mpad, D] float32,
+ *   each at a 256-byte-aligned offset, Mpad = max_q rounded up to 64).
+ *   FORK_EINVAL for null pointers, bad sizes, misaligned buffers or a short
+ *   workspace, with nothing launched.
+ * ------------------------------------------------------------------------ */
+size_t fork_readout_mlp_workspace_bytes(int32_t max_q, int32_t D, int32_t F);
+int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D, int32_t F, const float* g1,
+                     const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                     const float* g2, const uint16_t* w_opt, const int32_t* opt_off, float* p,
+                     void* workspace, size_t ws_bytes, uint32_t flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,6 +68,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fork_gdn_branches": (ctypes.c_int, [MP, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                              u32, vp]),
         "fork_readout": (ctypes.c_int, [MP, vp, i32, vp, vp, vp, u32, vp]),
+        "fork_readout_mlp_workspace_bytes": (sz, [i32, i32, i32]),
+        "fork_readout_mlp": (ctypes.c_int, [MP, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, u32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -172,3 +174,15 @@ def fork_gdn_branches(meta: Meta, q, k, v, alpha, eta, conv_w, H: int, d: int, K
 def fork_readout(meta: Meta, h, D: int, w_opt, opt_off, p, flags: int = 0, stream=None):
     _check("fork_readout", load().fork_readout(meta.ref, _ptr(h), D, _ptr(w_opt), _ptr(opt_off), _ptr(p),
                                                flags, _stream(stream)))
+
+
+def fork_readout_mlp_workspace_bytes(max_q: int, D: int, F: int) -> int:
+    return load().fork_readout_mlp_workspace_bytes(max_q, D, F)
+
+
+def fork_readout_mlp(meta: Meta, h, D: int, F: int, g1, w_gate, w_up, w_down, g2, w_opt, opt_off, p,
+                     workspace, flags: int = 0, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fork_readout_mlp", load().fork_readout_mlp(
+        meta.ref, _ptr(h), D, F, _ptr(g1), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(g2), _ptr(w_opt),
+        _ptr(opt_off), _ptr(p), _ptr(workspace), ws_bytes, flags, _stream(stream)))

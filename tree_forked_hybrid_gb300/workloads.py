@@ -354,3 +354,16 @@ def custom_round(trunk_len, n_q, q_len, *, attn_shapes, gdn_shape, T_cap, seed=0
                 prefix=pref)
     rnd._rng = rng
     return rnd
+
+
+def readout_block_weights(D: int, F: int, seed: int = 7):
+    """Seeded weights of the last layer's pointwise block (selective readout):
+    norm gains g1, g2 = 1 + N(0, 0.1^2) (float32); W_gate, W_up [F, D] ~ N(0, 1/D)
+    and W_down [D, F] ~ N(0, 1/F), rounded to bfloat16 (uint16 bit patterns)."""
+    rng = np.random.default_rng(seed)
+    g1 = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    g2 = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wg = bf16_bits(rng.standard_normal((F, D), dtype=np.float32) * np.float32(1.0 / math.sqrt(D)))
+    wu = bf16_bits(rng.standard_normal((F, D), dtype=np.float32) * np.float32(1.0 / math.sqrt(D)))
+    wd = bf16_bits(rng.standard_normal((D, F), dtype=np.float32) * np.float32(1.0 / math.sqrt(F)))
+    return {"g1": g1, "g2": g2, "w_gate": wg, "w_up": wu, "w_down": wd}
