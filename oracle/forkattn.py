@@ -547,6 +547,69 @@ def run_readout(view: RoundView, h_stream: np.ndarray, w: np.ndarray, off: np.nd
     return readout(h, w, off, dtype)
 
 
+# ----------------------------------------------------------------------------
+# Token trees: branches that fork again (rainbus summary "未来方向" (2): a tree of
+# draft tokens has the shape of a request tree and runs in the same flat
+# stream).  Every node's result is that of its own sequence, its ancestors'
+# tokens followed by its own, run from scratch: the exactness statement at
+# every fork.
+# ----------------------------------------------------------------------------
+
+
+def run_tree(layers: Dict[str, Dict[str, np.ndarray]], parent: np.ndarray, node_len: np.ndarray,
+             attn: Sequence[tuple], gdn_name: str, w: np.ndarray, off: np.ndarray, dtype=np.float32):
+    """Outputs of a forest of token trees, node by node.
+
+    layers[name][field]: float32 rows of all nodes, node after node; attn: (name,
+    window, rope_theta) per attention layer.  Returns dict: "attn" {name: [T, Hq, d]},
+    "gdn" [T, H, dv], "S_end" [N, H, dv, dk] (state after the node's last token),
+    "p" (eq. (1) at each leaf's last token, leaves in node order).
+    """
+    N = parent.shape[0]
+    start = np.concatenate([[0], np.cumsum(node_len)[:-1]]).astype(np.int64)
+    T = int(node_len.sum())
+
+    def chain(k):
+        c = [k]
+        while parent[c[-1]] >= 0:
+            c.append(int(parent[c[-1]]))
+        return c[::-1]
+
+    def seq(name, field, k):
+        return np.concatenate([layers[name][field][start[a]:start[a] + node_len[a]] for a in chain(k)], axis=0)
+
+    out = {"attn": {}, "S_end": None}
+    for name, window, theta in attn:
+        Hq, d = layers[name]["q"].shape[1:]
+        o_all = np.zeros((T, Hq, d), dtype=dtype)
+        for k in range(N):
+            L = int(node_len[k])
+            if L == 0:
+                continue
+            q, kk, v = seq(name, "q", k), seq(name, "k", k), seq(name, "v", k)
+            rows = np.arange(q.shape[0] - L, q.shape[0])
+            o_all[start[k]:start[k] + L] = attention_sequence(q, kk, v, window=window, rope_theta=theta,
+                                                              dtype=dtype, rows=rows)
+        out["attn"][name] = o_all
+    lay = layers[gdn_name]
+    H, dk = lay["q"].shape[1:]
+    dv = lay["v"].shape[2]
+    o_all = np.zeros((T, H, dv), dtype=dtype)
+    S_end = np.zeros((N, H, dv, dk), dtype=dtype)
+    for k in range(N):
+        q, kk, v, a, e = (seq(gdn_name, f, k) for f in ("q", "k", "v", "alpha", "eta"))
+        o, S, _, _ = gdn_sequence(q, kk, v, a, e, lay["conv_w"], dtype=dtype)
+        L = int(node_len[k])
+        o_all[start[k]:start[k] + L] = o[q.shape[0] - L:]
+        S_end[k] = S
+    out["gdn"] = o_all
+    out["S_end"] = S_end
+    leaves = [k for k in range(N) if not np.any(parent == k)]
+    last = np.array([start[k] + node_len[k] - 1 for k in leaves], dtype=np.int64)
+    out["p"] = readout(o_all[last].reshape(len(leaves), -1), w, off, dtype)
+    return out
+
+
 # Pins of each oracle function (what ties it to something other than itself).
 PINS = {
     "meta_ref": "hand-written arrays (tests/golden) + randomized property checks",
@@ -559,4 +622,6 @@ PINS = {
     "rms_norm": "constant rows map to sign * g; unit mean square; scale invariance",
     "mlp_block": "W_down = 0 gives h; literal per-row loop in fp64; rows independent (selective = full)",
     "readout_mlp": "W_down = 0 and g2 = 1 reduce to eq. (1) on rms_norm(h)",
+    "run_tree": "depth-1 trees equal the round oracle; a chain tree equals one sequence; node outputs "
+                "do not depend on other branches",
 }

@@ -367,3 +367,80 @@ def readout_block_weights(D: int, F: int, seed: int = 7):
     wu = bf16_bits(rng.standard_normal((F, D), dtype=np.float32) * np.float32(1.0 / math.sqrt(D)))
     wd = bf16_bits(rng.standard_normal((D, F), dtype=np.float32) * np.float32(1.0 / math.sqrt(F)))
     return {"g1": g1, "g2": g2, "w_gate": wg, "w_up": wu, "w_down": wd}
+
+
+@dataclasses.dataclass
+class TreeRound:
+    """A forest of token trees (requests whose branches fork again).
+
+    Node k has ``parent[k]`` (-1 for a root) and ``node_len[k]`` tokens of its
+    own, stored node after node in ``layers`` (rows [node_start[k],
+    node_start[k] + node_len[k])).  A node without children is a leaf: a
+    question, with at least one token and ``n_opt[k]`` options (option weights
+    ``w_opt``, CSR ``opt_off`` over the leaves in node order).  Every node's
+    sequence is its ancestors' tokens followed by its own.
+    """
+
+    parent: np.ndarray  # [N] int32
+    node_len: np.ndarray  # [N] int32
+    n_opt: np.ndarray  # [N] int32, 0 for internal nodes
+    attn_shapes: tuple
+    gdn_shape: GdnShape
+    layers: Dict[str, Dict[str, np.ndarray]]
+    w_opt: np.ndarray  # [sum O, D] uint16
+    opt_off: np.ndarray  # [leaves + 1] int32
+
+    @property
+    def N(self) -> int:
+        return int(self.parent.shape[0])
+
+    @property
+    def node_start(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.node_len)[:-1]]).astype(np.int64)
+
+    def children(self, k: int) -> List[int]:
+        return [c for c in range(self.N) if int(self.parent[c]) == k]
+
+    def is_leaf(self, k: int) -> bool:
+        return not any(int(p) == k for p in self.parent)
+
+    def leaves(self) -> List[int]:
+        return [k for k in range(self.N) if self.is_leaf(k)]
+
+    def depth(self, k: int) -> int:
+        d = 0
+        while int(self.parent[k]) >= 0:
+            k = int(self.parent[k])
+            d += 1
+        return d
+
+    def ancestors(self, k: int) -> List[int]:
+        """Ancestors of node k, root first."""
+        out = []
+        while int(self.parent[k]) >= 0:
+            k = int(self.parent[k])
+            out.append(k)
+        return out[::-1]
+
+
+def make_tree_round(parent, node_len, *, attn_shapes, gdn_shape, seed=0, n_opt=None) -> TreeRound:
+    """A forest with explicit structure; rows, gates, conv and option weights drawn
+    as for a round (same draw order: layers, conv weights, option weights)."""
+    parent = np.asarray(parent, dtype=np.int32)
+    node_len = np.asarray(node_len, dtype=np.int32)
+    N = parent.shape[0]
+    for k in range(N):
+        if not (-1 <= parent[k] < k):
+            raise ValueError("parents must precede their children")
+    rng = np.random.default_rng(seed)
+    leaf = np.array([not np.any(parent == k) for k in range(N)])
+    if np.any(node_len[leaf] < 1):
+        raise ValueError("a leaf (question) needs at least one token")
+    if n_opt is None:
+        n_opt = np.where(leaf, rng.integers(2, 8, size=N, endpoint=True), 0).astype(np.int32)
+    n_opt = np.asarray(n_opt, dtype=np.int32)
+    T = int(node_len.sum())
+    layers = _draw_layers(rng, T, max(T, 1), attn_shapes, gdn_shape)
+    layers[gdn_shape.name]["conv_w"] = _draw_conv(rng, gdn_shape)
+    wo, off = _draw_wopt(rng, n_opt[leaf], gdn_shape.H * gdn_shape.dv)
+    return TreeRound(parent, node_len, n_opt, tuple(attn_shapes), gdn_shape, layers, wo, off)
