@@ -32,11 +32,14 @@ class DeviceRound:
     DeviceRound of the round that produced it (its S_ckpt / conv_ckpt are the
     initial state and conv window; the prefix K/V rows come from this round's
     ``prefix`` arrays, i.e. the earlier round's attention inputs).
+    ``init_state`` / ``init_conv``: the initial states [R, H, d, d] and conv
+    windows [R, K-1, 3, H, d] of the resumed trunks, given directly instead.
     """
 
     def __init__(self, rnd: Round, device="cuda", max_req: Optional[int] = None,
                  max_q: Optional[int] = None, resume_from: Optional["DeviceRound"] = None,
-                 flags: int = 0):
+                 flags: int = 0, init_state: Optional[torch.Tensor] = None,
+                 init_conv: Optional[torch.Tensor] = None):
         self.rnd = rnd
         self.device = device
         self.flags = flags
@@ -83,7 +86,9 @@ class DeviceRound:
         self.S_ckpt = torch.zeros_like(self.S_P) if self.has_ckpt else None
         self.conv_ckpt = torch.zeros_like(self.conv_win) if self.has_ckpt else None
         self.init_state = self.init_conv = None
-        if self.prefix_rows > 0:
+        if init_state is not None:
+            self.init_state, self.init_conv = init_state.contiguous(), init_conv.contiguous()
+        elif self.prefix_rows > 0:
             if resume_from is None or resume_from.S_ckpt is None:
                 raise ValueError("a round with prefix rows needs the checkpoint it resumes from")
             self.init_state = resume_from.S_ckpt
@@ -188,3 +193,63 @@ class GraphRound:
 
     def replay(self):
         self.graph.replay()
+
+
+class TreeRunner:
+    """A forest of token trees (branches that fork again) on the device, one
+    round per depth (``tree.decompose``): a level's trunks start from their
+    parent requests' S_P and conv windows of the previous level, gathered on
+    the device; their prefix K/V rows are the ancestors' rows."""
+
+    def __init__(self, tree, device="cuda", flags: int = 0):
+        from . import tree as TR
+        self.tree = tree
+        self.device = device
+        self.flags = flags
+        self.levels = TR.decompose(tree)
+        self.rounds = []
+
+    def run(self):
+        self.rounds = []
+        prev = None
+        for lv in self.levels:
+            r = lv.round
+            init_state = init_conv = None
+            if int(r.prefix_len.sum()) > 0:
+                idx = torch.tensor([max(j, 0) for j in lv.parent_request], dtype=torch.long, device=self.device)
+                init_state = prev.S_P.index_select(0, idx)
+                init_conv = prev.conv_win.index_select(0, idx)
+            dr = DeviceRound(r, device=self.device, flags=self.flags, init_state=init_state, init_conv=init_conv)
+            dr.run()
+            self.rounds.append(dr)
+            prev = dr
+
+    def status(self) -> int:
+        st = 0
+        for dr in self.rounds:
+            st |= dr.status()
+        return st
+
+    def outputs(self):
+        """Attention and GDN rows in tree layout (node after node) and the leaves' probabilities (host)."""
+        from . import tree as TR
+        t = self.tree
+        T = int(t.node_len.sum())
+        start = t.node_start
+        attn = {a.name: np.zeros((T, a.Hq, a.d), np.float32) for a in t.attn_shapes}
+        g = t.gdn_shape
+        gdn = np.zeros((T, g.H, g.dv), np.float32)
+        p = np.zeros(int(t.opt_off[-1]), np.float32)
+        leaf_index = {k: i for i, k in enumerate(t.leaves())}
+        for lv, dr in zip(self.levels, self.rounds):
+            a_out = {n: o.float().cpu().numpy() for n, o in dr.attn_out.items()}
+            g_out = dr.gdn_out.float().cpu().numpy()
+            pp = dr.p.cpu().numpy()
+            for k, rows in TR.node_rows(lv, t):
+                for n in a_out:
+                    attn[n][start[k]:start[k] + rows.shape[0]] = a_out[n][rows]
+                gdn[start[k]:start[k] + rows.shape[0]] = g_out[rows]
+            for i, k in enumerate(lv.question_nodes):
+                li = leaf_index[k]
+                p[t.opt_off[li]:t.opt_off[li + 1]] = pp[lv.round.opt_off[i]:lv.round.opt_off[i + 1]]
+        return attn, gdn, p
