@@ -96,3 +96,35 @@ def test_argument_errors_return_before_any_launch(lib):
                                  None) == 1
     assert lib.fork_readout(ref, fake, 100, fake, fake, fake, 0, None) == 1
     assert lib.fork_readout(ref, None, 128, fake, fake, fake, 0, None) == 1
+
+
+def test_readout_mlp_argument_errors_and_workspace_size(lib):
+    from tree_forked_hybrid_gb300 import fork as F
+    n = lib.fork_meta_bytes(128, 4, 8)
+    buf = ctypes.create_string_buffer(n + 16)
+    addr = (ctypes.addressof(buf) + 15) & ~15
+    h = F.fork_meta()
+    assert lib.fork_meta_init(ctypes.byref(h), ctypes.c_void_p(addr), n, 128, 4, 8, 32) == 0
+    ref = ctypes.byref(h)
+    fake = ctypes.c_void_p(0x1000)
+    ws_bytes = lib.fork_readout_mlp_workspace_bytes(8, 256, 512)
+    # Mpad = 64 rows: normalised rows (bf16), activations (bf16), y (float32)
+    assert ws_bytes == 64 * 256 * 2 + 64 * 512 * 2 + 64 * 256 * 4
+    assert lib.fork_readout_mlp_workspace_bytes(8, 100, 512) == 0     # D not a multiple of 64
+    assert lib.fork_readout_mlp_workspace_bytes(8, 256, 96) == 0      # F not a multiple of 64
+    assert lib.fork_readout_mlp_workspace_bytes(8, 16384, 512) == 0   # D above 8192
+    args = [ref, fake, 256, 512, fake, fake, fake, fake, fake, fake, fake, fake, fake, ws_bytes, 0, None]
+    good = list(args)
+    for i in (1, 4, 5, 6, 7, 8, 9, 10, 11, 12):  # each pointer null in turn
+        a = list(good)
+        a[i] = None
+        assert lib.fork_readout_mlp(*a) == 1
+    a = list(good)
+    a[2] = 200  # D
+    assert lib.fork_readout_mlp(*a) == 1
+    a = list(good)
+    a[13] = ws_bytes - 1  # short workspace
+    assert lib.fork_readout_mlp(*a) == 1
+    a = list(good)
+    a[5] = ctypes.c_void_p(0x1008)  # misaligned weights
+    assert lib.fork_readout_mlp(*a) == 1

@@ -1,0 +1,29 @@
+"""Host logic of bench.py and of request sharding that needs no GPU."""
+import numpy as np
+
+import bench
+from tree_forked_hybrid_gb300 import shard as S
+from tree_forked_hybrid_gb300 import workloads as wl
+
+
+def test_traffic_is_reported_only_for_the_measured_sources(monkeypatch):
+    t = dict(bench.TRAFFIC)
+    assert bench._sources_sha256(t["sources"]) == bench._sources_sha256(t["sources"])
+    if t["sha256"] is not None:
+        assert bench._traffic() == t["bytes"]
+    monkeypatch.setitem(bench.TRAFFIC, "sha256", "0" * 64)
+    assert bench._traffic() is None
+    monkeypatch.setitem(bench.TRAFFIC, "sha256", None)
+    assert bench._traffic() is None
+
+
+def test_more_ranks_than_requests_gives_empty_shards():
+    a = wl.AttnShape("attn", 2, 1, 16, 0, 0.0)
+    g = wl.GdnShape("gdn", 1, 16, 16, 4, 64)
+    rnd = wl.custom_round([5, 3], [1, 2], [2, 4, 1], attn_shapes=(a,), gdn_shape=g, T_cap=64, seed=1)
+    parts = S.assign_requests(S.request_tokens(rnd), 4)
+    assert sorted(j for p in parts for j in p) == [0, 1]
+    assert sum(1 for p in parts if not p) == 2
+    sub, qids = S.shard_round(rnd, [])
+    assert sub.R == 0 and sub.Nq == 0 and sub.T == 0 and qids == []
+    assert np.all(sub.layers["attn"]["q"] == 0)
