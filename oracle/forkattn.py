@@ -543,7 +543,7 @@ def run_readout(view: RoundView, h_stream: np.ndarray, w: np.ndarray, off: np.nd
                 dtype=np.float32) -> np.ndarray:
     """Eq. (1) at each question's last stream row of h (flattened heads)."""
     rows = view.meta["q_last"]
-    h = h_stream[rows].reshape(rows.shape[0], -1)
+    h = h_stream[rows].reshape(rows.shape[0], int(np.prod(h_stream.shape[1:])))  # also for no question
     return readout(h, w, off, dtype)
 
 

@@ -131,3 +131,41 @@ def test_levels_through_round_oracle_reproduce_the_tree():
         assert np.array_equal(got["attn"][n], want["attn"][n]), n
     assert np.array_equal(got["gdn"], want["gdn"])
     assert np.array_equal(got["p"], want["p"])
+
+
+def random_forest(seed):
+    rng = np.random.default_rng(seed)
+    parent, node_len = [], []
+    for k in range(int(rng.integers(3, 12))):
+        if k == 0 or rng.random() < 0.15:
+            parent.append(-1)
+        else:
+            # attach to an earlier node whose depth stays below 4
+            cand = [p for p in range(k) if _depth(parent, p) < 3]
+            parent.append(int(rng.choice(cand)))
+        node_len.append(int(rng.integers(0, 12)))
+    leaves = [k for k in range(len(parent)) if k not in parent]
+    for k in leaves:
+        node_len[k] = max(node_len[k], 1)
+    return wl.make_tree_round(parent, node_len, attn_shapes=(A1, A2), gdn_shape=G, seed=seed)
+
+
+def _depth(parent, k):
+    d = 0
+    while parent[k] >= 0:
+        k = parent[k]
+        d += 1
+    return d
+
+
+def test_random_forests_through_round_oracle():
+    for seed in range(12):
+        t = random_forest(100 + seed)
+        want = tree_oracle(t)
+        got = run_levels_with_round_oracle(t)
+        for n in want["attn"]:
+            assert np.array_equal(got["attn"][n], want["attn"][n]), (seed, n)
+        assert np.array_equal(got["gdn"], want["gdn"]), seed
+        assert np.array_equal(got["p"], want["p"]), seed
+        qs = sorted(k for lv in TR.decompose(t) for k in lv.question_nodes)
+        assert qs == t.leaves(), seed

@@ -59,7 +59,8 @@ class DeviceRound:
         for name, lay in rnd.layers.items():
             self.inputs[name] = {k: (_bf16(v, device) if v.dtype == np.uint16 else _f32(v, device))
                                  for k, v in lay.items()}
-        self.w_opt = _bf16(rnd.w_opt, device)
+        # at least one row, so that a round without questions still passes valid pointers
+        self.w_opt = _bf16(rnd.w_opt if rnd.w_opt.shape[0] else np.zeros((1, rnd.D), np.uint16), device)
         self.opt_off = torch.from_numpy(rnd.opt_off.astype(np.int32)).to(device)
         self.prefix_rows = int(rnd.prefix_len.sum())
         self.prefix = {}
