@@ -65,6 +65,18 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def aggregate_over_ranks(torch, dist, device, elapsed_ms: float, tokens: int):
+    """Whole-job figures of one process per GPU: the slowest rank's elapsed time
+    and the tokens of all ranks' rounds (each rank draws its own round)."""
+    if dist is None:
+        return elapsed_ms, tokens
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([tokens], dtype=torch.int64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -263,14 +275,10 @@ def main():
     torch.cuda.synchronize()
     w1 = time.time()
     sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([elapsed_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms, tokens_all = aggregate_over_ranks(torch, dist, f"cuda:{local}", t_start.elapsed_time(t_end),
+                                                  rnd.T)
     per_call = {name: statistics.mean(a.elapsed_time(b) for a, b in lst) for name, lst in ev.items()}
     kernel_alone = attn_kernel_alone(torch, dr, rnd, stream)
-    tokens_all = rnd.T * ws
     value = tokens_all * args.steps / (elapsed_ms / 1e3)
     ms_per_step = elapsed_ms / args.steps
 
@@ -477,12 +485,8 @@ def e2e(torch, dr, rnd, args, stream, dist, local, ws):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": T * ws * args.steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    ms, tokens_all = aggregate_over_ranks(torch, dist, f"cuda:{local}", e0.elapsed_time(e1), T)
+    return {"value": tokens_all * args.steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
 
 

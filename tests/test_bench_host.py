@@ -27,3 +27,31 @@ def test_more_ranks_than_requests_gives_empty_shards():
     sub, qids = S.shard_round(rnd, [])
     assert sub.R == 0 and sub.Nq == 0 and sub.T == 0 and qids == []
     assert np.all(sub.layers["attn"]["q"] == 0)
+
+
+def _agg_rank(rank, world, port):
+    import os
+
+    import torch
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms, tok = bench.aggregate_over_ranks(torch, dist, "cpu", [12.5, 30.25][rank], [22003, 21711][rank])
+        assert ms == 30.25 and tok == 22003 + 21711
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_aggregate_slowest_time_and_all_tokens():
+    import socket
+
+    import pytest
+    mp = pytest.importorskip("torch.multiprocessing")
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mp.spawn(_agg_rank, args=(2, port), nprocs=2, join=True)
+    import torch
+    assert bench.aggregate_over_ranks(torch, None, "cpu", 7.0, 5) == (7.0, 5)
