@@ -36,7 +36,7 @@ METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 # SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
 TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
                        "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
-           "sha256": "05bcebf9af2dfac67abbafe77c15605bf0cef673b97c45a9fd9f89aa8f79e9cf", "bytes": 459936000}
+           "sha256": None, "bytes": None}
 
 
 def _sources_sha256(paths):
@@ -173,20 +173,29 @@ def oracle_sample(rnd, trunk_cap=None, n_questions=1):
     return T_s, time.perf_counter() - t0
 
 
+REF_TRUNK_CAP = 1024  # oracle sample: request 0, trunk cut to its first 1024 tokens, first question
+
+
+def _oracle_sample_note(rnd, n):
+    return (f"request 0 of the round with its trunk cut to its first {min(REF_TRUNK_CAP, int(rnd.trunk_len[0]))} "
+            f"tokens plus its first question ({n} stream tokens), run through the oracle (numpy fp32)")
+
+
 def run_reference(args):
+    """The reference arm: the CPU oracle on the machine's host cores, each step one
+    oracle sample (the same sample the cpu_baseline of the GPU arm times)."""
     ws, rank, _ = _dist()
     if rank != 0:
         return
     from tree_forked_hybrid_gb300 import workloads as wl
     rnd = wl.make_round(WORKLOAD_ID)
     cores = len(os.sched_getaffinity(0))
-    cap = 512
     for _ in range(args.warmup):
-        oracle_sample(rnd, cap)
+        oracle_sample(rnd, REF_TRUNK_CAP)
     tok = 0
     t = 0.0
     for _ in range(args.steps):
-        n, dt = oracle_sample(rnd, cap)
+        n, dt = oracle_sample(rnd, REF_TRUNK_CAP)
         tok += n
         t += dt
     value = tok / t
@@ -196,10 +205,22 @@ def run_reference(args):
            "impl": "reference",
            "config": _config(rnd),
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                            "sample": f"per step: request 0 of the round, trunk cut to its first {cap} tokens, "
-                                      f"plus its first question, run through the oracle (numpy fp32)"},
+                            "sample": "per step: " + _oracle_sample_note(rnd, tok // max(args.steps, 1))},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
+
+
+def cpu_baseline(rnd, min_seconds=10.0):
+    """The oracle on the same sample as the reference arm, repeated until about
+    min_seconds of CPU work have been timed."""
+    tok, t, reps = 0, 0.0, 0
+    while t < min_seconds and reps < 8:
+        n, dt = oracle_sample(rnd, REF_TRUNK_CAP)
+        tok += n
+        t += dt
+        reps += 1
+    return {"value": tok / t, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{reps} repetitions of: " + _oracle_sample_note(rnd, tok // reps) + f"; {t:.1f} s in total"}
 
 
 def _config(rnd):
@@ -207,6 +228,75 @@ def _config(rnd):
                         "attn 32q/8kv d=128 RoPE; SWA W=1024; GDN 32 heads d=128 chunk 64; readout D=4096",
             "T": rnd.T, "T_cap": rnd.T_cap, "R": rnd.R, "Nq": rnd.Nq,
             "l2": "inputs larger than L2 (about 1.2 GB of layer inputs per step)"}
+
+
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def step_times(torch, fn, stream, steps):
+    """CUDA-event duration (ms) of each of `steps` back-to-back calls of fn."""
+    ev = _events(torch, steps + 1)
+    ev[0].record(stream)
+    for i in range(steps):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
+def latency_stats(ms):
+    return {"median": float(np.median(ms)), "p10": float(np.percentile(ms, 10)),
+            "p90": float(np.percentile(ms, 90)), "mean": float(np.mean(ms))}
+
+
+def layer_roofline(RL, rnd, ms, peaks):
+    work = RL.round_work(rnd)
+    t_f = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_b = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(t_f, t_b)
+    return {"t_roof_us": t_roof * 1e6, "t_meas_us": ms * 1e3, "frac": t_roof / (ms / 1e3),
+            "bound": "tensor" if t_f >= t_b else "hbm", "flops": work["flops"], "bytes": work["bytes"]}
+
+
+WORKLOAD_NAMES = {1: "short requests: R=32, P~U[256,512], n~U{1..4}, |q|~U[16,48]; attn 16q/4kv d=128 RoPE; "
+                     "GDN 16 heads d=128; T_cap 16384",
+                  2: "many questions: R=8, P~U[256,400], n=48, |q|~U[12,32]; attn 16q/4kv d=128 + SWA W=512; "
+                     "GDN 16 heads; T_cap 16384",
+                  3: "long documents: R=4, P~U[4096,6144], n~U{8..20}, |q|~U[32,64]; attn 32q/8kv d=128 + SWA "
+                     "W=1024; GDN 32 heads; T_cap 32768",
+                  "4A": "wide fork: one request, P=16384, 64 questions of U[16,64] tokens, checkpoint at 15360; "
+                        "shapes as the long-document round",
+                  "4B": "resume: 15360 prefix rows (K/V, GDN state and conv window from the checkpoint) + 2048 "
+                        "new trunk tokens + 64 questions"}
+
+
+def per_config(torch, RL, wl, DeviceRound, peaks, steps, warmup, local, main_entry):
+    """Round latency (median/p10/p90), tokens/s and layer roofline fraction of the other workloads."""
+    out = {"3": main_entry}
+    dev = f"cuda:{local}"
+    stream = torch.cuda.current_stream()
+
+    def one(key, rnd, dr):
+        for _ in range(max(warmup, 3)):
+            dr.run()
+        ms = step_times(torch, dr.run, stream, steps)
+        if dr.status() != 0:
+            raise RuntimeError(f"workload {key}: device status {dr.status():#x}")
+        st = latency_stats(ms)
+        out[str(key)] = {"workload": WORKLOAD_NAMES[key], "T": rnd.T, "T_cap": rnd.T_cap,
+                         "tokens_per_s": rnd.T / (st["median"] / 1e3), "round_ms": st,
+                         "layer_roofline": layer_roofline(RL, rnd, st["median"], peaks)}
+
+    for wid in (1, 2):
+        rnd = wl.make_round(wid)
+        one(wid, rnd, DeviceRound(rnd, device=dev))
+    ra = wl.make_round(4)
+    dra = DeviceRound(ra, device=dev)
+    one("4A", ra, dra)
+    rb = wl.make_resume_round(ra)
+    one("4B", rb, DeviceRound(rb, device=dev, resume_from=dra))
+    return out
 
 
 def main():
@@ -217,10 +307,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--readout-mlp", action="store_true",
                     help="also time the selective-readout block (norm, SwiGLU MLP, final norm, eq. (1))")
-    ap.add_argument("--graph", action="store_true",
-                    help="also time the short-request round eagerly and as one CUDA graph replay")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the short-request round timed eagerly and as one CUDA graph replay")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -235,6 +326,7 @@ def main():
     torch.cuda.set_device(local)
     from tree_forked_hybrid_gb300 import build as B
     B.build()
+    from tree_forked_hybrid_gb300 import fork as F
     from tree_forked_hybrid_gb300 import workloads as wl
     from tree_forked_hybrid_gb300 import roofline as RL
     from tree_forked_hybrid_gb300.runner import DeviceRound
@@ -258,12 +350,11 @@ def main():
     time.sleep(0.3)
     dr.run()  # one more untimed step after the idle wait for the sampler
     ev = {name: [] for name, _ in calls}
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    step_ev = _events(torch, args.steps + 1)
     torch.cuda.synchronize()
     w0 = time.time()
-    t_start.record(stream)
-    for _ in range(args.steps):
+    step_ev[0].record(stream)
+    for i in range(args.steps):
         for name, fn in calls:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -271,12 +362,13 @@ def main():
             fn()
             e1.record(stream)
             ev[name].append((e0, e1))
-    t_end.record(stream)
+        step_ev[i + 1].record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
     sampler.stop()
-    elapsed_ms, tokens_all = aggregate_over_ranks(torch, dist, f"cuda:{local}", t_start.elapsed_time(t_end),
+    elapsed_ms, tokens_all = aggregate_over_ranks(torch, dist, f"cuda:{local}", step_ev[0].elapsed_time(step_ev[-1]),
                                                   rnd.T)
+    step_ms = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
     per_call = {name: statistics.mean(a.elapsed_time(b) for a, b in lst) for name, lst in ev.items()}
     kernel_alone = attn_kernel_alone(torch, dr, rnd, stream)
     value = tokens_all * args.steps / (elapsed_ms / 1e3)
@@ -284,63 +376,81 @@ def main():
 
     peaks = _peaks()
     work = RL.round_work(rnd)
-    t_roof = RL.roofline_time(work, peaks["bf16_tflops"], peaks["hbm_gbs"])
-    # dominant call and its roofline
+    # dominant call and its roofline; the timed region lasts well under a second, so the
+    # tensor-core peak is the burst one (the sustained figure is reported beside it)
     top = max(per_call, key=per_call.get)
     if top.startswith("attn_"):
         f = work["attn"][top[5:]]["flops"]
         ach = f / (per_call[top] / 1e3) / 1e12
         traffic = _traffic() if top == "attn_attn" else None
-        roof = {"kernel": f"fork_attn ({top[5:]}): rotary tables, key and query rotation, attn_tc_kernel",
-                "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"], "traffic": traffic,
+        roof = {"kernel": f"fork_attn ({top[5:]}): rotary tables, key rotation, attn_tc_kernel",
+                "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
                 "traffic_unit": "bytes per call (all launches of the call)",
-                "peak_note": f"bf16 dense sustained ({peaks['source']}); call timed inside a long step"}
+                "peak_note": f"bf16 dense burst ({peaks['source']}): the timed region lasts "
+                             f"{elapsed_ms:.0f} ms",
+                "frac_of_sustained": ach / peaks["bf16_tflops_sustained"]}
         if top == "attn_attn" and kernel_alone:
             ka = f / (kernel_alone / 1e3) / 1e12
-            roof["kernel_alone"] = {"kernel": "attn_tc_kernel (same round, queries and keys not rotated: the "
-                                              "same visible pairs and FLOPs)",
+            roof["kernel_alone"] = {"kernel": "attn_tc_kernel (same round, keys not rotated: the same visible "
+                                              "pairs and FLOPs)",
                                     "ms": kernel_alone, "achieved": ka, "peak": peaks["bf16_tflops"],
                                     "frac": ka / peaks["bf16_tflops"],
                                     "peak_note": f"bf16 dense burst ({peaks['source']}); timed alone after the "
                                                  "timed region"}
     else:
         key = "gdn" if top.startswith("gdn") else "readout"
-        b = work[key]["bytes"] if key != "gdn" else work["gdn"]["bytes"]
+        b = work[key]["bytes"]
         ach = b / (per_call[top] / 1e3) / 1e9
         roof = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "traffic": None, "peak_note": f"HBM copy ({peaks['source']})"}
+    main_lat = latency_stats(step_ms)
+    main_entry = {"workload": WORKLOAD_NAMES[3], "T": rnd.T, "T_cap": rnd.T_cap,
+                  "tokens_per_s": rnd.T / (main_lat["median"] / 1e3), "round_ms": main_lat,
+                  "layer_roofline": layer_roofline(RL, rnd, ms_per_step, peaks)}
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(rnd),
            "roofline": roof,
-           "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_meas_us": ms_per_step * 1e3,
-                              "frac": t_roof / (ms_per_step / 1e3), "flops": work["flops"],
-                              "bytes": work["bytes"],
-                              "peaks": f"{peaks['bf16_tflops']} TFLOP/s bf16, {peaks['hbm_gbs']} GB/s "
-                                       f"({peaks['source']})"},
+           "layer_roofline": dict(main_entry["layer_roofline"],
+                                  peaks=f"{peaks['bf16_tflops']} TFLOP/s bf16 burst, {peaks['hbm_gbs']} GB/s "
+                                        f"({peaks['source']})"),
+           "round_ms": main_lat,
            "per_call_us": {k: v * 1e3 for k, v in per_call.items()},
            "gpu_launches": dr.launches_per_round() * args.steps,
            "clocks": sampler.summary(w0, w1)}
 
+    # FORK_DETERMINISTIC: the same round with the flag (every kernel is composition-invariant
+    # by construction, so the flag selects the same kernels)
+    det = DeviceRound(rnd, device=f"cuda:{local}", flags=F.FORK_DETERMINISTIC)
+    for _ in range(3):
+        det.run()
+    det_ms = latency_stats(step_times(torch, det.run, stream, args.steps))
+    out["deterministic"] = {"round_ms": det_ms, "cost_vs_default": det_ms["median"] / main_lat["median"] - 1.0,
+                            "identical_outputs": bool(torch.equal(det.gdn_out, dr.gdn_out) and
+                                                      all(torch.equal(det.attn_out[n], dr.attn_out[n])
+                                                          for n in dr.attn_out) and torch.equal(det.p, dr.p))}
+    del det
     if not args.no_e2e:
         out["e2e"] = e2e(torch, dr, rnd, args, stream, dist, local, ws)
+    if not args.no_configs and ws == 1:
+        try:
+            out["per_config"] = per_config(torch, RL, wl, DeviceRound, peaks, args.steps, args.warmup, local,
+                                           main_entry)
+        except Exception as exc:  # reported, never fatal for the main line
+            out["per_config"] = {"error": f"{type(exc).__name__}: {exc}"}
     if args.readout_mlp:
         try:
             out["readout_mlp"] = readout_mlp_timing(torch, dr, rnd, stream, peaks)
         except Exception as exc:  # reported, never fatal for the main line
             out["readout_mlp"] = {"error": f"{type(exc).__name__}: {exc}"}
-    if args.graph:
+    if not args.no_graph and ws == 1:
         try:
             out["graph_replay"] = graph_timing(torch, args, local)
         except Exception as exc:  # reported, never fatal for the main line
             out["graph_replay"] = {"error": f"{type(exc).__name__}: {exc}"}
     if rank == 0 and ws == 1 and not args.no_cpu:
-        n, dt = oracle_sample(rnd, None, 1)
-        out["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
-                               "kind": "oracle",
-                               "sample": f"request 0 of the round (trunk of {int(rnd.trunk_len[0])} tokens) with "
-                                         f"its first question, {n} stream tokens, {dt:.1f} s, numpy fp32"}
+        out["cpu_baseline"] = cpu_baseline(rnd)
     if rank == 0:
         print(json.dumps(out))
     if dist:
@@ -467,11 +577,21 @@ def e2e(torch, dr, rnd, args, stream, dist, local, ws):
     p_host = torch.empty(dr.p.shape, dtype=dr.p.dtype, pin_memory=True)
     d2h = p_host.numel() * p_host.element_size()
 
-    def step():
+    ev = []
+
+    def step(mark=False):
+        e = _events(torch, 3) if mark else None
         for hp, dev in host:
             dev.copy_(hp, non_blocking=True)
+        if mark:
+            e[0].record(stream)
         dr.run()
+        if mark:
+            e[1].record(stream)
         p_host.copy_(dr.p, non_blocking=True)
+        if mark:
+            e[2].record(stream)
+            ev.append(e)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -486,8 +606,17 @@ def e2e(torch, dr, rnd, args, stream, dist, local, ws):
     e1.record(stream)
     torch.cuda.synchronize()
     ms, tokens_all = aggregate_over_ranks(torch, dist, f"cuda:{local}", e0.elapsed_time(e1), T)
+    # split of one step into its parts (a separate pass with events between the parts)
+    for _ in range(min(args.steps, 10)):
+        step(mark=True)
+    torch.cuda.synchronize()
+    compute = statistics.mean(a[0].elapsed_time(a[1]) for a in ev)
+    d2h_ms = statistics.mean(a[1].elapsed_time(a[2]) for a in ev)
+    per_step = ms / args.steps
     return {"value": tokens_all * args.steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h, "ms_per_step": per_step,
+            "split_ms": {"h2d": max(per_step - compute - d2h_ms, 0.0), "compute": compute, "d2h": d2h_ms,
+                         "note": "h2d = step time minus the event-timed compute and read-back"}}
 
 
 if __name__ == "__main__":

@@ -12,7 +12,9 @@
  *   - All pointers named d_* or described as "device" are CUDA device
  *     pointers; the caller allocates and owns every buffer (metadata,
  *     workspace, inputs, outputs).  The library allocates nothing and keeps
- *     no global state between calls.
+ *     no global state between calls, with one exception: fork_attn_noalloc
+ *     takes its scratch from a file-scope device array that the library owns
+ *     (and caches that array's device address per device).
  *   - bf16 tensors are passed as uint16_t bit patterns (bfloat16), row-major
  *     with the layout stated per argument.  Every base pointer must be
  *     16-byte aligned.
@@ -52,16 +54,27 @@ extern "C" {
 #define FORK_STATUS_TIMEOUT 0x8    /* a bounded wait inside a kernel gave up */
 #define FORK_STATUS_BAD_PREFIX 0x10 /* a request's prefix rows lie outside the prefix buffers or
                                        the resume state/window buffers are missing */
+#define FORK_STATUS_CHECK 0x20      /* a FORK_CHECKS bounds check failed (the work was skipped) */
 
 /* Flags */
 #define FORK_DETERMINISTIC 0x1u /* bitwise identical results for a question under any round
                                    composition.  Every kernel here already computes each output
                                    from segment-aligned tiles and chunks in a fixed order, so the
                                    flag is accepted and changes nothing. */
-#define FORK_CHECKS 0x2u        /* extra device-side consistency checks (status word) */
+#define FORK_CHECKS 0x2u        /* bounds checks on the device: fork_build_meta verifies the tables
+                                   it built; fork_attn and fork_gdn_* check that every row range
+                                   and state index a CTA is about to use lies inside the round;
+                                   fork_readout checks the option offsets.  A failed check sets
+                                   FORK_STATUS_CHECK and the CTA skips that work (no trap). */
 #define FORK_WARP_MMA 0x4u      /* fork_attn, fork_gdn_*: run the warp-level mma.sync kernels instead
                                    of the tcgen05 ones (same results within rounding; for
                                    comparisons; d = 64 GDN always uses them) */
+#define FORK_TEST_STALL 0x100u  /* test hook of the bounded waits (fork_attn, fork_gdn_* with
+                                   d = 128): one role of every CTA waits on a barrier that
+                                   nothing completes, so the wait runs out after
+                                   fork_meta.wait_us; the CTA then drains its own copies and
+                                   products, frees its tensor memory and exits, and the call
+                                   reports FORK_STATUS_TIMEOUT.  Never set in normal use. */
 
 /* ------------------------------------------------------------------------
  * Metadata (Flide pages: onedev summary "무엇과 다른가" - per-token (j, c, t),
@@ -82,6 +95,10 @@ typedef struct fork_meta {
   int32_t max_q;       /* most questions a round may hold */
   int32_t tile_tokens; /* tokens per attention work item: 256 / (Hq / Hkv) (two 128-row
                           query tiles per CTA), or 128 / (Hq / Hkv) (one tile) */
+  uint32_t wait_us;    /* limit of every bounded wait inside the tensor-core kernels, in
+                          microseconds (0 = 2 s); a wait that runs out sets
+                          FORK_STATUS_TIMEOUT.  fork_meta_init sets 0; the caller may
+                          change it between calls. */
 } fork_meta;
 
 /* Bytes of the metadata buffer for a stream capacity T_cap (tokens), at most
@@ -130,12 +147,12 @@ int fork_read_status(const fork_meta* m, int32_t* h_status, void* stream);
  * rotary positions they would have alone).
  * ------------------------------------------------------------------------ */
 
-/* Workspace bytes fork_attn needs: rotated keys of the stream, rotated prefix
- * keys, two small rotary tables, and room for rotated queries (written only
- * with FORK_WARP_MMA: the default kernel rotates its query tiles in shared
+/* Workspace bytes fork_attn needs with these flags: rotated keys of the
+ * stream, rotated prefix keys, two small rotary tables, and with FORK_WARP_MMA
+ * also rotated queries (the default kernel rotates its query tiles in shared
  * memory).  0 when rope_theta == 0. */
 size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq, int32_t Hkv,
-                                 int32_t d, float rope_theta);
+                                 int32_t d, float rope_theta, uint32_t flags);
 
 /* o_x = sum_y softmax_y(<R(q_x,t_x), R(k_y,t_y)> * scale) v_y over visible y.
  *   q [T_cap, Hq, d], k and v [T_cap, Hkv, d] bf16 (stream rows; pad rows
@@ -150,7 +167,7 @@ size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq,
  *   trunk positions 0..prefix_len_j-1 held outside the stream (incremental
  *   resume), request j's rows starting at the sum of earlier prefix lengths;
  *   NULL when no request has a prefix.
- *   workspace: device buffer of fork_attn_workspace_bytes(...) bytes. */
+ *   workspace: device buffer of fork_attn_workspace_bytes(..., flags) bytes. */
 int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k, const uint16_t* v,
               uint16_t* o, int32_t Hq, int32_t Hkv, int32_t d, int32_t window, float rope_theta,
               float scale, const uint16_t* prefix_k, const uint16_t* prefix_v, int32_t prefix_rows,
@@ -166,10 +183,13 @@ int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k, const ui
  * of FORK_NOALLOC_SCRATCH_BYTES bytes owned by the library, which every GPU
  * that loads the library keeps allocated until the process exits.
  *   - Returns FORK_ECAPACITY when fork_attn_workspace_bytes(T_cap,
- *     prefix_rows, Hq, Hkv, d, rope_theta) exceeds FORK_NOALLOC_SCRATCH_BYTES
- *     (e.g. T_cap = 4096 with 16 q-heads, 4 kv-heads, d = 128 fits;
- *     T_cap = 16384 with the same heads does not).
- *   - Calls no allocating routine.  The first call on a device looks up the
+ *     prefix_rows, Hq, Hkv, d, rope_theta, flags) exceeds
+ *     FORK_NOALLOC_SCRATCH_BYTES (e.g. T_cap = 16384 with 16 q-heads,
+ *     4 kv-heads, d = 128 fits (about 17 MB: rotated keys and tables);
+ *     T_cap = 32768 with 8 kv-heads does not, nor T_cap = 16384 with
+ *     FORK_WARP_MMA, which also needs rotated queries).
+ *   - Calls no allocating routine (the array is the one piece of state the
+ *     library keeps between calls).  The first call on a device looks up the
  *     array's device address (and loads the module there); make that first
  *     call before any stream capture.
  *   - Every call, on any stream, uses the same array and leaves its contents

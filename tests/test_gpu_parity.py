@@ -211,12 +211,14 @@ def test_resume_round_matches_scratch():
     check_readout(rb, drb, vb, questions=qs)
 
 
-def test_edge_cases_round():
+@pytest.mark.parametrize("d", [64, 128])
+def test_edge_cases_round(d):
     """Empty trunk, a request without questions, one-token questions, odd tails,
-    a stream that fills the capacity exactly."""
-    a = wl.AttnShape("attn", 4, 1, 64, 0, 10000.0)
-    s = wl.AttnShape("swa", 4, 1, 64, 5, 10000.0)
-    g = wl.GdnShape("gdn", 2, 64, 64, 4, 64)
+    a stream that fills the capacity exactly; at d = 128 the tensor-core GDN
+    kernel (the d = 64 one is the warp-MMA kernel)."""
+    a = wl.AttnShape("attn", 4, 1, d, 0, 10000.0)
+    s = wl.AttnShape("swa", 4, 1, d, 5, 10000.0)
+    g = wl.GdnShape("gdn", 2, d, d, 4, 64)
     P = [0, 67, 130, 1, 2]
     n = [2, 0, 3, 1, 1]
     ql = [1, 5, 64, 65, 1, 3, 2]
@@ -247,11 +249,13 @@ def test_pad_rows_untouched():
 
 
 def test_warp_mma_variant_matches_oracle():
-    """The warp-level mma.sync attention kernel (FORK_WARP_MMA) against the oracle."""
-    torch = require_gpu()
+    """The warp-level mma.sync kernels (FORK_WARP_MMA: attention and GDN) against the oracle."""
+    require_gpu()
     from tree_forked_hybrid_gb300 import fork as F
     rnd = wl.make_round(2)
     dr = run_device(rnd, flags=F.FORK_WARP_MMA)
     view = oracle_view(rnd)
     for a in rnd.attn_shapes:
         check_attention(rnd, dr, view, a.name)
+    check_gdn(rnd, dr, view)
+    check_readout(rnd, dr, view)

@@ -180,11 +180,13 @@ struct AttnWs {
   size_t qr, kr, pkr, hi, lo, total;
 };
 
-static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hkv, int64_t d) {
+// Rotated keys (stream, prefix), the two rotary tables and, for the warp-MMA kernel only,
+// rotated queries (the tcgen05 kernel rotates its query tiles in shared memory).
+static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hkv, int64_t d, bool warp_mma) {
   AttnWs w;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   w.qr = 0;
-  w.kr = al(w.qr + static_cast<size_t>(T_cap) * Hq * d * 2);
+  w.kr = al(w.qr + (warp_mma ? static_cast<size_t>(T_cap) * Hq * d * 2 : 0));
   w.pkr = al(w.kr + static_cast<size_t>(T_cap) * Hkv * d * 2);
   w.hi = al(w.pkr + static_cast<size_t>(prefix_rows) * Hkv * d * 2);
   w.lo = al(w.hi + static_cast<size_t>(rope_hi_rows(T_cap + prefix_rows)) * (d / 2) * 8);
@@ -197,10 +199,10 @@ static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hk
 using namespace fork;
 
 extern "C" size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq,
-                                            int32_t Hkv, int32_t d, float rope_theta) {
+                                            int32_t Hkv, int32_t d, float rope_theta, uint32_t flags) {
   if (T_cap < 1 || prefix_rows < 0 || Hkv < 1 || Hq < Hkv || (d != 64 && d != 128)) return 0;
   if (rope_theta == 0.f) return 0;
-  return attn_ws(T_cap, prefix_rows, Hq, Hkv, d).total;
+  return attn_ws(T_cap, prefix_rows, Hq, Hkv, d, (flags & FORK_WARP_MMA) != 0).total;
 }
 
 extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k,
@@ -246,9 +248,12 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.rope_hi_rows = 0;
   p.rotate_q = 0;
+  p.checks = (flags & FORK_CHECKS) ? 1 : 0;
+  p.stall = (flags & FORK_TEST_STALL) ? 1 : 0;
+  p.wait_ns = wait_ns_of(m);
 
   if (rope_theta != 0.f) {
-    const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hq, Hkv, d);
+    const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hq, Hkv, d, warp_mma);
     if (!workspace || ws_bytes < w.total || !is_aligned16(workspace)) return FORK_EINVAL;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     uint16_t* qr = reinterpret_cast<uint16_t*>(ws + w.qr);
@@ -257,7 +262,7 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     float2* hi = reinterpret_cast<float2*>(ws + w.hi);
     float2* lo = reinterpret_cast<float2*>(ws + w.lo);
     const int hi_rows = static_cast<int>(rope_hi_rows(static_cast<int64_t>(L.T_cap) + prefix_rows));
-    rope_tables_kernel<<<2 * 152, 128, 0, s>>>(hi, hi_rows, lo, d / 2, static_cast<double>(rope_theta));
+    rope_tables_kernel<<<2 * sm_count(), 128, 0, s>>>(hi, hi_rows, lo, d / 2, static_cast<double>(rope_theta));
     // keys of the stream and of the prefix (grids from the capacities: blocks past the
     // round's rows return); the queries here only for the warp-MMA kernel: the tcgen05
     // kernel rotates each query tile in shared memory once it has landed
@@ -346,7 +351,7 @@ extern "C" int fork_attn_noalloc(const fork_meta* m, const uint16_t* q, const ui
   int rc = check_meta(m, &L);
   if (rc != FORK_OK) return rc;
   if (prefix_rows < 0 || Hkv < 1 || (d != 64 && d != 128)) return FORK_EINVAL;
-  const size_t need = fork_attn_workspace_bytes(L.T_cap, prefix_rows, Hq, Hkv, d, rope_theta);
+  const size_t need = fork_attn_workspace_bytes(L.T_cap, prefix_rows, Hq, Hkv, d, rope_theta, flags);
   if (need > FORK_NOALLOC_SCRATCH_BYTES) return FORK_ECAPACITY;
   void* scratch = nullptr;
   if (need > 0 && (rc = noalloc_scratch(&scratch)) != FORK_OK) return rc;

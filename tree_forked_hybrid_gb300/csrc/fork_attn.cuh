@@ -34,7 +34,24 @@ struct AttnParams {
   float scale_log2;          // scale * log2(e)
   int rope_hi_rows;          // rows of rope_hi
   int rotate_q;              // queries are rotated by the attention kernel (tcgen05 path)
+  int checks;                // FORK_CHECKS
+  int stall;                 // FORK_TEST_STALL (tcgen05 path)
+  uint64_t wait_ns;          // limit of a bounded wait
 };
+
+// FORK_CHECKS: work item w's segment, its offset, its request and its trunk range lie
+// inside the round (the prefix range is checked against the prefix buffers separately).
+__device__ __forceinline__ bool attn_item_in_bounds(const int32_t* meta, const MetaLayout& L, int w) {
+  const int T = meta[H_T], nseg = meta[H_NSEG], R = meta[H_R];
+  if (meta[H_NWORK] > L.max_work) return false;
+  const int s = meta[L.work_seg + w];
+  if (s < 0 || s >= nseg || s >= L.max_seg) return false;
+  const int st = meta[L.seg_start + s], len = meta[L.seg_len + s], off = meta[L.work_off + w];
+  const int j = meta[L.seg_req + s];
+  const int ts = meta[L.seg_trunk_start + s], tl = meta[L.seg_trunk_len + s];
+  return st >= 0 && len >= 1 && st + len <= T && off >= 0 && off < len && j >= 0 && j < R && ts >= 0 &&
+         tl >= 0 && ts + tl <= T;
+}
 
 // (cos, sin) of t * f_i from the two-level table: t = 64 a + b,
 // angle(t) = angle(64 a) + angle(b), combined by the angle-addition formula.

@@ -86,6 +86,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   const int g = blockIdx.y;  // kv head
   const int G = p.G;
   const int tile = kRows / G;
+  if (p.checks && !attn_item_in_bounds(meta, L, w)) {
+    if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_CHECK);
+    return;
+  }
 
   const int s = meta[L.work_seg + w];
   const int off = meta[L.work_off + w];

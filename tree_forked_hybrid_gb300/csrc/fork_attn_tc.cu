@@ -59,7 +59,7 @@ struct TcLayout {
 
 enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_VFULL2, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
            B_VEMPTY1, B_VEMPTY2, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_QROT,
-           B_COUNT };
+           B_STALL, B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -91,8 +91,9 @@ struct TcParams {
   uint16_t* o;
   const float2* rope_hi;  // (cos, sin) tables of the rotary embedding (rotate_q)
   const float2* rope_lo;
-  int Hq, Hkv, G, prefix_rows, window, two_tiles, rotate_q, rope_hi_rows;
+  int Hq, Hkv, G, prefix_rows, window, two_tiles, rotate_q, rope_hi_rows, checks, stall;
   float scale_log2;
+  uint64_t wait_ns;
 };
 
 // Rotary embedding of one query row held in a 128-byte-swizzled tile (boxes of 64
@@ -154,6 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = blockIdx.y;
   const int G = p.G;
   const int tile = kRows / G;  // tokens per MMA tile
+  if (p.checks && !attn_item_in_bounds(meta, L, w)) {
+    if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_CHECK);
+    return;
+  }
   const int s = meta[L.work_seg + w];
   const int off = meta[L.work_off + w];
   const int seg_start = meta[L.seg_start + s];
@@ -229,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(&bars[B_FIN], 1);
     tc::mbar_init(&bars[B_QROT], 256);
+    tc::mbar_init(&bars[B_STALL], 1);  // completed by nothing (FORK_TEST_STALL)
     *abort = 0;
     const int tab[12] = {lo0, cnt0, r_len_0, r_pos0_0, lo1, cnt1, r_len_1, r_pos0_1, lo2, cnt2, r_len_2, r_pos0_2};
     for (int i = 0; i < 12; ++i) rtab[i] = tab[i];
@@ -272,19 +278,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* km = kt.r == 0 ? &pkmap : &kmap;
         const CUtensorMap* vm = kt.r == 0 ? &pvmap : &vmap;
         const int row = kt.row0 + kt.t * kKeys;
-        if (f >= 2 && !tc::mbar_wait(&bars[B_KEMPTY0 + st], ((f >> 1) - 1) & 1, abort)) break;
+        if (f >= 2 && !tc::mbar_wait(&bars[B_KEMPTY0 + st], ((f >> 1) - 1) & 1, abort, p.wait_ns)) break;
         tc::mbar_expect_tx(&bars[B_KFULL0 + st], NB * kBox);
         for (int b = 0; b < NB; ++b) tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KFULL0 + st], b * 64, g, row);
-        if (f >= kVStages && !tc::mbar_wait(&bars[B_VEMPTY0 + vs], ((f / kVStages) - 1) & 1, abort)) break;
+        if (f >= kVStages && !tc::mbar_wait(&bars[B_VEMPTY0 + vs], ((f / kVStages) - 1) & 1, abort, p.wait_ns))
+          break;
         tc::mbar_expect_tx(&bars[B_VFULL0 + vs], NB * kBox);
         for (int b = 0; b < NB; ++b) tc::tma_load_3d(sV + (vs * NB + b) * kBox, vm, &bars[B_VFULL0 + vs], b * 64, g, row);
         issued = f + 1;
       }
-      // drain: the last loads issued complete by themselves
-      tc::mbar_wait(&bars[B_QFULL], 0, abort);
-      for (int f = max(0, issued - 2); f < issued; ++f) tc::mbar_wait(&bars[B_KFULL0 + (f & 1)], (f >> 1) & 1, abort);
+      // drain: the Q tiles and the last loads issued into each slot complete by themselves
+      // (no load is issued into a slot after them, so their phases are the slots' last)
+      tc::mbar_drain(&bars[B_QFULL], 0);
+      for (int f = max(0, issued - 2); f < issued; ++f) tc::mbar_drain(&bars[B_KFULL0 + (f & 1)], (f >> 1) & 1);
       for (int f = max(0, issued - kVStages); f < issued; ++f)
-        tc::mbar_wait(&bars[B_VFULL0 + f % kVStages], (f / kVStages) & 1, abort);
+        tc::mbar_drain(&bars[B_VFULL0 + f % kVStages], (f / kVStages) & 1);
     }
   } else if (warp == 9) {
     // ===================== MMA issuer =====================
@@ -298,9 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint64_t kBoxU = kBox / 16, kStageU = NB * kBox / 16;
     // every lane waits; the warp proceeds only if all of them saw the phase complete
     auto wwait = [&](int b, uint32_t par) -> bool {
-      return __all_sync(0xffffffffu, tc::mbar_wait(&bars[b], par, abort)) != 0;
+      return __all_sync(0xffffffffu, tc::mbar_wait(&bars[b], par, abort, p.wait_ns)) != 0;
     };
-    bool ok = wwait(p.rotate_q ? B_QROT : B_QFULL, 0);
+    bool ok = !p.stall || wwait(B_STALL, 0);  // FORK_TEST_STALL: runs out, nothing is issued
+    ok = ok && wwait(p.rotate_q ? B_QROT : B_QFULL, 0);
     const int last_tile = total - 1;
     // V tile f ready for the PV products; a range that ends inside the tile is followed by
     // rows that may be pad rows of the stream (any bits), zeroed here: their p is 0 but
@@ -376,10 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     }
-    // every MMA issued by this warp has completed before TMEM is released
+    // every MMA issued by this warp has completed before TMEM is released (also after an
+    // abort: the products already issued finish by themselves)
     if (lane == 0) tc::mma_commit(&bars[B_FIN]);
     __syncwarp();
-    wwait(B_FIN, 0);
+    tc::mbar_drain(&bars[B_FIN], 0);
+    __syncwarp();
   } else {
     // ===================== softmax warpgroups (tile t = warp / 4, row = tid % 128) ==========
     const int t = warp >> 2;
@@ -400,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const bool okq = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_QFULL], 0, abort));
+      const bool okq = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_QFULL], 0, abort, p.wait_ns));
       if (okq && t < ntiles) {
         const int row = tid & 127, tok = row / G;
         if (tok < min(tile, n_all - t * tile)) {
@@ -424,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       const float sl2 = p.scale_log2;
       for (int f = 0; ok && f < total; ++f) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SFULL0 + t], f & 1, abort));
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SFULL0 + t], f & 1, abort, p.wait_ns));
         if (!ok) break;
         tc::tc_fence_after();
         float sv[kKeys];
@@ -508,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_before();
         tc::mbar_arrive(&bars[B_PFULL0 + t]);
       }
-      if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OFULL0 + t], 0, abort));
+      if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OFULL0 + t], 0, abort, p.wait_ns));
       if (ok) {
         tc::tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -566,6 +577,9 @@ int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, boo
   p.rope_lo = a.rope_lo;
   p.rope_hi_rows = a.rope_hi_rows;
   p.scale_log2 = a.scale_log2;
+  p.checks = a.checks;
+  p.stall = a.stall;
+  p.wait_ns = a.wait_ns;
   dim3 grid(grid_x, a.Hkv);
   attn_tc_kernel<D><<<grid, kThreads, LY::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cuda_rc(cudaGetLastError());

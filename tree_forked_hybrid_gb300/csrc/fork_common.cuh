@@ -84,6 +84,14 @@ inline bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p)
 
 int check_device();  // FORK_OK on an sm_103 device, else FORK_EUNSUPPORTED/FORK_ECUDA
 
+// Limit of the bounded waits of a call, in nanoseconds (fork_meta.wait_us; 0 = 2 s).
+inline uint64_t wait_ns_of(const fork_meta* m) {
+  return m->wait_us == 0 ? 2000000000ull : static_cast<uint64_t>(m->wait_us) * 1000ull;
+}
+
+// Streaming multiprocessors of the current device (grid sizing), cached per device.
+int sm_count();
+
 // Record a failing CUDA runtime result for fork_last_cuda_error (per host thread);
 // returns FORK_ECUDA when e is an error, FORK_OK otherwise.
 int cuda_rc(cudaError_t e);

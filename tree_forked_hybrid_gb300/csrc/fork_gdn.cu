@@ -142,6 +142,10 @@ __global__ void __launch_bounds__(NT, 1) gdn_chunk_kernel(const GdnParams p) {
     seg = idx;
     j = idx;
   }
+  if (p.checks && !gdn_segs_in_bounds(meta, L, seg, seg + 1, j)) {
+    if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_CHECK);
+    return;
+  }
   const int h = blockIdx.y;
   const int H = p.H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -554,6 +558,9 @@ extern "C" int fork_gdn_trunk(const fork_meta* m, const uint16_t* q, const uint1
   p.S_ckpt = S_ckpt;
   p.conv_ckpt = conv_ckpt;
   p.o = o;
+  p.checks = (flags & FORK_CHECKS) ? 1 : 0;
+  p.stall = (flags & FORK_TEST_STALL) ? 1 : 0;
+  p.wait_ns = wait_ns_of(m);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 128 && !(flags & FORK_WARP_MMA)) return launch_gdn_tc(p, false, m->max_req, s);
   return d == 64 ? launch_gdn<64, false>(p, m->max_req, s) : launch_gdn<128, false>(p, m->max_req, s);
@@ -588,6 +595,9 @@ extern "C" int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const ui
   p.S_ckpt = nullptr;
   p.conv_ckpt = nullptr;
   p.o = o;
+  p.checks = (flags & FORK_CHECKS) ? 1 : 0;
+  p.stall = (flags & FORK_TEST_STALL) ? 1 : 0;
+  p.wait_ns = wait_ns_of(m);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 128 && !(flags & FORK_WARP_MMA)) return launch_gdn_tc(p, true, m->max_q, s);
   return d == 64 ? launch_gdn<64, true>(p, m->max_q, s) : launch_gdn<128, true>(p, m->max_q, s);

@@ -69,7 +69,7 @@ static_assert(Lay::SMEM <= 232448, "shared memory budget");
 static_assert(3 * kQG * 4 <= 64, "segment table");
 static_assert(Lay::RAW % 128 == 0 && Lay::RAWS % 128 == 0, "TMA destinations");
 
-enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_OUT, B_FINP, B_FINC, B_N };
+enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_OUT, B_FINP, B_FINC, B_STALL, B_N };
 
 // SFU approximations (relative error ~2^-22): 2^x, 1/x, 1/sqrt(x)
 __device__ __forceinline__ float ex2f(float x) {
@@ -154,6 +154,10 @@ __global__ void __launch_bounds__(NT, 1)
     // the CTA of question x leads a group of up to kQG consecutive questions of its request
     if (x >= meta[H_NQ]) return;
     j = meta[L.seg_req + R + x];
+    if (p.checks && (j < 0 || j >= R)) {
+      if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_CHECK);
+      return;
+    }
     const int fq = meta[L.req_first_q + j], nq = meta[L.req_n_q + j];
     if ((x - fq) % kQG != 0) return;
     seg_first = R + x;
@@ -163,6 +167,10 @@ __global__ void __launch_bounds__(NT, 1)
     j = x;
     seg_first = x;
     seg_end = x + 1;
+  }
+  if (p.checks && !gdn_segs_in_bounds(meta, L, seg_first, seg_end, j)) {
+    if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_CHECK);
+    return;
   }
   const int h = blockIdx.y;
   const int H = p.H;
@@ -195,6 +203,7 @@ __global__ void __launch_bounds__(NT, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(sm + Lay::BAR + B_N * 8 + 8);
 
   if (tid == 0) {
+    // B_STALL is completed by nothing (FORK_TEST_STALL)
     for (int b = 0; b < B_N; ++b) tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1 || b == B_OUT) ? NCH : 1);
     *abort = 0;
     tc::fence_mbar_init();
@@ -235,7 +244,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int ch = q4 * 32 + lane;     // channel = TMEM lane of this thread
     const int u0 = hf * 32;            // first token of this thread's half
     auto pwait = [&](int b, uint32_t par) -> bool {
-      return role_and(1, NP, tc::mbar_wait(&bars[b], par, abort));
+      return role_and(1, NP, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
     };
     // conv weights: the v stream for channel ch; q, k for the channel pair of the P4 mapping
     const int cp = (warp & 1) * 32 + lane, c2 = 2 * cp;
@@ -646,11 +655,12 @@ __global__ void __launch_bounds__(NT, 1)
       si = nsi;
       c0 = nc0;
     }
-    // drain: own MMAs, and a raw-row load still in flight after an abort
+    // drain: own MMAs, and a raw-row load still in flight after an abort (the last one
+    // issued: its phase is the barrier's last)
     if (tid == 0) {
       tc::mma_commit(&bars[B_FINP]);
-      tc::mbar_wait(&bars[B_FINP], 0, abort);
-      if (!ok && raw_issued > 0) tc::mbar_wait(&bars[B_RAW], (raw_issued - 1) & 1, abort);
+      tc::mbar_drain(&bars[B_FINP], 0);
+      if (!ok && raw_issued > 0) tc::mbar_drain(&bars[B_RAW], (raw_issued - 1) & 1);
     }
     asm volatile("cp.async.wait_group 0;\n" ::);
   } else {
@@ -658,7 +668,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int ct = tid - NP;
     const int v = q4 * 32 + lane;  // row of S (v index) = TMEM lane
     auto cwait = [&](int b, uint32_t par) -> bool {
-      return role_and(2, NCH, tc::mbar_wait(&bars[b], par, abort));
+      return role_and(2, NCH, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
     };
     // S <- a state from global memory (row v), or zero
     auto load_state = [&](const float* src) {
@@ -684,7 +694,7 @@ __global__ void __launch_bounds__(NT, 1)
       tc::tmem_wait_st();
     };
     if (!BRANCH) load_state(S0);
-    bool ok = true;
+    bool ok = !p.stall || cwait(B_STALL, 0);  // FORK_TEST_STALL: runs out, nothing is issued
     int si = first_seg(seg_first), c0 = 0, k = 0;
     while (ok && si < seg_end) {
       const int start = seg_start(si), len = seg_len(si), pos0 = seg_pos0(si);
@@ -850,7 +860,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (ct == 0) {
       tc::mma_commit(&bars[B_FINC]);
-      tc::mbar_wait(&bars[B_FINC], 0, abort);
+      tc::mbar_drain(&bars[B_FINC], 0);
     }
   }
 

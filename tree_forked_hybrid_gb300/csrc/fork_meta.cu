@@ -31,6 +31,18 @@ int check_device() {
   return (major == 10 && minor == 3) ? FORK_OK : FORK_EUNSUPPORTED;
 }
 
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 static bool valid_caps(int32_t T_cap, int32_t max_req, int32_t max_q) {
   return T_cap >= 1 && T_cap <= (1 << 20) && max_req >= 1 && max_req <= (1 << 16) && max_q >= 0 &&
          max_q <= (1 << 18);
@@ -234,6 +246,46 @@ __global__ void __launch_bounds__(256) meta_tokens_kernel(int32_t* __restrict__ 
   }
 }
 
+// FORK_CHECKS: one block re-derives what the tables must satisfy and sets
+// FORK_STATUS_CHECK on any mismatch.  Segments tile [0, T) in order, trunks
+// first; each token's (request, branch, position) is its segment's; pad rows are
+// -1; each work item lies inside its segment; question last rows end their
+// segments.
+__global__ void __launch_bounds__(1024) meta_check_kernel(int32_t* __restrict__ meta, MetaLayout L) {
+  if (meta[H_VALID] == 0) return;
+  const int R = meta[H_R], Nq = meta[H_NQ], T = meta[H_T], nseg = meta[H_NSEG], nwork = meta[H_NWORK];
+  const int tile = meta[H_TILE];
+  int bad = (nseg != R + Nq || T < 0 || T > L.T_cap || R > L.max_req || Nq > L.max_q || nwork > L.max_work ||
+             tile < 1) ? 1 : 0;
+  if (!bad) {
+    for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
+      const int st = meta[L.seg_start + s], len = meta[L.seg_len + s], j = meta[L.seg_req + s];
+      const int c = meta[L.seg_branch + s];
+      const int end = s + 1 < nseg ? meta[L.seg_start + s + 1] : T;
+      if (st < 0 || len < 0 || st + len != end || j < 0 || j >= R) { bad = 1; continue; }
+      if ((s < R) != (c == 0) || (s >= R && len < 1)) bad = 1;
+      if (meta[L.seg_trunk_start + s] != meta[L.seg_start + j] || meta[L.seg_trunk_len + s] != meta[L.seg_len + j] ||
+          meta[L.seg_state_idx + s] != j)
+        bad = 1;
+      if (s >= R && meta[L.q_last + (s - R)] != st + len - 1) bad = 1;
+    }
+    if (nseg > 0 && meta[L.seg_start] != 0) bad = 1;
+    for (int w = threadIdx.x; w < nwork; w += blockDim.x) {
+      const int s = meta[L.work_seg + w], off = meta[L.work_off + w];
+      if (s < 0 || s >= nseg || off < 0 || off % tile != 0 || off >= meta[L.seg_len + s]) bad = 1;
+    }
+    for (int x = threadIdx.x; x < L.T_cap; x += blockDim.x) {
+      const int j = meta[L.tok_req + x], c = meta[L.tok_branch + x], t = meta[L.tok_pos + x];
+      if (x >= T) {
+        if (j != -1 || c != -1 || t != -1) bad = 1;
+      } else if (j < 0 || j >= R || c < 0 || t < 0) {
+        bad = 1;
+      }
+    }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(meta + H_STATUS, FORK_STATUS_CHECK);
+}
+
 }  // namespace fork
 
 using namespace fork;
@@ -253,6 +305,7 @@ extern "C" int fork_meta_init(fork_meta* m, void* d_buf, size_t bytes, int32_t T
   t.max_req = max_req;
   t.max_q = max_q;
   t.tile_tokens = tile_tokens;
+  t.wait_us = 0;
   MetaLayout L;
   int rc = check_meta(&t, &L);
   if (rc != FORK_OK) return rc;
@@ -262,7 +315,6 @@ extern "C" int fork_meta_init(fork_meta* m, void* d_buf, size_t bytes, int32_t T
 
 extern "C" int fork_build_meta(const fork_meta* m, const int32_t* d_desc, int32_t R, int32_t Nq,
                                uint32_t flags, void* stream) {
-  (void)flags;
   MetaLayout L;
   int rc = check_meta(m, &L);
   if (rc != FORK_OK) return rc;
@@ -273,6 +325,7 @@ extern "C" int fork_build_meta(const fork_meta* m, const int32_t* d_desc, int32_
   int32_t* meta = static_cast<int32_t*>(m->d_buf);
   meta_tables_kernel<<<1, 1024, 0, s>>>(d_desc, R, Nq, meta, L, m->tile_tokens);
   meta_tokens_kernel<<<L.max_seg + 1, 256, 0, s>>>(meta, L);
+  if (flags & FORK_CHECKS) meta_check_kernel<<<1, 1024, 0, s>>>(meta, L);
   return cuda_rc(cudaGetLastError());
 }
 

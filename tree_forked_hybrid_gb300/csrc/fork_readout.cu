@@ -13,12 +13,17 @@ __global__ void __launch_bounds__(256) readout_kernel(const int32_t* __restrict_
                                                       const uint16_t* __restrict__ h, int D,
                                                       const uint16_t* __restrict__ w,
                                                       const int32_t* __restrict__ off,
-                                                      float* __restrict__ p) {
+                                                      float* __restrict__ p, int checks) {
   if (meta[H_VALID] == 0) return;
   const int i = blockIdx.x;
   if (i >= meta[H_NQ]) return;
   const int a = off[i], b = off[i + 1];
   const int x = meta[L.q_last + i];
+  // FORK_CHECKS: offsets start at 0 and grow (at least one option each); the row is a stream row
+  if (checks && (a < 0 || b <= a || (i == 0 && a != 0) || x < 0 || x >= meta[H_T])) {
+    if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_CHECK);
+    return;
+  }
   const uint4* hrow = reinterpret_cast<const uint4*>(h + static_cast<int64_t>(x) * D);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = D / 8;
@@ -58,7 +63,6 @@ using namespace fork;
 
 extern "C" int fork_readout(const fork_meta* m, const uint16_t* h, int32_t D, const uint16_t* w_opt,
                             const int32_t* opt_off, float* p, uint32_t flags, void* stream) {
-  (void)flags;
   MetaLayout L;
   int rc = check_meta(m, &L);
   if (rc != FORK_OK) return rc;
@@ -69,6 +73,6 @@ extern "C" int fork_readout(const fork_meta* m, const uint16_t* h, int32_t D, co
   if (m->max_q == 0) return FORK_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   readout_kernel<<<m->max_q, 256, 0, s>>>(static_cast<const int32_t*>(m->d_buf), L, h, D, w_opt,
-                                         opt_off, p);
+                                         opt_off, p, (flags & FORK_CHECKS) ? 1 : 0);
   return cuda_rc(cudaGetLastError());
 }

@@ -8,7 +8,8 @@
 namespace fork {
 namespace tc {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait longer than 2 s is a failure
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // default limit of a wait: 2 s
+constexpr uint64_t kDrainLimitNs = 2000000000ull;  // limit of a wait for the CTA's own copies / products
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -56,18 +57,30 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 // Wait for the completion of the barrier phase with the given parity.  Gives
-// up (returns false, sets *abort) after kWaitLimitNs or when another role of
-// the CTA has already given up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// up (returns false, sets *abort) after limit_ns or when another role of the
+// CTA has already given up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
+  }
+}
+// Wait for a phase that the CTA's own bulk copies or tensor-core products
+// complete (they finish by themselves once issued): used before the CTA frees
+// tensor memory or exits, so it does not give up when another role has, only
+// after kDrainLimitNs.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (globaltimer() - t0 > kDrainLimitNs) return false;
   }
 }
 

@@ -15,10 +15,14 @@ import torch
 from . import build as _build
 
 STATUS = {0: "FORK_OK", 1: "FORK_EINVAL", 2: "FORK_ECAPACITY", 3: "FORK_EUNSUPPORTED", 4: "FORK_ECUDA"}
-STATUS_BITS = {0x1: "BAD_DESC", 0x2: "CAPACITY", 0x4: "BAD_CKPT", 0x8: "TIMEOUT", 0x10: "BAD_PREFIX"}
+STATUS_BITS = {0x1: "BAD_DESC", 0x2: "CAPACITY", 0x4: "BAD_CKPT", 0x8: "TIMEOUT", 0x10: "BAD_PREFIX",
+               0x20: "CHECK"}
+FORK_STATUS_TIMEOUT = 0x8
+FORK_STATUS_CHECK = 0x20
 FORK_DETERMINISTIC = 0x1
 FORK_CHECKS = 0x2
 FORK_WARP_MMA = 0x4
+FORK_TEST_STALL = 0x100
 FORK_NOALLOC_SCRATCH_BYTES = 32 << 20  # size of the library's scratch array (include/forkattn.h)
 
 _lib = None
@@ -34,7 +38,8 @@ class ForkError(RuntimeError):
 
 class fork_meta(ctypes.Structure):
     _fields_ = [("d_buf", ctypes.c_void_p), ("bytes", ctypes.c_size_t), ("T_cap", ctypes.c_int32),
-                ("max_req", ctypes.c_int32), ("max_q", ctypes.c_int32), ("tile_tokens", ctypes.c_int32)]
+                ("max_req", ctypes.c_int32), ("max_q", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
+                ("wait_us", ctypes.c_uint32)]
 
 
 def lib_path() -> str:
@@ -58,7 +63,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fork_build_meta": (ctypes.c_int, [MP, vp, i32, i32, u32, vp]),
         "fork_read_status": (ctypes.c_int, [MP, ctypes.POINTER(i32), vp]),
         "fork_last_cuda_error": (ctypes.c_int, []),
-        "fork_attn_workspace_bytes": (sz, [i32, i32, i32, i32, i32, f32]),
+        "fork_attn_workspace_bytes": (sz, [i32, i32, i32, i32, i32, f32, u32]),
         "fork_attn": (ctypes.c_int, [MP, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, vp, vp, i32, vp,
                                      sz, u32, vp]),
         "fork_attn_noalloc": (ctypes.c_int, [MP, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, vp, vp, i32,
@@ -114,6 +119,10 @@ class Meta:
                                                   nbytes, T_cap, max_req, max_q, tile_tokens))
         self.T_cap, self.max_req, self.max_q, self.tile_tokens = T_cap, max_req, max_q, tile_tokens
 
+    def set_wait_limit_us(self, us: int):
+        """Limit of the kernels' bounded waits for later calls (0 = the default 2 s)."""
+        self.handle.wait_us = int(us)
+
     @property
     def ref(self):
         return ctypes.byref(self.handle)
@@ -133,8 +142,9 @@ def fork_read_status(meta: Meta, stream=None) -> int:
     return out.value
 
 
-def fork_attn_workspace_bytes(T_cap: int, prefix_rows: int, Hq: int, Hkv: int, d: int, rope_theta: float) -> int:
-    return load().fork_attn_workspace_bytes(T_cap, prefix_rows, Hq, Hkv, d, rope_theta)
+def fork_attn_workspace_bytes(T_cap: int, prefix_rows: int, Hq: int, Hkv: int, d: int, rope_theta: float,
+                              flags: int = 0) -> int:
+    return load().fork_attn_workspace_bytes(T_cap, prefix_rows, Hq, Hkv, d, rope_theta, flags)
 
 
 def fork_attn(meta: Meta, q, k, v, o, Hq: int, Hkv: int, d: int, window: int, rope_theta: float,

@@ -74,7 +74,7 @@ class DeviceRound:
                          for a in rnd.attn_shapes}
         self.attn_ws = {}
         for a in rnd.attn_shapes:
-            nb = F.fork_attn_workspace_bytes(T_cap, self.prefix_rows, a.Hq, a.Hkv, a.d, a.rope_theta)
+            nb = F.fork_attn_workspace_bytes(T_cap, self.prefix_rows, a.Hq, a.Hkv, a.d, a.rope_theta, flags)
             self.attn_ws[a.name] = torch.empty(max(nb, 16), dtype=torch.uint8, device=device) if nb else None
         g = rnd.gdn_shape
         if g.dk != g.dv:
