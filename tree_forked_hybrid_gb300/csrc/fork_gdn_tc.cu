@@ -1,32 +1,42 @@
-// Two-call forked Gated DeltaNet on the 5th-generation tensor cores (tcgen05, TF32).
+// Two-call forked Gated DeltaNet on the 5th-generation tensor cores (tcgen05, fp16 operands).
 //
 // Gated delta rule of the rainbus summary "前置知识", in the chunked form that the
 // DFlash-TfM summary ("GDN을 위한 롤백 없는 트리 검증") solves with a Gram matrix and a
 // triangular solve.  For a chunk of C = 64 tokens with start state S0 (d_v x d_k),
-// G_t = sum_{s<=t} log a_s, Gamma_ts = exp(G_t - G_s),
+// G_t = sum_{s<=t} log a_s, Gamma_ts = exp(G_t - G_s):
 //   A_ts = eta_t Gamma_ts k_t.k_s (s < t),  T = (I + A)^{-1}
 //   W = T diag(eta e^G) K,  U~ = T diag(eta) V        (independent of S0)
 //   U = U~ - W S0^T
 //   O = diag(e^G) Q S0^T + (tril(Gamma) * Q K^T) U
 //   S = e^{G_last} S0 + U^T diag(Gamma_last) K.
-// Everything above the line "U = ..." depends only on the chunk's inputs, so it is
-// prepared for chunk k+1 while the state of chunk k is being updated:
+// The L2 normalisation of q and k is never applied to a tile: with Y the conv + SiLU
+// rows and n_t = (sum_c Y_tc^2 + 1e-6)^(-1/2), K = diag(n_k) Y_k and Q = diag(n_q) Y_q,
+// so every product above takes the norms as row or column factors of a small matrix
+// (P, A, T diag(.), the output scale, the state-update scale) and the tensor cores read
+// Y itself.
 //
 // One CTA = one trunk (call 1) or a group of up to kQG questions of one request
-// (call 2) x one head; d = 128.  12 warps:
-//   warps 0-7   prep: raw q/k/v rows by TMA (67 rows: the chunk and the three before
-//               it), gates, causal conv + SiLU (eta V written straight into tensor
-//               memory as an MMA operand), L2 norm, Q K^T products, P and A, T by
-//               blocked forward substitution, then W^T = (eta e^G K)^T T^T and
-//               U~^T = (eta V)^T T^T on the tensor cores; -W replaces K in the
-//               operand tile.
-//   warps 8-11  state chain (thread = TMEM lane = row v of S): U^T = U~^T - S W^T and
-//               X = S Q^T (A operand S read from tensor memory), U^T rounded to TF32,
-//               X scaled by e^G, S by e^{G_last}, then O^T = X + U^T P^T and
-//               S += U^T diag(Gamma_last) K, and the output rows.
-// S (128 x 128 fp32) stays in tensor memory for the whole segment.  Operands written
-// by threads are rounded to TF32 (nearest); T is formed in fp32.  Every wait is
-// bounded and agreed by the threads of its role.
+// (call 2) x one head; d = 128.  16 warps:
+//   warps 0-11  prep of chunk k+1 (everything above the line "U = ..."):
+//               raw q/k/v rows by TMA (the chunk and the three rows before it, 128-byte
+//               swizzled), thread = (stream, channel half, token): causal conv + SiLU of
+//               64 channels, fp16 rows into the operand tiles, partial sums of squares;
+//               gates; [Y_q; Y_k] Y_k^T on the tensor cores -> P (fp16) and A (fp32);
+//               T = (I + A)^{-1} in fp32 (16x16 diagonal blocks by forward substitution,
+//               the rest in two levels); T diag(eta e^G n_k) and T diag(eta) as fp16
+//               tiles; W^T = Y_k^T (T diag(eta e^G n_k))^T and U~^T = Y_v^T (T diag(eta))^T
+//               on the tensor cores; -W as an fp16 tile.
+//   warps 12-15 state chain of chunk k (thread = TMEM lane = row v of S): U^T = U~^T -
+//               S W^T and X = S Y_q^T (A operand: an fp16 copy of S in tensor memory);
+//               U^T to fp16 twice (plain, and scaled by Gamma_last n_k for the update); X
+//               scaled by e^G n_q; S by e^{G_last}; then O^T = X + U^T P^T and
+//               S += (U^T diag(Gamma_last n_k)) Y_k; output rows; the fp16 copy of S.
+// S (128 x 128 fp32) stays in tensor memory for the whole segment.  Operands are fp16
+// (10-bit mantissa, as TF32; the values stay far inside the fp16 range), products
+// accumulate in fp32, T is formed in fp32.  Every wait is bounded and agreed by the
+// threads of its role.
+#include <cuda_fp16.h>
+
 #include "fork_attn.cuh"
 #include "fork_gdn.cuh"
 #include "tc_ptx.cuh"
@@ -36,40 +46,48 @@ namespace fork {
 namespace {
 constexpr int D = 128;
 constexpr int C = 64;
-constexpr int NT = 384;       // 8 prep warps + 4 chain warps
-constexpr int NP = 256;       // prep threads
-constexpr int NCH = 128;      // chain threads
+constexpr int NP = 384;        // prep threads (12 warps)
+constexpr int NCH = 128;       // chain threads (4 warps)
+constexpr int NT = NP + NCH;
 constexpr int KW = 4;
 constexpr int HR = C + KW - 1;  // raw rows staged per chunk
 constexpr int LDC = C + 4;      // plain 64-wide fp32 tiles
 constexpr int kQG = 4;          // questions per CTA in the branch call
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S, two (U, X) slots, eta V, Q K^T / (eta e^G K)^T
-constexpr uint32_t T_S = 0, T_AV = 384, T_M1 = 448;
-__device__ __forceinline__ uint32_t t_u(int slot) { return 128u + 128u * slot; }
-__device__ __forceinline__ uint32_t t_x(int slot) { return 192u + 128u * slot; }
+// TMEM columns: S (fp32), its fp16 copy, two U slots, X, the prep's product
+constexpr uint32_t T_S = 0, T_S16 = 128, T_X = 320, T_M1 = 384;
+__device__ __forceinline__ uint32_t t_u(int slot) { return 192u + 64u * slot; }
 
 struct Lay {
-  static constexpr int QK = 0;                 // [Q; K -> -W] 128 rows x 128 fp32 (4 boxes of 32 columns)
-  static constexpr int KT = QK + 4 * 16384;    // diag(Gamma_last) K, transposed: 128 rows (d_k) x 64 (2 boxes)
-  static constexpr int TB = KT + 2 * 16384;    // T: 64 x 64 (2 boxes)
-  static constexpr int PB = TB + 2 * 8192;     // P: 64 x 64 (2 boxes)
-  static constexpr int RAWS = HR * D * 2;      // one stream's raw rows (bf16)
-  static constexpr int RAW = PB + 2 * 8192;    // [3][HR][D] bf16
-  static constexpr int AM = RAW + 3 * RAWS;    // plain A [64][LDC]
-  static constexpr int TM = AM + C * LDC * 4;  // plain T [64][LDC]
-  static constexpr int XS = TM + C * LDC * 4;  // inverse scratch [3*256]
-  static constexpr int GT = XS + 3 * 256 * 4;  // raw alpha, eta [2][64]; per slot G, EG, GL, ETA, IG [2][5][64]
-  static constexpr int SEG = GT + (2 * C + 2 * 5 * C) * 4;  // this CTA's segments: start, len, pos0
+  static constexpr int RAWH = 9216;               // one 64-channel half of a stream's raw rows (HR used)
+  static constexpr int RAW = 0;                   // [3 streams][2 halves] bf16, 128-byte swizzled
+  static constexpr int YTS = 32768;               // one slot: [2 boxes][Y_q rows 0-63; Y_k rows 64-127][128 B]
+  static constexpr int YT = RAW + 6 * RAWH;       // [2 slots]
+  static constexpr int YV = YT + 2 * YTS;         // Y_v [2 boxes][64 rows][128 B]
+  static constexpr int WT = YV + 16384;           // -W  [2 boxes][64 rows][128 B]
+  static constexpr int PB = WT + 16384;           // P   [2 slots][64 rows][128 B]; output staging
+  static constexpr int TP = PB + 2 * 8192;        // T diag(eta e^G n_k) [64][128 B]
+  static constexpr int TPP = TP + 8192;           // T diag(eta)         [64][128 B]
+  static constexpr int AM = TPP + 8192;           // A fp32 [64][LDC]
+  static constexpr int TM = AM + C * LDC * 4;     // T fp32 [64][LDC]
+  static constexpr int XS = TM + C * LDC * 4;     // inverse scratch [3*256]
+  static constexpr int SS = XS + 3 * 256 * 4;     // partial sums of squares [2 halves][128 rows]
+  static constexpr int GA = SS + 2 * 128 * 4;     // raw alpha, eta of the next chunk [2][64]
+  static constexpr int GS = GA + 2 * C * 4;       // per slot [G, EG, GL, ETA, IG, NQ, NK][64]
+  static constexpr int SEG = GS + 2 * 7 * C * 4;  // this CTA's segments: start, len, pos0
   static constexpr int BAR = SEG + 64;
   static constexpr int BYTES = BAR + 256;
   static constexpr int SMEM = BYTES + 1024;
 };
 static_assert(Lay::SMEM <= 232448, "shared memory budget");
 static_assert(3 * kQG * 4 <= 64, "segment table");
-static_assert(Lay::RAW % 128 == 0 && Lay::RAWS % 128 == 0, "TMA destinations");
+static_assert(Lay::YT % 1024 == 0 && Lay::YV % 1024 == 0 && Lay::WT % 1024 == 0 && Lay::PB % 1024 == 0 &&
+                  Lay::TP % 1024 == 0 && Lay::TPP % 1024 == 0 && Lay::RAWH % 1024 == 0,
+              "128-byte-swizzled tiles start on 1024-byte boundaries");
+static_assert(HR * 128 <= Lay::RAWH, "raw rows");
 
-enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_OUT, B_FINP, B_FINC, B_STALL, B_N };
+enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_FINP, B_FINC, B_STALL, B_N };
+enum { G_G = 0, G_EG, G_GL, G_ETA, G_IG, G_NQ, G_NK };
 
 // SFU approximations (relative error ~2^-22): 2^x, 1/x, 1/sqrt(x)
 __device__ __forceinline__ float ex2f(float x) {
@@ -91,26 +109,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 // SiLU(y) = y / (1 + e^-y)
 __device__ __forceinline__ float silu(float y) { return y * rcpf(1.f + ex2f(-y * kLog2e)); }
 
-// x rounded to TF32 (10-bit mantissa), to nearest with ties away from zero: add half
-// a unit of the last kept place to the magnitude bits and clear the 13 dropped bits.
-// Exact for finite x (a carry into the exponent is the correct rounding up); two
-// integer operations instead of a conversion instruction.
-__device__ __forceinline__ uint32_t tf32_bits(float x) {
-  return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
-// byte offset of fp32 element (r, c) in a K-major 128-byte-swizzled tile of
-// 32-column boxes of `rows` rows
-__device__ __forceinline__ int swz(int rows, int r, int c) {
-  const int cc = c & 31;
-  return (c >> 5) * rows * 128 + r * 128 + ((((cc >> 2) ^ (r & 7))) << 4) + ((cc & 3) << 2);
-}
+// byte offset of 16-byte chunk j of row r in a 128-byte-swizzled box of 128-byte rows
+__device__ __forceinline__ int sw(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
 __device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(tc::smem_u32(dst)), "l"(src),
                "r"(valid ? 4 : 0));
 }
-__device__ __forceinline__ float bf_at(const unsigned char* p) {
-  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
-}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 // 32 consecutive fp32 values (16-byte aligned) into registers with 8 vector loads
 __device__ __forceinline__ void ld32f(const float* src, float* dst) {
 #pragma unroll
@@ -134,6 +144,10 @@ __device__ __forceinline__ bool role_and(int id, int n, bool ok) {
 }
 __device__ __forceinline__ void role_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// the i-th 32-bit word of a 16-byte vector (i a compile-time constant after unrolling)
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 }  // namespace
 
@@ -186,25 +200,28 @@ __global__ void __launch_bounds__(NT, 1)
   const float* S0 = (BRANCH || resumed) ? p.state_in : nullptr;
   const int64_t state_base = (static_cast<int64_t>(j) * H + h) * D * D;
 
-  unsigned char* qk = sm + Lay::QK;
-  unsigned char* kt = sm + Lay::KT;
-  unsigned char* tb = sm + Lay::TB;
-  unsigned char* pb = sm + Lay::PB;
   unsigned char* raw = sm + Lay::RAW;
+  unsigned char* yv = sm + Lay::YV;
+  unsigned char* wt = sm + Lay::WT;
+  unsigned char* tp = sm + Lay::TP;
+  unsigned char* tpp = sm + Lay::TPP;
   float* am = reinterpret_cast<float*>(sm + Lay::AM);
   float* tm = reinterpret_cast<float*>(sm + Lay::TM);
   float* xs = reinterpret_cast<float*>(sm + Lay::XS);
-  float* ga = reinterpret_cast<float*>(sm + Lay::GT);
+  float* ssq = reinterpret_cast<float*>(sm + Lay::SS);
+  float* ga = reinterpret_cast<float*>(sm + Lay::GA);
   float* ge = ga + C;
-  float* gslot = ge + C;  // [slot][G, EG, GL, ETA, IG][64]
   int* segt = reinterpret_cast<int*>(sm + Lay::SEG);  // [kQG][3], read instead of the metadata
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::BAR + B_N * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + Lay::BAR + B_N * 8 + 8);
+  auto yt = [&](int slot) { return sm + Lay::YT + slot * Lay::YTS; };
+  auto pbt = [&](int slot) { return sm + Lay::PB + slot * 8192; };
+  auto gate = [&](int slot, int a) { return reinterpret_cast<float*>(sm + Lay::GS) + (slot * 7 + a) * C; };
 
   if (tid == 0) {
     // B_STALL is completed by nothing (FORK_TEST_STALL)
-    for (int b = 0; b < B_N; ++b) tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1 || b == B_OUT) ? NCH : 1);
+    for (int b = 0; b < B_N; ++b) tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1) ? NCH : 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -225,8 +242,6 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t qk_a = tc::smem_u32(qk), kt_a = tc::smem_u32(kt), tb_a = tc::smem_u32(tb),
-                 pb_a = tc::smem_u32(pb);
   const int q4 = warp & 3;                                  // TMEM lane quarter of this warp
   const uint32_t lb = static_cast<uint32_t>(q4 * 32) << 16;  // its lane base
   auto seg_start = [&](int s) { return segt[3 * (s - seg_first)]; };
@@ -238,44 +253,36 @@ __global__ void __launch_bounds__(NT, 1)
     return s;
   };
 
-  if (warp < 8) {
-    // ============================ prep (256 threads) ============================
-    const int hf = warp >> 2;          // column / token half
-    const int ch = q4 * 32 + lane;     // channel = TMEM lane of this thread
-    const int u0 = hf * 32;            // first token of this thread's half
+  if (warp < NP / 32) {
+    // ============================ prep (384 threads) ============================
     auto pwait = [&](int b, uint32_t par) -> bool {
       return role_and(1, NP, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
     };
-    // conv weights: the v stream for channel ch; q, k for the channel pair of the P4 mapping
-    const int cp = (warp & 1) * 32 + lane, c2 = 2 * cp;
-    float wv[KW], wq[2][2][KW];
-#pragma unroll
-    for (int i = 0; i < KW; ++i) wv[i] = p.conv_w[((static_cast<int64_t>(2) * H + h) * D + ch) * KW + i];
-#pragma unroll
-    for (int st = 0; st < 2; ++st)
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-        for (int i = 0; i < KW; ++i)
-          wq[st][cc][i] = p.conv_w[((static_cast<int64_t>(st) * H + h) * D + c2 + cc) * KW + i];
-    // raw rows start-3 .. start+63 of the three streams (TMA; rows outside the tensor read
-    // as zero) and the gates of a chunk
+    // conv mapping: stream st, channel half hf, token u (one row of 64 channels)
+    const int st = tid >> 7, hf = (tid >> 6) & 1, u = tid & 63;
+    const float4* wrow =
+        reinterpret_cast<const float4*>(p.conv_w) + ((static_cast<int64_t>(st) * H + h) * D + hf * 64);
     const CUtensorMap* maps[3] = {&qmap, &kmap, &vmap};
     int raw_issued = 0;
     auto issue_loads = [&](int s, int cc) {
       const int st0 = seg_start(s), ln = seg_len(s);
       if (tid == 0) {
         tc::fence_proxy_async_smem();  // the rows were last read (and patched) by threads
-        tc::mbar_expect_tx(&bars[B_RAW], 3 * Lay::RAWS);
+        tc::mbar_expect_tx(&bars[B_RAW], 6 * HR * 128);
 #pragma unroll
-        for (int st = 0; st < 3; ++st) tc::tma_load_3d(raw + st * Lay::RAWS, maps[st], &bars[B_RAW], 0, h, st0 + cc - (KW - 1));
+        for (int s3 = 0; s3 < 3; ++s3)
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+            tc::tma_load_3d(raw + (s3 * 2 + half) * Lay::RAWH, maps[s3], &bars[B_RAW], half * 64, h,
+                            st0 + cc - (KW - 1));
       }
       ++raw_issued;
       if (tid < 2 * C) {
-        const int u = tid & (C - 1);
-        const bool valid = cc + u < ln;
-        const float* src = (tid < C ? p.alpha : p.eta) + (static_cast<int64_t>(st0 + (valid ? cc + u : 0)) * H + h);
-        cp_async4(tid < C ? &ga[u] : &ge[u], src, valid);
+        const int uu = tid & (C - 1);
+        const bool valid = cc + uu < ln;
+        const float* src =
+            (tid < C ? p.alpha : p.eta) + (static_cast<int64_t>(st0 + (valid ? cc + uu : 0)) * H + h);
+        cp_async4(tid < C ? &ga[uu] : &ge[uu], src, valid);
       }
       asm volatile("cp.async.commit_group;\n" ::);
     };
@@ -284,11 +291,9 @@ __global__ void __launch_bounds__(NT, 1)
       tc::prefetch_tmap(&kmap);
       tc::prefetch_tmap(&vmap);
     }
-    // blocks of T above the diagonal stay zero (the operand tile, and the blocks (0,1) and
-    // (2,3) of the fp32 copy, which the two-level products read)
+    // blocks (0,1) and (2,3) of the fp32 T stay zero (the two-level products read them)
     for (int e = tid; e < C * C; e += NP) {
       const int t = e >> 6, s = e & 63;
-      if ((s >> 4) > (t >> 4)) *reinterpret_cast<uint32_t*>(tb + swz(64, t, s)) = 0u;
       if ((s >> 4) == (t >> 4) + 1 && (t >> 4) % 2 == 0) tm[t * LDC + s] = 0.f;
     }
     bool ok = true;
@@ -298,30 +303,36 @@ __global__ void __launch_bounds__(NT, 1)
       const int len = seg_len(si);
       const int n = min(C, len - c0);
       const int slot = k & 1;
-      float* G = gslot + slot * 5 * C;
-      float* EG = G + C;
-      float* GL = EG + C;
-      float* ETA = GL + C;
-      float* IG = ETA + C;
+      float* G = gate(slot, G_G);
+      float* EG = gate(slot, G_EG);
+      float* GL = gate(slot, G_GL);
+      float* ETA = gate(slot, G_ETA);
+      float* IG = gate(slot, G_IG);
+      float* NQ = gate(slot, G_NQ);
+      float* NK = gate(slot, G_NK);
+      unsigned char* yts = yt(slot);
+      unsigned char* pb = pbt(slot);
       int nsi = si, nc0 = c0 + C;
       if (nc0 >= len) {
         nsi = first_seg(si + 1);
         nc0 = 0;
       }
-      // ---- P0: this chunk's rows and gates have landed; history rows of a segment start
+      // ---- P0: this chunk's rows and gates have landed; history rows of a segment start;
+      //      the slot's tiles are free once the chain has finished chunk k-2
       if (!(ok = pwait(B_RAW, (raw_issued - 1) & 1))) break;
       asm volatile("cp.async.wait_group 0;\n" ::);
       if (c0 == 0) {
         for (int e = tid; e < 3 * (KW - 1) * D; e += NP) {
-          const int st = e / ((KW - 1) * D), i = (e / D) % (KW - 1), c = e % D;
+          const int s3 = e / ((KW - 1) * D), i = (e / D) % (KW - 1), c = e % D;
           const uint16_t hv =
-              hist ? hist[((static_cast<int64_t>(j * (KW - 1) + i) * 3 + st) * H + h) * D + c] : uint16_t(0);
-          *reinterpret_cast<uint16_t*>(raw + st * Lay::RAWS + i * D * 2 + c * 2) = hv;
+              hist ? hist[((static_cast<int64_t>(j * (KW - 1) + i) * 3 + s3) * H + h) * D + c] : uint16_t(0);
+          *reinterpret_cast<uint16_t*>(raw + (s3 * 2 + (c >> 6)) * Lay::RAWH + sw(i, (c & 63) >> 3) + (c & 7) * 2) = hv;
         }
       }
+      if (k >= 2 && !(ok = pwait(B_EPI0 + slot, ((k - 2) >> 1) & 1))) break;
       role_sync(1, NP);
       // ---- P1: gates (warp 0; SFU log and exp: the cumulative log gate is off by at most
-      //      ~3e-5 over a chunk, far below the TF32 rounding of the operands it scales) ----
+      //      ~3e-5 over a chunk, far below the fp16 rounding of the operands it scales) ----
       if (warp == 0) {
         const int a0 = 2 * lane, a1 = a0 + 1;
         const float l0 = a0 < n ? __logf(ga[a0]) : 0.f, l1 = a1 < n ? __logf(ga[a1]) : 0.f;
@@ -343,156 +354,77 @@ __global__ void __launch_bounds__(NT, 1)
         IG[a0] = __expf(-g0);  // used only when no G of the chunk is below -80 (no overflow)
         IG[a1] = __expf(-g1);
       }
-      role_sync(1, NP);
-      // ---- P2: v stream: conv + SiLU, times eta, TF32, into TMEM (A operand of U~) ----
+      //      conv + SiLU: thread = (stream, channel half, token u); 8 groups of 8 channels,
+      //      raw rows u..u+3 (positions u-3..u), fp16 row into its operand tile, sum of squares
       {
-        const unsigned char* col = raw + 2 * Lay::RAWS + ch * 2;
-        float x0 = bf_at(col + (u0 + 0) * D * 2), x1 = bf_at(col + (u0 + 1) * D * 2), x2 = bf_at(col + (u0 + 2) * D * 2);
-        uint32_t av[32];
-        float etv[32];
-        ld32f(ETA + u0, etv);
+        const unsigned char* rb = raw + (st * 2 + hf) * Lay::RAWH;
+        unsigned char* dst = st == 2 ? yv + hf * 8192 : yts + hf * 16384;
+        const int drow = st == 1 ? C + u : u;
+        const bool valid = u < n;
+        float sq = 0.f;
+#pragma unroll 2
+        for (int g = 0; g < 8; ++g) {
+          uint4 xr[KW];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x3 = bf_at(col + (u0 + e + 3) * D * 2);
-          const float y = silu(wv[0] * x0 + wv[1] * x1 + wv[2] * x2 + wv[3] * x3);
-          av[e] = (u0 + e < n) ? tf32_bits(etv[e] * y) : 0u;
-          x0 = x1;
-          x1 = x2;
-          x2 = x3;
-        }
-        tc::tmem_st32(tmem + T_AV + u0 + lb, av);
-      }
-      // ---- P3: the operand tile is free once the chain's S [-W; Q]^T of chunk k-1 is done
-      if (k >= 1 && !(ok = pwait(B_MA, (k - 1) & 1))) break;
-      // ---- P4: q, k streams: conv + SiLU (fp32) into the [Q; K] tile; thread = channel
-      //      pair (32 per warp: 128 contiguous bytes of a raw row) x 16 tokens --------------
-      {
-        const int ub = (warp >> 1) * 16;  // first token; channels c2, c2 + 1
-        float xr[2][2][KW];  // [stream][channel][tap]: raw rows of tokens u-3 .. u
-        auto ld2 = [&](int st, int r, float* x) {
-          const uint32_t wv = *reinterpret_cast<const uint32_t*>(raw + st * Lay::RAWS + r * D * 2 + c2 * 2);
-          x[0] = __uint_as_float(wv << 16);
-          x[1] = __uint_as_float(wv & 0xffff0000u);
-        };
+          for (int i = 0; i < KW; ++i) xr[i] = *reinterpret_cast<const uint4*>(rb + sw(u + i, g));
+          float y[8];
 #pragma unroll
-        for (int st = 0; st < 2; ++st)
+          for (int e = 0; e < 8; ++e) {
+            const float4 w = __ldg(wrow + g * 8 + e);  // taps 0..3 of channel hf*64 + 8g + e
+            const float wv[KW] = {w.x, w.y, w.z, w.w};
+            float a = 0.f;
 #pragma unroll
-          for (int i = 0; i < KW - 1; ++i) {
-            float x[2];
-            ld2(st, ub + i, x);
-            xr[st][0][i] = x[0];
-            xr[st][1][i] = x[1];
-          }
-        const int cbox = (c2 >> 5) * 16384 + ((c2 & 3) << 2), cch = (c2 & 31) >> 2;
-#pragma unroll 4
-        for (int e = 0; e < 16; ++e) {
-          const int u = ub + e;
-#pragma unroll
-          for (int st = 0; st < 2; ++st) {
-            float x[2];
-            ld2(st, u + KW - 1, x);
-            float y[2];
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              xr[st][cc][KW - 1] = x[cc];
-              const float a = wq[st][cc][0] * xr[st][cc][0] + wq[st][cc][1] * xr[st][cc][1] +
-                              wq[st][cc][2] * xr[st][cc][2] + wq[st][cc][3] * xr[st][cc][3];
-              y[cc] = u < n ? silu(a) : 0.f;
-#pragma unroll
-              for (int i = 0; i < KW - 1; ++i) xr[st][cc][i] = xr[st][cc][i + 1];
+            for (int i = 0; i < KW; ++i) {
+              const uint32_t word = word_of(xr[i], e >> 1);
+              a = fmaf(wv[i], (e & 1) ? bf_hi(word) : bf_lo(word), a);
             }
-            const int r = st * C + u;
-            *reinterpret_cast<float2*>(qk + cbox + r * 128 + ((cch ^ (r & 7)) << 4)) = make_float2(y[0], y[1]);
+            y[e] = valid ? silu(a) : 0.f;
+            sq = fmaf(y[e], y[e], sq);
           }
+          *reinterpret_cast<uint4*>(dst + sw(drow, g)) =
+              make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
         }
-      }
-      role_sync(1, NP);
-      // ---- P5: next chunk's loads (the raw buffer is free); L2 norm of the 128 rows ----
-      if (nsi < seg_end) issue_loads(nsi, nc0);
-      // 8 threads per row, one 16-byte chunk of each of the 4 column boxes: the 8 lanes of
-      // a 16-byte access phase then touch 8 different chunks of one box row (all 32 banks).
-      // A thread's 4 rows (r, r + 32, r + 64, r + 96) are processed two at a time.
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int l8 = tid & 7, r0 = (tid >> 3) + 64 * half;
-        float4 xv[2][4];
-        float ss[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int r = r0 + 32 * i;
-          const unsigned char* base = qk + r * 128 + ((l8 ^ (r & 7)) << 4);
-          ss[i] = 0.f;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            xv[i][q] = *reinterpret_cast<const float4*>(base + q * 16384);
-            ss[i] += xv[i][q].x * xv[i][q].x + xv[i][q].y * xv[i][q].y + xv[i][q].z * xv[i][q].z + xv[i][q].w * xv[i][q].w;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], 1);
-          ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], 2);
-          ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], 4);
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int r = r0 + 32 * i;
-          unsigned char* base = qk + r * 128 + ((l8 ^ (r & 7)) << 4);
-          const float inv = rsqrtf_(ss[i] + 1e-6f);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(base + q * 16384) =
-                make_uint4(tf32_bits(xv[i][q].x * inv), tf32_bits(xv[i][q].y * inv), tf32_bits(xv[i][q].z * inv),
-                           tf32_bits(xv[i][q].w * inv));
-        }
+        if (st < 2) ssq[hf * 128 + st * C + u] = sq;
       }
       tc::fence_proxy_async_smem();
       role_sync(1, NP);
-      // ---- P6: [Q; K] K^T on the tensor cores; meanwhile diag(Gamma_last) K transposed
-      //      (B operand of the state update) and (eta e^G K)^T (A operand of W^T) -------
+      // ---- P2: next chunk's loads (the raw buffer is free); [Y_q; Y_k] Y_k^T on the tensor
+      //      cores; meanwhile the norms n_q, n_k ----------------------------------------------
+      if (nsi < seg_end) issue_loads(nsi, nc0);
       if (tid == 0) {
         tc::tc_fence_after();
-        constexpr uint32_t id1 = tc::idesc_tf32(128, 64, 0, 0);
-        const uint64_t dq = tc::sdesc_sw128(qk_a, 16, 1024), dk = tc::sdesc_sw128(qk_a + C * 128, 16, 1024);
+        constexpr uint32_t id1 = tc::idesc_fp16(128, 64, 0, 0);
+        const uint64_t da = tc::sdesc_sw128(tc::smem_u32(yts), 16, 1024);
+        const uint64_t db = tc::sdesc_sw128(tc::smem_u32(yts + C * 128), 16, 1024);
 #pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks) {
-          const uint64_t off = static_cast<uint64_t>((ks >> 2) * 1024 + (ks & 3) * 2);
-          tc::mma_tf32_ss(tmem + T_M1, dq + off, dk + off, id1, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t off = static_cast<uint64_t>((ks >> 2) * (16384 / 16) + (ks & 3) * 2);
+          tc::mma_bf16(tmem + T_M1, da + off, db + off, id1, ks > 0);
         }
         tc::mma_commit(&bars[B_M1]);
       }
-      // P and diag(Gamma_last) K^T are read by the chain's products of chunk k-1, and the
-      // K^T tile then stages that chunk's output rows until the chain has written them out
-      if (k >= 1 && !(ok = pwait(B_OUT, (k - 1) & 1))) break;
-      {
-        uint32_t kv4[32];
-        float glv[32];
-        ld32f(GL + u0, glv);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int t = u0 + e;
-          const float kv = *reinterpret_cast<const float*>(qk + swz(128, C + t, ch));
-          kv4[e] = tf32_bits(glv[e] * kv);
-        }
-        unsigned char* row = kt + hf * 16384 + ch * 128;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(row + ((q ^ (ch & 7)) << 4)) =
-              make_uint4(kv4[4 * q], kv4[4 * q + 1], kv4[4 * q + 2], kv4[4 * q + 3]);
+      if (tid < 2 * C) {
+        const float nv = rsqrtf_(ssq[tid] + ssq[128 + tid] + 1e-6f);
+        if (tid < C) NQ[tid] = nv; else NK[tid - C] = nv;
       }
-      // ---- P7: P (q rows) and A (k rows) from [Q; K] K^T -----------------------------
+      role_sync(1, NP);
+      // ---- P3: P (q rows) and A (k rows) from [Y_q; Y_k] Y_k^T, warps 0-7 ---------------
       if (!(ok = pwait(B_M1, k & 1))) break;
       tc::tc_fence_after();
-      {
+      if (warp < 8) {
+        const int ch = warp >> 2;  // column half
+        const int r = q4 * 32 + lane;
+        const int u0 = ch * 32;
         uint32_t v32[32];
         tc::tmem_ld32(tmem + T_M1 + u0 + lb, v32);
         tc::tmem_wait_ld();
-        const int t = ch < C ? ch : ch - C;
-        const float gt = G[t] * kLog2e, et = ETA[t], egt = EG[t];
+        const int t = r < C ? r : r - C;
+        const float gt = G[t] * kLog2e, egt = EG[t];
         // Gamma_ts = e^{G_t} e^{-G_s} while e^{-G} stays finite (G decreases along the
         // chunk), else 2^{(G_t - G_s) log2 e} per element
         const bool prod = G[C - 1] > -80.f;
-        float vals[32];
+        float vals[32], nk[32];
+        ld32f(NK + u0, nk);
         if (prod) {
           ld32f(IG + u0, vals);
 #pragma unroll
@@ -502,21 +434,21 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) vals[e] = ex2f(gt - vals[e] * kLog2e);
         }
-        // vals = Gamma_{t, u0+e}; masked and scaled by the products
-        const float scale = ch < C ? 1.f : et;
-        const int lim = ch < C ? t : t - 1;  // P keeps s <= t, A keeps s < t
+        // P_ts = n_q,t n_k,s Gamma_ts (Y_q Y_k^T)_ts (s <= t);
+        // A_ts = eta_t n_k,t n_k,s Gamma_ts (Y_k Y_k^T)_ts (s < t)
+        const float scale = r < C ? NQ[t] : ETA[t] * NK[t];
+        const int lim = r < C ? t : t - 1;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int s = u0 + e;
-          vals[e] = s <= lim ? scale * vals[e] * __uint_as_float(v32[e]) : 0.f;
+          vals[e] = s <= lim ? scale * nk[e] * vals[e] * __uint_as_float(v32[e]) : 0.f;
         }
-        if (ch < C) {
-          unsigned char* row = pb + hf * 8192 + t * 128;
+        if (r < C) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4*>(row + ((q ^ (t & 7)) << 4)) =
-                make_uint4(tf32_bits(vals[4 * q]), tf32_bits(vals[4 * q + 1]), tf32_bits(vals[4 * q + 2]),
-                           tf32_bits(vals[4 * q + 3]));
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(pb + sw(t, ch * 4 + q)) =
+                make_uint4(pack_h2(vals[8 * q], vals[8 * q + 1]), pack_h2(vals[8 * q + 2], vals[8 * q + 3]),
+                           pack_h2(vals[8 * q + 4], vals[8 * q + 5]), pack_h2(vals[8 * q + 6], vals[8 * q + 7]));
         } else {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -526,22 +458,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc::tc_fence_before();
       role_sync(1, NP);
-      tc::tc_fence_after();
-      // (eta e^G K)^T into the TMEM columns of Q K^T, now read by everyone
-      {
-        uint32_t aw[32];
-        float etv[32], egv[32];
-        ld32f(ETA + u0, etv);
-        ld32f(EG + u0, egv);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int t = u0 + e;
-          aw[e] = tf32_bits(etv[e] * egv[e] * *reinterpret_cast<const float*>(qk + swz(128, C + t, ch)));
-        }
-        tc::tmem_st32(tmem + T_M1 + u0 + lb, aw);
-      }
-      // ---- P8: T = (I + A)^{-1} (fp32): diagonal 16x16 blocks, then the others; each
-      //      finished block also goes (rounded) into the B-operand tile --------------
+      // ---- P4: T = (I + A)^{-1} (fp32): diagonal 16x16 blocks, then the others ----------
       if (tid < 64) {
         const int bi = tid >> 4, c = tid & 15, base = bi * 16;
         float xv[16];
@@ -556,18 +473,14 @@ __global__ void __launch_bounds__(NT, 1)
           xv[r] = r < c ? 0.f : a0 + a1;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          tm[(base + r) * LDC + base + c] = xv[r];
-          *reinterpret_cast<uint32_t*>(tb + swz(64, base + r, base + c)) = tf32_bits(xv[r]);
-        }
+        for (int r = 0; r < 16; ++r) tm[(base + r) * LDC + base + c] = xv[r];
       }
       role_sync(1, NP);
       // Off-diagonal blocks of T in two levels (T_ij = -T_ii A_ij T_jj for a 2 x 2 block
       // lower-triangular matrix): first the 16 x 16 blocks (1,0) and (3,2), then the 32 x 32
       // block T_BA = -T_BB (A_BA T_AA) with T_AA, T_BB the two 32 x 32 diagonal blocks.
-      // Thread = (row, four columns): one float4 of T per term, so each shared-memory load
-      // feeds four products.  T's upper blocks (0,1) and (2,3) hold zeros (set at the
-      // start), so the sums run over whole blocks; Y = A_BA T_AA goes to T's unused
+      // Thread = (row, four columns): one float4 of T per term.  T's blocks (0,1) and (2,3)
+      // hold zeros, so the sums run over whole blocks; Y = A_BA T_AA goes to T's unused
       // upper-right quarter.
       auto dot16 = [&](const float* arow, const float* bcol, int ldb, float4& acc) {
 #pragma unroll
@@ -585,10 +498,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       };
       auto put_t = [&](int row, int col4, const float4& acc) {  // T(row, col4..+3) = -acc
-        const float v4[4] = {-acc.x, -acc.y, -acc.z, -acc.w};
-        *reinterpret_cast<float4*>(tm + row * LDC + col4) = make_float4(v4[0], v4[1], v4[2], v4[3]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(tb + swz(64, row, col4 + i)) = tf32_bits(v4[i]);
+        *reinterpret_cast<float4*>(tm + row * LDC + col4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       };
       {
         const int pr = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
@@ -608,44 +518,78 @@ __global__ void __launch_bounds__(NT, 1)
       }
       {
         const int i = tid >> 3, c4 = (tid & 7) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        dot16(am + (32 + i) * LDC, tm + c4, LDC, acc);
-        dot16(am + (32 + i) * LDC + 16, tm + 16 * LDC + c4, LDC, acc);
-        *reinterpret_cast<float4*>(tm + i * LDC + 32 + c4) = acc;
+        if (tid < 256) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          dot16(am + (32 + i) * LDC, tm + c4, LDC, acc);
+          dot16(am + (32 + i) * LDC + 16, tm + 16 * LDC + c4, LDC, acc);
+          *reinterpret_cast<float4*>(tm + i * LDC + 32 + c4) = acc;
+        }
         role_sync(1, NP);
-        acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        dot16(tm + (32 + i) * LDC + 32, tm + 32 + c4, LDC, acc);
-        dot16(tm + (32 + i) * LDC + 48, tm + 16 * LDC + 32 + c4, LDC, acc);
-        put_t(32 + i, c4, acc);
+        if (tid < 256) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          dot16(tm + (32 + i) * LDC + 32, tm + 32 + c4, LDC, acc);
+          dot16(tm + (32 + i) * LDC + 48, tm + 16 * LDC + 32 + c4, LDC, acc);
+          put_t(32 + i, c4, acc);
+        }
         role_sync(1, NP);
       }
-      // ---- P9: W^T into the X columns of this slot (free once the chain has written out
-      //      chunk k-2's rows) and U~^T into its U columns ---------------------------------
-      if (k >= 2 && !(ok = pwait(B_EPI0 + slot, ((k - 2) >> 1) & 1))) break;
-      tc::tmem_wait_st();
+      // ---- P5: T diag(eta e^G n_k) and T diag(eta) as fp16 tiles (row t, 8 columns each) ----
+      for (int e = tid; e < C * 8; e += NP) {
+        const int t = e >> 3, g = e & 7;
+        const float4 a = *reinterpret_cast<const float4*>(tm + t * LDC + 8 * g);
+        const float4 b = *reinterpret_cast<const float4*>(tm + t * LDC + 8 * g + 4);
+        const float tv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float v1[8], v2[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int s = 8 * g + i;
+          const float tt = s <= t ? tv[i] : 0.f;  // the upper-right quarter holds scratch
+          v2[i] = tt * ETA[s];
+          v1[i] = v2[i] * EG[s] * NK[s];
+        }
+        *reinterpret_cast<uint4*>(tp + sw(t, g)) =
+            make_uint4(pack_h2(v1[0], v1[1]), pack_h2(v1[2], v1[3]), pack_h2(v1[4], v1[5]), pack_h2(v1[6], v1[7]));
+        *reinterpret_cast<uint4*>(tpp + sw(t, g)) =
+            make_uint4(pack_h2(v2[0], v2[1]), pack_h2(v2[2], v2[3]), pack_h2(v2[4], v2[5]), pack_h2(v2[6], v2[7]));
+      }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       role_sync(1, NP);
+      // ---- P6: W^T = Y_k^T T'^T into the product columns, U~^T = Y_v^T T''^T into this
+      //      slot's U columns (free: the chain finished chunk k-2) ------------------------
       if (tid == 0) {
         tc::tc_fence_after();
-        constexpr uint32_t id4 = tc::idesc_tf32(128, 64, 0, 0);
-        for (int ks = 0; ks < C / 8; ++ks) {
-          const uint64_t bd = tc::sdesc_sw128(tb_a + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-          tc::mma_tf32_ts(tmem + t_x(slot), tmem + T_M1 + ks * 8, bd, id4, ks > 0);
-          tc::mma_tf32_ts(tmem + t_u(slot), tmem + T_AV + ks * 8, bd, id4, ks > 0);
+        constexpr uint32_t id4 = tc::idesc_fp16(128, 64, 1, 0);
+        const uint64_t dyk = tc::sdesc_sw128(tc::smem_u32(yts + C * 128), 16384, 1024);
+        const uint64_t dyv = tc::sdesc_sw128(tc::smem_u32(yv), 8192, 1024);
+        const uint64_t dtp = tc::sdesc_sw128(tc::smem_u32(tp), 16, 1024);
+        const uint64_t dtpp = tc::sdesc_sw128(tc::smem_u32(tpp), 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t ao = static_cast<uint64_t>(ks * (2048 / 16)), bo = static_cast<uint64_t>(ks * 2);
+          tc::mma_bf16(tmem + T_M1, dyk + ao, dtp + bo, id4, ks > 0);
+          tc::mma_bf16(tmem + t_u(slot), dyv + ao, dtpp + bo, id4, ks > 0);
         }
         tc::mma_commit(&bars[B_MW]);
       }
-      // ---- P10: -W (rounded) replaces K in the operand tile -------------------------
+      // ---- P7: -W (fp16) into its tile, free once the chain's products of chunk k-1 that
+      //      read it are done (warps 0-7: lane = channel c, 32 tokens each) ------------------
       if (!(ok = pwait(B_MW, k & 1))) break;
+      if (k >= 1 && !(ok = pwait(B_MA, (k - 1) & 1))) break;
       tc::tc_fence_after();
-      {
+      if (warp < 8) {
+        const int ch = warp >> 2;
+        const int c = q4 * 32 + lane;
         uint32_t v32[32];
-        tc::tmem_ld32(tmem + t_x(slot) + u0 + lb, v32);
+        tc::tmem_ld32(tmem + T_M1 + ch * 32 + lb, v32);
         tc::tmem_wait_ld();
+        unsigned char* col = wt + (c >> 6) * 8192 + (c & 7) * 2;
+        const int jc = (c & 63) >> 3;
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          *reinterpret_cast<uint32_t*>(qk + swz(128, C + u0 + e, ch)) = tf32_bits(-__uint_as_float(v32[e]));
+        for (int e = 0; e < 32; ++e) {
+          const int t = ch * 32 + e;
+          *reinterpret_cast<__half*>(col + sw(t, jc)) = __float2half_rn(-__uint_as_float(v32[e]));
+        }
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
@@ -670,137 +614,213 @@ __global__ void __launch_bounds__(NT, 1)
     auto cwait = [&](int b, uint32_t par) -> bool {
       return role_and(2, NCH, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
     };
-    // S <- a state from global memory (row v), or zero
+    // 64 fp32 values -> 32 words of fp16 pairs
+    auto pack64 = [&](const uint32_t* a, const uint32_t* b, uint32_t* hv) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        hv[e] = pack_h2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+        hv[16 + e] = pack_h2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
+      }
+    };
+    // fp16 copy of S (the A operand of the chain's first products)
+    auto make_s16 = [&]() {
+#pragma unroll
+      for (int cb = 0; cb < D; cb += 64) {
+        uint32_t a[32], b[32], hv[32];
+        tc::tmem_ld32(tmem + T_S + cb + lb, a);
+        tc::tmem_ld32(tmem + T_S + cb + 32 + lb, b);
+        tc::tmem_wait_ld();
+        pack64(a, b, hv);
+        tc::tmem_st32(tmem + T_S16 + cb / 2 + lb, hv);
+      }
+    };
+    // S <- a state from global memory (row v), or zero; and its fp16 copy
     auto load_state = [&](const float* src) {
 #pragma unroll
-      for (int cb = 0; cb < D; cb += 32) {
-        uint32_t v32[32];
+      for (int cb = 0; cb < D; cb += 64) {
+        uint32_t a[32], b[32], hv[32];
         if (src) {
           const float4* s4 = reinterpret_cast<const float4*>(src + state_base + static_cast<int64_t>(v) * D + cb);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 f = s4[q];
-            v32[4 * q] = __float_as_uint(f.x);
-            v32[4 * q + 1] = __float_as_uint(f.y);
-            v32[4 * q + 2] = __float_as_uint(f.z);
-            v32[4 * q + 3] = __float_as_uint(f.w);
+            const float4 f = s4[q], g2 = s4[8 + q];
+            a[4 * q] = __float_as_uint(f.x);
+            a[4 * q + 1] = __float_as_uint(f.y);
+            a[4 * q + 2] = __float_as_uint(f.z);
+            a[4 * q + 3] = __float_as_uint(f.w);
+            b[4 * q] = __float_as_uint(g2.x);
+            b[4 * q + 1] = __float_as_uint(g2.y);
+            b[4 * q + 2] = __float_as_uint(g2.z);
+            b[4 * q + 3] = __float_as_uint(g2.w);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v32[e] = 0u;
+          for (int e = 0; e < 32; ++e) a[e] = b[e] = 0u;
         }
-        tc::tmem_st32(tmem + T_S + cb + lb, v32);
+        pack64(a, b, hv);
+        tc::tmem_st32(tmem + T_S + cb + lb, a);
+        tc::tmem_st32(tmem + T_S + cb + 32 + lb, b);
+        tc::tmem_st32(tmem + T_S16 + cb / 2 + lb, hv);
       }
       tc::tmem_wait_st();
     };
     if (!BRANCH) load_state(S0);
     bool ok = !p.stall || cwait(B_STALL, 0);  // FORK_TEST_STALL: runs out, nothing is issued
+    bool s_is_start = !BRANCH;  // branch call: S holds S_P[j] (no question has updated it)
     int si = first_seg(seg_first), c0 = 0, k = 0;
     while (ok && si < seg_end) {
       const int start = seg_start(si), len = seg_len(si), pos0 = seg_pos0(si);
       const int n = min(C, len - c0);
       const int slot = k & 1;
-      const float* G = gslot + slot * 5 * C;
-      const float* EG = G + C;
-      const bool need_state = !BRANCH || (c0 + C < len);
+      const float* G = gate(slot, G_G);
+      const float* EG = gate(slot, G_EG);
+      const float* GL = gate(slot, G_GL);
+      const float* NQ = gate(slot, G_NQ);
+      const float* NK = gate(slot, G_NK);
+      unsigned char* yts = yt(slot);
+      unsigned char* pb = pbt(slot);
+      const bool more = c0 + C < len;  // another chunk of this segment follows
+      const bool need_state = !BRANCH || more;
       // ---- C0: operands of chunk k ready; a question starts from its request's S_P ----
       if (!(ok = cwait(B_PREP, k & 1))) break;
-      if (BRANCH && c0 == 0) load_state(S0);
+      if (BRANCH && c0 == 0 && !s_is_start) {
+        load_state(S0);
+        s_is_start = true;
+      }
       tc::tc_fence_before();
       role_sync(2, NCH);
       if (ct == 0) {
         tc::tc_fence_after();
-        constexpr uint32_t ida = tc::idesc_tf32(128, 64, 0, 0);
-        const uint64_t dq = tc::sdesc_sw128(qk_a, 16, 1024), dw = tc::sdesc_sw128(qk_a + C * 128, 16, 1024);
+        constexpr uint32_t ida = tc::idesc_fp16(128, 64, 0, 0);
+        const uint64_t dw = tc::sdesc_sw128(tc::smem_u32(wt), 16, 1024);
+        const uint64_t dq = tc::sdesc_sw128(tc::smem_u32(yts), 16, 1024);
 #pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks) {
-          const uint64_t off = static_cast<uint64_t>((ks >> 2) * 1024 + (ks & 3) * 2);
-          tc::mma_tf32_ts(tmem + t_u(slot), tmem + T_S + ks * 8, dw + off, ida, 1u);  // U~^T - S W^T
-          tc::mma_tf32_ts(tmem + t_x(slot), tmem + T_S + ks * 8, dq + off, ida, ks > 0);  // S Q^T
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t ow = static_cast<uint64_t>((ks >> 2) * (8192 / 16) + (ks & 3) * 2);
+          const uint64_t oq = static_cast<uint64_t>((ks >> 2) * (16384 / 16) + (ks & 3) * 2);
+          tc::mma_f16_ts(tmem + t_u(slot), tmem + T_S16 + ks * 8, dw + ow, ida, 1u);  // U~^T - S W^T
+          tc::mma_f16_ts(tmem + T_X, tmem + T_S16 + ks * 8, dq + oq, ida, ks > 0);    // S Y_q^T
         }
         tc::mma_commit(&bars[B_MA]);
       }
-      // ---- C1: U^T to TF32, X scaled by e^G, checkpoint, S scaled by e^{G_last} ------
+      // ---- C1: checkpoint; U^T to fp16 (plain, and scaled by Gamma_last n_k); X scaled by
+      //      e^G n_q; S scaled by e^{G_last} ------------------------------------------------
       if (!(ok = cwait(B_MA, k & 1))) break;
       tc::tc_fence_after();
-      {
-        uint32_t v32[32];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          tc::tmem_ld32(tmem + t_u(slot) + q * 32 + lb, v32);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v32[e] = tf32_bits(__uint_as_float(v32[e]));
-          tc::tmem_st32(tmem + t_u(slot) + q * 32 + lb, v32);
-          tc::tmem_ld32(tmem + t_x(slot) + q * 32 + lb, v32);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v32[e] = __float_as_uint(__uint_as_float(v32[e]) * EG[q * 32 + e]);
-          tc::tmem_st32(tmem + t_x(slot) + q * 32 + lb, v32);
-        }
-      }
       if (!BRANCH && ck >= 0 && p.S_ckpt) {
         // state after r of this chunk's tokens (rare): e^{G_{r-1}} S0 + sum_{s<r}
-        // e^{G_{r-1} - G_s} u_s k_s^T, with k_s = (Gamma_last-scaled copy) / Gamma_last,s
+        // e^{G_{r-1} - G_s} n_k,s u_s y_k,s^T
         const int r_ck = ck - pos0 - c0;
         if (r_ck >= 1 && r_ck <= n) {
-          tc::tmem_wait_st();
-          uint32_t ua[32], ub[32], s32[32];
-          tc::tmem_ld32(tmem + t_u(slot) + lb, ua);
-          tc::tmem_ld32(tmem + t_u(slot) + 32 + lb, ub);
-          tc::tmem_wait_ld();
-          const float gr = G[r_ck - 1], f = expf(gr - G[C - 1]);
+          const float gr = G[r_ck - 1];
+#pragma unroll 1
           for (int cb = 0; cb < D; cb += 32) {
+            uint32_t s32[32];
             tc::tmem_ld32(tmem + T_S + cb + lb, s32);
             tc::tmem_wait_ld();
             float acc[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) acc[e] = expf(gr) * __uint_as_float(s32[e]);
+            const unsigned char* ybox = yts + (cb >> 6) * 16384;
+#pragma unroll 1
             for (int s = 0; s < r_ck; ++s) {
-              const float us = __uint_as_float(s < 32 ? ua[s & 31] : ub[s & 31]) * f;
+              const uint32_t u1 = tc::tmem_ld1(tmem + t_u(slot) + s + lb);  // u_s of row v (fp32)
+              tc::tmem_wait_ld();
+              const float us = __uint_as_float(u1) * expf(gr - G[s]) * NK[s];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) acc[e] += us * *reinterpret_cast<const float*>(kt + swz(128, cb + e, s));
+              for (int q = 0; q < 4; ++q) {
+                const uint4 w = *reinterpret_cast<const uint4*>(ybox + sw(C + s, ((cb & 63) >> 3) + q));
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                  const uint32_t wv = word_of(w, e2);
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv));
+                  acc[8 * q + 2 * e2] += us * f.x;
+                  acc[8 * q + 2 * e2 + 1] += us * f.y;
+                }
+              }
             }
 #pragma unroll
             for (int e = 0; e < 32; ++e) p.S_ckpt[state_base + static_cast<int64_t>(v) * D + cb + e] = acc[e];
           }
         }
       }
+      {
+        // columns 0-31 of the slot: U^T (s = 0..63, two per column); 32-63: U^T diag(Gamma_last n_k)
+        uint32_t ua[32], ub[32], w32[32];
+        tc::tmem_ld32(tmem + t_u(slot) + lb, ua);
+        tc::tmem_ld32(tmem + t_u(slot) + 32 + lb, ub);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          w32[e] = pack_h2(__uint_as_float(ua[2 * e]), __uint_as_float(ua[2 * e + 1]));
+          w32[16 + e] = pack_h2(__uint_as_float(ub[2 * e]), __uint_as_float(ub[2 * e + 1]));
+        }
+        tc::tmem_st32(tmem + t_u(slot) + lb, w32);
+        const float4* gl4 = reinterpret_cast<const float4*>(GL);
+        const float4* nk4 = reinterpret_cast<const float4*>(NK);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 g = gl4[q], nk = nk4[q];
+          const uint32_t* src = q < 8 ? ua + 4 * q : ub + 4 * (q - 8);
+          w32[2 * q] = pack_h2(__uint_as_float(src[0]) * g.x * nk.x, __uint_as_float(src[1]) * g.y * nk.y);
+          w32[2 * q + 1] = pack_h2(__uint_as_float(src[2]) * g.z * nk.z, __uint_as_float(src[3]) * g.w * nk.w);
+        }
+        tc::tmem_st32(tmem + t_u(slot) + 32 + lb, w32);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t v32[32];
+        tc::tmem_ld32(tmem + T_X + q * 32 + lb, v32);
+        tc::tmem_wait_ld();
+        const float4* eg4 = reinterpret_cast<const float4*>(EG + q * 32);
+        const float4* nq4 = reinterpret_cast<const float4*>(NQ + q * 32);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 g = eg4[e4], nq = nq4[e4];
+          v32[4 * e4] = __float_as_uint(__uint_as_float(v32[4 * e4]) * g.x * nq.x);
+          v32[4 * e4 + 1] = __float_as_uint(__uint_as_float(v32[4 * e4 + 1]) * g.y * nq.y);
+          v32[4 * e4 + 2] = __float_as_uint(__uint_as_float(v32[4 * e4 + 2]) * g.z * nq.z);
+          v32[4 * e4 + 3] = __float_as_uint(__uint_as_float(v32[4 * e4 + 3]) * g.w * nq.w);
+        }
+        tc::tmem_st32(tmem + T_X + q * 32 + lb, v32);
+      }
       if (need_state) {
         const float egl = EG[C - 1];
-        uint32_t v32[32];
 #pragma unroll
         for (int cb = 0; cb < D; cb += 32) {
+          uint32_t v32[32];
           tc::tmem_ld32(tmem + T_S + cb + lb, v32);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) v32[e] = __float_as_uint(__uint_as_float(v32[e]) * egl);
           tc::tmem_st32(tmem + T_S + cb + lb, v32);
         }
+        s_is_start = false;
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
       role_sync(2, NCH);
-      // ---- C2: O^T += U^T P^T and S += U^T diag(Gamma_last) K ---------------------------
+      // ---- C2: O^T += U^T P^T and S += (U^T diag(Gamma_last n_k)) Y_k --------------------
       if (ct == 0) {
         tc::tc_fence_after();
-        constexpr uint32_t id5 = tc::idesc_tf32(128, 64, 0, 0);
-        constexpr uint32_t id6 = tc::idesc_tf32(128, 128, 0, 0);
-        for (int ks = 0; ks < C / 8; ++ks)
-          tc::mma_tf32_ts(tmem + t_x(slot), tmem + t_u(slot) + ks * 8,
-                          tc::sdesc_sw128(pb_a + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id5, 1u);
+        constexpr uint32_t id5 = tc::idesc_fp16(128, 64, 0, 0);
+        constexpr uint32_t id6 = tc::idesc_fp16(128, 128, 0, 1);
+        const uint64_t dp = tc::sdesc_sw128(tc::smem_u32(pb), 16, 1024);
+        const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(yts + C * 128), 16384, 1024);
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          tc::mma_f16_ts(tmem + T_X, tmem + t_u(slot) + ks * 8, dp + static_cast<uint64_t>(ks * 2), id5, 1u);
         if (need_state)
-          for (int ks = 0; ks < C / 8; ++ks)
-            tc::mma_tf32_ts(tmem + T_S, tmem + t_u(slot) + ks * 8,
-                            tc::sdesc_sw128(kt_a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id6, 1u);
+#pragma unroll
+          for (int ks = 0; ks < C / 16; ++ks)
+            tc::mma_f16_ts(tmem + T_S, tmem + t_u(slot) + 32 + ks * 8, dk + static_cast<uint64_t>(ks * (2048 / 16)),
+                           id6, 1u);
         tc::mma_commit(&bars[B_MB]);
       }
-      // ---- C3: output rows.  Thread v holds column v of the chunk's 64 x 128 output; the
-      //      columns are staged as bf16 rows (token-major, 256 bytes each) in the K^T tile,
-      //      free now that the products of this chunk are complete, then written out as
-      //      coalesced 16-byte stores.  Lane pairs swap values so that each shared-memory
-      //      store carries two neighbouring columns of one token; odd rows are rotated by
-      //      64 bytes so that the two tokens of one store instruction use different banks.
+      // ---- C3: output rows, staged 32 tokens at a time in this slot's P tile (read by the
+      //      products just completed).  Thread v holds column v; lane pairs swap values so
+      //      that each shared-memory store carries two neighbouring columns of one token; odd
+      //      rows are rotated by 64 bytes so the two tokens of one store use different banks.
       if (!(ok = cwait(B_MB, k & 1))) break;
       tc::tc_fence_after();
       {
@@ -809,32 +829,35 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           uint32_t v32[32];
-          tc::tmem_ld32(tmem + t_x(slot) + q * 32 + lb, v32);
+          tc::tmem_ld32(tmem + T_X + q * 32 + lb, v32);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             // even lane: (token t, columns v, v+1); odd lane: (token t+1, columns v-1, v)
             const float mine_t = __uint_as_float(v32[e]), mine_t1 = __uint_as_float(v32[e + 1]);
             const float other = __shfl_xor_sync(0xffffffffu, odd ? mine_t : mine_t1, 1);
-            const int t = q * 32 + e + (odd ? 1 : 0);
-            const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine_t1) : __floats2bfloat162_rn(mine_t, other);
-            *reinterpret_cast<__nv_bfloat162*>(kt + t * (D * 2) + ((v0 * 2 + (t & 1) * 64) & (D * 2 - 1))) = pr;
+            const int t = e + (odd ? 1 : 0);
+            const __nv_bfloat162 pr =
+                odd ? __floats2bfloat162_rn(other, mine_t1) : __floats2bfloat162_rn(mine_t, other);
+            *reinterpret_cast<__nv_bfloat162*>(pb + t * (D * 2) + ((v0 * 2 + (t & 1) * 64) & (D * 2 - 1))) = pr;
           }
-        }
-      }
-      role_sync(2, NCH);
-      {
-        const int cq = ct & 15;  // 16-byte piece of a 256-byte row
+          role_sync(2, NCH);
+          const int cq = ct & 15;  // 16-byte piece of a 256-byte row
 #pragma unroll
-        for (int pass = 0; pass < C / 8; ++pass) {
-          const int t = pass * 8 + (ct >> 4);
-          if (t < n) {
-            const uint4 val = *reinterpret_cast<const uint4*>(kt + t * (D * 2) + ((cq * 16 + (t & 1) * 64) & (D * 2 - 1)));
-            *reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(start + c0 + t) * H + h) * D + cq * 8) = val;
+          for (int pass = 0; pass < 4; ++pass) {
+            const int t = pass * 8 + (ct >> 4);
+            if (q * 32 + t < n) {
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(pb + t * (D * 2) + ((cq * 16 + (t & 1) * 64) & (D * 2 - 1)));
+              *reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(start + c0 + q * 32 + t) * H + h) * D + cq * 8) =
+                  val;
+            }
           }
+          role_sync(2, NCH);
         }
       }
-      tc::mbar_arrive(&bars[B_OUT]);
+      if (more) make_s16();  // the next chunk's products read S through its fp16 copy
+      tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::mbar_arrive(&bars[B_EPI0 + slot]);
       ++k;
@@ -895,8 +918,9 @@ __global__ void __launch_bounds__(NT, 1)
 int launch_gdn_tc(const GdnParams& p, bool branch, int grid_x, cudaStream_t s) {
   alignas(128) CUtensorMap maps[3];
   const uint16_t* src[3] = {p.q, p.k, p.v};
+  // boxes of 64 channels x 1 head x HR rows, 128-byte swizzle (zero fill outside the tensor)
   for (int i = 0; i < 3; ++i)
-    if (!encode_map_3d(&maps[i], src[i], D, p.H, p.L.T_cap, D, 1, HR, false)) return FORK_ECUDA;
+    if (!encode_map_3d(&maps[i], src[i], D, p.H, p.L.T_cap, 64, 1, HR, true)) return FORK_ECUDA;
   dim3 grid(grid_x, p.H);
   if (branch) {
     if (cuda_rc(cudaFuncSetAttribute(gdn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM)) !=
