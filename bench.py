@@ -495,33 +495,28 @@ def readout_mlp_timing(torch, dr, rnd, stream, peaks, reps=20):
 
 def graph_timing(torch, args, local, wid=1):
     """Round latency of the short-request round (32 requests, 14.9k tokens): the layer's
-    calls launched one by one, and the same calls replayed from one CUDA graph."""
+    calls launched one by one, and the same round replayed from the capacity-bucket graph
+    pool (smallest bucket that holds it; the copy of the round's inputs into the bucket
+    is not timed)."""
     from tree_forked_hybrid_gb300 import workloads as wl
-    from tree_forked_hybrid_gb300.runner import DeviceRound, GraphRound
+    from tree_forked_hybrid_gb300.runner import DeviceRound, GraphPool
     rnd = wl.make_round(wid)
     dr = DeviceRound(rnd, device=f"cuda:{local}")
-    g = GraphRound(DeviceRound(rnd, device=f"cuda:{local}"))
+    pool = GraphPool(rnd.attn_shapes, rnd.gdn_shape, buckets=(4096, 8192, 16384, 32768), max_req=64, max_q=256,
+                     max_opts=2048, device=f"cuda:{local}")
+    cr, graph = pool.bucket_for(rnd)
+    cr.load(rnd)
     stream = torch.cuda.current_stream()
-
-    def timed(fn):
-        for _ in range(max(args.warmup, 3)):
-            fn()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / args.steps
-
-    eager = timed(dr.run)
-    graph = timed(g.replay)
-    if g.dr.status() != 0 or dr.status() != 0:
+    eager = latency_stats(step_times(torch, dr.run, stream, max(args.steps, 20)))
+    for _ in range(3):
+        graph.replay()
+    replay = latency_stats(step_times(torch, graph.replay, stream, max(args.steps, 20)))
+    if cr.status() != 0 or dr.status() != 0:
         raise RuntimeError("device status set")
-    return {"workload": f"short requests: R={rnd.R}, T={rnd.T}, T_cap={rnd.T_cap}", "eager_ms": eager,
-            "graph_ms": graph, "launches_per_round": dr.launches_per_round()}
+    same = bool(torch.equal(cr.p[:int(rnd.opt_off[-1])], dr.p[:int(rnd.opt_off[-1])]))
+    return {"workload": f"short requests: R={rnd.R}, T={rnd.T}, Nq={rnd.Nq}", "bucket_T_cap": cr.T_cap,
+            "eager_ms": eager, "graph_ms": replay, "launches_per_round": dr.launches_per_round(),
+            "same_probabilities": same}
 
 
 def attn_kernel_alone(torch, dr, rnd, stream, reps=10):

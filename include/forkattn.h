@@ -132,6 +132,23 @@ int fork_meta_init(fork_meta* m, void* d_buf, size_t bytes, int32_t T_cap, int32
 int fork_build_meta(const fork_meta* m, const int32_t* d_desc, int32_t R, int32_t Nq,
                     uint32_t flags, void* stream);
 
+/* Words of a fixed-capacity device descriptor for fork_build_meta_dev:
+ * 2 + 4 * max_req + max_q (0 for invalid capacities). */
+size_t fork_desc_capacity_words(int32_t max_req, int32_t max_q);
+
+/* fork_build_meta with the request and question counts read on the device, so
+ * that one captured CUDA graph serves every round up to the capacities (the
+ * onedev summary's "어떻게 쓰나": one flat graph per capacity bucket, replayed for
+ * any round that fits).
+ *   d_desc   device int32 [fork_desc_capacity_words(max_req, max_q)]:
+ *            R, Nq | max_req trunk lengths | max_req question counts | max_q
+ *            question lengths | max_req prefix lengths | max_req checkpoint
+ *            positions; entries past R (requests) or Nq (questions) are ignored.
+ * Same results as fork_build_meta on the equivalent packed descriptor.  R or
+ * Nq outside [0, max_req] / [0, max_q] sets FORK_STATUS_CAPACITY (round empty).
+ * Errors: FORK_EINVAL (null pointer, invalid handle). */
+int fork_build_meta_dev(const fork_meta* m, const int32_t* d_desc, uint32_t flags, void* stream);
+
 /* cudaError_t value of the most recent CUDA runtime call of this library that
  * failed on the calling host thread (0 if none): the detail behind FORK_ECUDA. */
 int fork_last_cuda_error(void);

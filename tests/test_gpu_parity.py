@@ -65,6 +65,23 @@ def test_meta_workloads(wid):
     check_meta_equal(rnd.desc(), rnd.R, rnd.Nq, rnd.T_cap, tile, max_req=rnd.R + 3, max_q=rnd.Nq + 5)
 
 
+@pytest.mark.parametrize("wid", [1, 3])
+def test_work_items_launch_longest_first(wid):
+    """The launch order is a permutation of the work list in non-increasing key count
+    (position after the item's last query), ties in list order."""
+    rnd = wl.make_round(wid)
+    tile = 256 // (rnd.attn_shapes[0].Hq // rnd.attn_shapes[0].Hkv)
+    got, _ = device_meta(rnd.desc(), rnd.R, rnd.Nq, rnd.T_cap, tile)
+    want = orc.meta_ref(rnd.desc(), rnd.R, rnd.Nq, rnd.T_cap, tile)
+    nw = want["work_seg"].shape[0]
+    order = got["work_order"][:nw]
+    assert sorted(order.tolist()) == list(range(nw))
+    seg, off = want["work_seg"], want["work_off"]
+    cost = want["seg_pos0"][seg] + off + np.minimum(tile, want["seg_len"][seg] - off)
+    expect = sorted(range(nw), key=lambda w: (-int(cost[w]), w))
+    assert order.tolist() == expect
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_meta_random(seed):
     rng = np.random.default_rng(100 + seed)

@@ -43,7 +43,7 @@ struct AttnParams {
 // inside the round (the prefix range is checked against the prefix buffers separately).
 __device__ __forceinline__ bool attn_item_in_bounds(const int32_t* meta, const MetaLayout& L, int w) {
   const int T = meta[H_T], nseg = meta[H_NSEG], R = meta[H_R];
-  if (meta[H_NWORK] > L.max_work) return false;
+  if (meta[H_NWORK] > L.max_work || w < 0 || w >= meta[H_NWORK]) return false;
   const int s = meta[L.work_seg + w];
   if (s < 0 || s >= nseg || s >= L.max_seg) return false;
   const int st = meta[L.seg_start + s], len = meta[L.seg_len + s], off = meta[L.work_off + w];

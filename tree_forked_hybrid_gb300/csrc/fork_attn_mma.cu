@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const AttnParams 
   const int32_t* meta = p.meta;
   const MetaLayout& L = p.L;
   if (meta[H_VALID] == 0) return;
-  const int w = blockIdx.x;
-  if (w >= meta[H_NWORK]) return;
+  if (static_cast<int>(blockIdx.x) >= meta[H_NWORK]) return;
+  const int w = meta[L.work_order + blockIdx.x];  // longest items first
   const int g = blockIdx.y;  // kv head
   const int G = p.G;
   const int tile = kRows / G;

@@ -31,6 +31,8 @@
 // Operands are bf16, accumulation f32 in TMEM.  Every wait is bounded; on a
 // timeout the CTA raises the status bit, drains its own copies and MMAs,
 // frees TMEM and exits.
+#include <cuda_fp16.h>
+
 #include "fork_attn.cuh"
 #include "tc_ptx.cuh"
 
@@ -66,11 +68,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 2^x on the SFU (flush-to-zero; 2^-inf = 0)
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+// 2^a, 2^b of two scores on the SFU in one half-precision pair operation (2^-inf = 0).
+// The arguments are at most 2^8 (the running maximum lags by at most that) and P is
+// rounded to bf16 afterwards, so the half-precision argument and result lose nothing
+// that the bf16 P keeps; returns the pair in fp32.
+__device__ __forceinline__ float2 exp2_pair(float a, float b) {
+  const __half2 x = __floats2half2_rn(a, b);
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(*reinterpret_cast<const uint32_t*>(&x)));
+  return __half22float2(*reinterpret_cast<const __half2*>(&y));
+}
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // tcgen05.mma kind::f16 with A (bf16, 2 per 32-bit column) read from TMEM
@@ -150,8 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* meta = p.meta;
   const MetaLayout& L = p.L;
   if (meta[H_VALID] == 0) return;
-  const int w = blockIdx.x;
-  if (w >= meta[H_NWORK]) return;
+  if (static_cast<int>(blockIdx.x) >= meta[H_NWORK]) return;
+  const int w = meta[L.work_order + blockIdx.x];  // longest items first
   const int g = blockIdx.y;
   const int G = p.G;
   const int tile = kRows / G;  // tokens per MMA tile
@@ -467,14 +479,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cc = 0; cc < kKeys; ++cc)
             if (cc >= lim_len || cc > lim_causal || cc <= lim_win) sv[cc] = -INFINITY;
         }
-        // row maximum (raw scores; the scale is positive)
+        // row maximum (raw scores; the scale is positive): 8 independent chains of
+        // three-input maxima
         float mx[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx[e] = sv[e];
 #pragma unroll
-        for (int cc = 8; cc < kKeys; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], sv[cc]);
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        for (int cc = 8; cc < kKeys - 8; cc += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = max3(mx[e], sv[cc + e], sv[cc + 8 + e]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[kKeys - 8 + e]);
+        const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
         const bool resc = mt > m_used + kRescale;
         const float m_new = resc ? mt : m_used;
         const float base = (m_new == -INFINITY) ? 0.f : m_new;
@@ -490,11 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int cc = h2 * 32 + 2 * e;
-            const float a = fast_exp2(fmaf(sv[cc], sl2, -base));
-            const float b = fast_exp2(fmaf(sv[cc + 1], sl2, -base));
-            ps[(2 * e) & 7] += a;
-            ps[(2 * e + 1) & 7] += b;
-            pk[e] = pack_bf16(a, b);
+            const float2 ab = exp2_pair(fmaf(sv[cc], sl2, -base), fmaf(sv[cc + 1], sl2, -base));
+            ps[(2 * e) & 7] += ab.x;
+            ps[(2 * e + 1) & 7] += ab.y;
+            pk[e] = pack_bf16(ab.x, ab.y);
           }
           tc::tmem_st16(ts + h2 * 16, pk);
         }

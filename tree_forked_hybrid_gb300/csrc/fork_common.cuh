@@ -29,7 +29,7 @@ struct MetaLayout {
   int64_t req_trunk_len, req_prefix_len, req_prefix_off, req_ckpt_pos, req_trunk_start,
       req_first_q, req_n_q;
   int64_t q_last;
-  int64_t work_seg, work_off;
+  int64_t work_seg, work_off, work_order;
   int64_t total;
 };
 
@@ -65,6 +65,7 @@ __host__ __device__ inline MetaLayout meta_layout(int32_t T_cap, int32_t max_req
   L.q_last = take(max_q > 0 ? max_q : 1);
   L.work_seg = take(L.max_work);
   L.work_off = take(L.max_work);
+  L.work_order = take(L.max_work);
   L.total = o;
   return L;
 }

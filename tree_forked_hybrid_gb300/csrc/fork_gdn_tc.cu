@@ -19,8 +19,9 @@
 // (call 2) x one head; d = 128.  16 warps:
 //   warps 0-11  prep of chunk k+1 (everything above the line "U = ..."):
 //               raw q/k/v rows by TMA (the chunk and the three rows before it, 128-byte
-//               swizzled), thread = (stream, channel half, token): causal conv + SiLU of
-//               64 channels, fp16 rows into the operand tiles, partial sums of squares;
+//               swizzled), thread = (stream, 8 channels, 8 tokens): causal conv + SiLU
+//               with the weights in registers, fp16 rows into the operand tiles, the
+//               L2 norms from sums of squares reduced over a half warp;
 //               gates; [Y_q; Y_k] Y_k^T on the tensor cores -> P (fp16) and A (fp32);
 //               T = (I + A)^{-1} in fp32 (16x16 diagonal blocks by forward substitution,
 //               the rest in two levels); T diag(eta e^G n_k) and T diag(eta) as fp16
@@ -70,9 +71,7 @@ struct Lay {
   static constexpr int TPP = TP + 8192;           // T diag(eta)         [64][128 B]
   static constexpr int AM = TPP + 8192;           // A fp32 [64][LDC]
   static constexpr int TM = AM + C * LDC * 4;     // T fp32 [64][LDC]
-  static constexpr int XS = TM + C * LDC * 4;     // inverse scratch [3*256]
-  static constexpr int SS = XS + 3 * 256 * 4;     // partial sums of squares [2 halves][128 rows]
-  static constexpr int GA = SS + 2 * 128 * 4;     // raw alpha, eta of the next chunk [2][64]
+  static constexpr int GA = TM + C * LDC * 4;     // raw alpha, eta of the next chunk [2][64]
   static constexpr int GS = GA + 2 * C * 4;       // per slot [G, EG, GL, ETA, IG, NQ, NK][64]
   static constexpr int SEG = GS + 2 * 7 * C * 4;  // this CTA's segments: start, len, pos0
   static constexpr int BAR = SEG + 64;
@@ -86,18 +85,18 @@ static_assert(Lay::YT % 1024 == 0 && Lay::YV % 1024 == 0 && Lay::WT % 1024 == 0 
               "128-byte-swizzled tiles start on 1024-byte boundaries");
 static_assert(HR * 128 <= Lay::RAWH, "raw rows");
 
-enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_FINP, B_FINC, B_STALL, B_N };
+enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_GATE, B_MA, B_MB, B_EPI0, B_EPI1, B_FINP, B_FINC, B_STALL, B_N };
 enum { G_G = 0, G_EG, G_GL, G_ETA, G_IG, G_NQ, G_NK };
 
-// SFU approximations (relative error ~2^-22): 2^x, 1/x, 1/sqrt(x)
+// SFU approximations: 2^x, 1/sqrt(x) (relative error ~2^-22), tanh (~2^-11)
+__device__ __forceinline__ float tanhf_(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float rcpf(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 __device__ __forceinline__ float rsqrtf_(float x) {
@@ -106,8 +105,13 @@ __device__ __forceinline__ float rsqrtf_(float x) {
   return y;
 }
 constexpr float kLog2e = 1.4426950408889634f;
-// SiLU(y) = y / (1 + e^-y)
-__device__ __forceinline__ float silu(float y) { return y * rcpf(1.f + ex2f(-y * kLog2e)); }
+// SiLU(y) = y sigmoid(y) = y/2 + (y/2) tanh(y/2): one SFU operation.  The tanh error is
+// relative to tanh(y/2), so the result keeps ~2^-11 relative precision wherever the conv
+// outputs live (|y| of a few units), the precision of the fp16 operand it becomes.
+__device__ __forceinline__ float silu(float y) {
+  const float h = 0.5f * y;
+  return fmaf(h, tanhf_(h), h);
+}
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
@@ -207,8 +211,6 @@ __global__ void __launch_bounds__(NT, 1)
   unsigned char* tpp = sm + Lay::TPP;
   float* am = reinterpret_cast<float*>(sm + Lay::AM);
   float* tm = reinterpret_cast<float*>(sm + Lay::TM);
-  float* xs = reinterpret_cast<float*>(sm + Lay::XS);
-  float* ssq = reinterpret_cast<float*>(sm + Lay::SS);
   float* ga = reinterpret_cast<float*>(sm + Lay::GA);
   float* ge = ga + C;
   int* segt = reinterpret_cast<int*>(sm + Lay::SEG);  // [kQG][3], read instead of the metadata
@@ -221,7 +223,8 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (tid == 0) {
     // B_STALL is completed by nothing (FORK_TEST_STALL)
-    for (int b = 0; b < B_N; ++b) tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1) ? NCH : 1);
+    for (int b = 0; b < B_N; ++b)
+      tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1) ? NCH : (b == B_GATE ? 32 : 1));
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -258,15 +261,15 @@ __global__ void __launch_bounds__(NT, 1)
     auto pwait = [&](int b, uint32_t par) -> bool {
       return role_and(1, NP, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
     };
-    // conv mapping: stream st, channel half hf, token u (one row of 64 channels)
-    const int st = tid >> 7, hf = (tid >> 6) & 1, u = tid & 63;
-    const float4* wrow =
-        reinterpret_cast<const float4*>(p.conv_w) + ((static_cast<int64_t>(st) * H + h) * D + hf * 64);
+    // conv mapping: stream st, 8-channel group cg (channels 8cg..8cg+7), block of 8 tokens
+    // tb; the 16 lanes of a half warp hold the 128 channels of the same 8 tokens
+    const int st = tid >> 7, cg = tid & 15, tb = (tid >> 4) & 7;
+    const float4* cw4 = reinterpret_cast<const float4*>(p.conv_w) + ((static_cast<int64_t>(st) * H + h) * D + 8 * cg);
     const CUtensorMap* maps[3] = {&qmap, &kmap, &vmap};
     int raw_issued = 0;
     auto issue_loads = [&](int s, int cc) {
       const int st0 = seg_start(s), ln = seg_len(s);
-      if (tid == 0) {
+      if (tid == 32) {  // (thread 0 issues the products meanwhile)
         tc::fence_proxy_async_smem();  // the rows were last read (and patched) by threads
         tc::mbar_expect_tx(&bars[B_RAW], 6 * HR * 128);
 #pragma unroll
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       asm volatile("cp.async.commit_group;\n" ::);
     };
-    if (tid == 0) {
+    if (tid == 32) {
       tc::prefetch_tmap(&qmap);
       tc::prefetch_tmap(&kmap);
       tc::prefetch_tmap(&vmap);
@@ -353,38 +356,66 @@ __global__ void __launch_bounds__(NT, 1)
         ETA[a1] = a1 < n ? ge[a1] : 0.f;
         IG[a0] = __expf(-g0);  // used only when no G of the chunk is below -80 (no overflow)
         IG[a1] = __expf(-g1);
+        tc::mbar_arrive(&bars[B_GATE]);  // the chain scales S by this chunk's decay early
       }
-      //      conv + SiLU: thread = (stream, channel half, token u); 8 groups of 8 channels,
-      //      raw rows u..u+3 (positions u-3..u), fp16 row into its operand tile, sum of squares
+      //      conv + SiLU: thread = (stream, 8 channels, 8 tokens), a sliding window of raw
+      //      rows (positions u-3..u for token u); fp16 rows into the operand tiles; the
+      //      norms n_q, n_k from sums of squares over the 16 lanes of a token block
       {
-        const unsigned char* rb = raw + (st * 2 + hf) * Lay::RAWH;
-        unsigned char* dst = st == 2 ? yv + hf * 8192 : yts + hf * 16384;
-        const int drow = st == 1 ? C + u : u;
-        const bool valid = u < n;
-        float sq = 0.f;
-#pragma unroll 2
-        for (int g = 0; g < 8; ++g) {
-          uint4 xr[KW];
+        const unsigned char* rb = raw + (st * 2 + (cg >> 3)) * Lay::RAWH;
+        const int jc = cg & 7;
+        unsigned char* dst = st == 2 ? yv + (cg >> 3) * 8192 : yts + (cg >> 3) * 16384;
+        const int u0 = tb * 8;
+        float cw[8][KW];  // the group's conv weights (8 channels x 4 taps), L1-resident
 #pragma unroll
-          for (int i = 0; i < KW; ++i) xr[i] = *reinterpret_cast<const uint4*>(rb + sw(u + i, g));
+        for (int e = 0; e < 8; ++e) {
+          const float4 w = __ldg(cw4 + e);
+          cw[e][0] = w.x;
+          cw[e][1] = w.y;
+          cw[e][2] = w.z;
+          cw[e][3] = w.w;
+        }
+        uint4 xw[KW];
+#pragma unroll
+        for (int i = 0; i < KW - 1; ++i) xw[i + 1] = *reinterpret_cast<const uint4*>(rb + sw(u0 + i, jc));
+        float ssum[8];
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu) {
+          const int u = u0 + uu;
+#pragma unroll
+          for (int i = 0; i < KW - 1; ++i) xw[i] = xw[i + 1];
+          xw[KW - 1] = *reinterpret_cast<const uint4*>(rb + sw(u + KW - 1, jc));  // position u
           float y[8];
+          float sq = 0.f;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float4 w = __ldg(wrow + g * 8 + e);  // taps 0..3 of channel hf*64 + 8g + e
-            const float wv[KW] = {w.x, w.y, w.z, w.w};
             float a = 0.f;
 #pragma unroll
             for (int i = 0; i < KW; ++i) {
-              const uint32_t word = word_of(xr[i], e >> 1);
-              a = fmaf(wv[i], (e & 1) ? bf_hi(word) : bf_lo(word), a);
+              const uint32_t word = word_of(xw[i], e >> 1);
+              a = fmaf(cw[e][i], (e & 1) ? bf_hi(word) : bf_lo(word), a);
             }
-            y[e] = valid ? silu(a) : 0.f;
+            y[e] = u < n ? silu(a) : 0.f;
             sq = fmaf(y[e], y[e], sq);
           }
-          *reinterpret_cast<uint4*>(dst + sw(drow, g)) =
+          ssum[uu] = sq;
+          *reinterpret_cast<uint4*>(dst + sw(st == 1 ? C + u : u, jc)) =
               make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
         }
-        if (st < 2) ssq[hf * 128 + st * C + u] = sq;
+        if (st < 2) {
+#pragma unroll
+          for (int uu = 0; uu < 8; ++uu) {
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) ssum[uu] += __shfl_xor_sync(0xffffffffu, ssum[uu], o);
+          }
+          if (cg < 8) {
+            float sv = ssum[0];
+#pragma unroll
+            for (int uu = 1; uu < 8; ++uu)
+              if (cg == uu) sv = ssum[uu];
+            (st == 0 ? NQ : NK)[u0 + cg] = rsqrtf_(sv + 1e-6f);
+          }
+        }
       }
       tc::fence_proxy_async_smem();
       role_sync(1, NP);
@@ -402,10 +433,6 @@ __global__ void __launch_bounds__(NT, 1)
           tc::mma_bf16(tmem + T_M1, da + off, db + off, id1, ks > 0);
         }
         tc::mma_commit(&bars[B_M1]);
-      }
-      if (tid < 2 * C) {
-        const float nv = rsqrtf_(ssq[tid] + ssq[128 + tid] + 1e-6f);
-        if (tid < C) NQ[tid] = nv; else NK[tid - C] = nv;
       }
       role_sync(1, NP);
       // ---- P3: P (q rows) and A (k rows) from [Y_q; Y_k] Y_k^T, warps 0-7 ---------------
@@ -479,57 +506,72 @@ __global__ void __launch_bounds__(NT, 1)
       // Off-diagonal blocks of T in two levels (T_ij = -T_ii A_ij T_jj for a 2 x 2 block
       // lower-triangular matrix): first the 16 x 16 blocks (1,0) and (3,2), then the 32 x 32
       // block T_BA = -T_BB (A_BA T_AA) with T_AA, T_BB the two 32 x 32 diagonal blocks.
-      // Thread = (row, four columns): one float4 of T per term.  T's blocks (0,1) and (2,3)
-      // hold zeros, so the sums run over whole blocks; Y = A_BA T_AA goes to T's unused
-      // upper-right quarter.
-      auto dot16 = [&](const float* arow, const float* bcol, int ldb, float4& acc) {
+      // T's blocks (0,1) and (2,3) hold zeros, so the sums run over whole blocks; Y = A_BA T_AA
+      // goes to T's unused upper-right quarter.  Each thread keeps a block of rows x 4 columns
+      // in registers, so every value read from shared memory feeds several products.
+      // rows[i] (+)= sum_k X[r_i][k] * Z[k][c4..c4+3], X and Z row-major with stride ld
+      auto blk = [&](float4* acc, int nr, const float* x0, const float* z0, int kn) {
+#pragma unroll 2
+        for (int k4 = 0; k4 < kn; k4 += 4) {
+          float4 xv[4];
 #pragma unroll
-        for (int m4 = 0; m4 < 16; m4 += 4) {
-          const float4 a = *reinterpret_cast<const float4*>(arow + m4);
-          const float av4[4] = {a.x, a.y, a.z, a.w};
+          for (int i = 0; i < 4; ++i)
+            if (i < nr) xv[i] = *reinterpret_cast<const float4*>(x0 + i * LDC + k4);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 t4 = *reinterpret_cast<const float4*>(bcol + (m4 + i) * ldb);
-            acc.x += av4[i] * t4.x;
-            acc.y += av4[i] * t4.y;
-            acc.z += av4[i] * t4.z;
-            acc.w += av4[i] * t4.w;
+          for (int kk = 0; kk < 4; ++kk) {
+            const float4 z = *reinterpret_cast<const float4*>(z0 + (k4 + kk) * LDC);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (i < nr) {
+                const float xs_ = kk == 0 ? xv[i].x : kk == 1 ? xv[i].y : kk == 2 ? xv[i].z : xv[i].w;
+                acc[i].x = fmaf(xs_, z.x, acc[i].x);
+                acc[i].y = fmaf(xs_, z.y, acc[i].y);
+                acc[i].z = fmaf(xs_, z.z, acc[i].z);
+                acc[i].w = fmaf(xs_, z.w, acc[i].w);
+              }
+            }
           }
         }
       };
-      auto put_t = [&](int row, int col4, const float4& acc) {  // T(row, col4..+3) = -acc
-        *reinterpret_cast<float4*>(tm + row * LDC + col4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-      };
       {
-        const int pr = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        // level 1: 64 threads, product pr in {0, 1} -> blocks (2pr+1, 2pr); rows 2rp, 2rp+1
+        const int pr = tid >> 5, rp = (tid >> 2) & 7, c4 = (tid & 3) * 4;
         const int bi = 2 * pr + 1, bj = 2 * pr;
-        if (tid < 128) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          dot16(am + (bi * 16 + r) * LDC + bj * 16, tm + (bj * 16) * LDC + bj * 16 + c4, LDC, acc);
-          *reinterpret_cast<float4*>(xs + (pr << 8) + r * 16 + c4) = acc;
+        float* yb = tm + 32 + pr * 16;  // Y = A_ij T_jj [16][16] in T's upper-right quarter (free)
+        if (tid < 64) {
+          float4 acc[4] = {};
+          blk(acc, 2, am + (bi * 16 + 2 * rp) * LDC + bj * 16, tm + (bj * 16) * LDC + bj * 16 + c4, 16);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) *reinterpret_cast<float4*>(yb + (2 * rp + i) * LDC + c4) = acc[i];
         }
         role_sync(1, NP);
-        if (tid < 128) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          dot16(tm + (bi * 16 + r) * LDC + bi * 16, xs + (pr << 8) + c4, 16, acc);
-          put_t(bi * 16 + r, bj * 16 + c4, acc);
+        if (tid < 64) {
+          float4 acc[4] = {};
+          blk(acc, 2, tm + (bi * 16 + 2 * rp) * LDC + bi * 16, yb + c4, 16);
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<float4*>(tm + (bi * 16 + 2 * rp + i) * LDC + bj * 16 + c4) =
+                make_float4(-acc[i].x, -acc[i].y, -acc[i].z, -acc[i].w);
         }
         role_sync(1, NP);
       }
       {
-        const int i = tid >> 3, c4 = (tid & 7) * 4;
-        if (tid < 256) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          dot16(am + (32 + i) * LDC, tm + c4, LDC, acc);
-          dot16(am + (32 + i) * LDC + 16, tm + 16 * LDC + c4, LDC, acc);
-          *reinterpret_cast<float4*>(tm + i * LDC + 32 + c4) = acc;
+        // level 2: 64 threads, rows 4rq..4rq+3 x columns c4..c4+3 of the 32 x 32 blocks
+        const int rq = tid >> 3, c4 = (tid & 7) * 4;
+        if (tid < 64) {
+          float4 acc[4] = {};
+          blk(acc, 4, am + (32 + 4 * rq) * LDC, tm + c4, 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(tm + (4 * rq + i) * LDC + 32 + c4) = acc[i];
         }
         role_sync(1, NP);
-        if (tid < 256) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          dot16(tm + (32 + i) * LDC + 32, tm + 32 + c4, LDC, acc);
-          dot16(tm + (32 + i) * LDC + 48, tm + 16 * LDC + 32 + c4, LDC, acc);
-          put_t(32 + i, c4, acc);
+        if (tid < 64) {
+          float4 acc[4] = {};
+          blk(acc, 4, tm + (32 + 4 * rq) * LDC + 32, tm + 32 + c4, 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4*>(tm + (32 + 4 * rq + i) * LDC + c4) =
+                make_float4(-acc[i].x, -acc[i].y, -acc[i].z, -acc[i].w);
         }
         role_sync(1, NP);
       }
@@ -604,8 +646,8 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0) {
       tc::mma_commit(&bars[B_FINP]);
       tc::mbar_drain(&bars[B_FINP], 0);
-      if (!ok && raw_issued > 0) tc::mbar_drain(&bars[B_RAW], (raw_issued - 1) & 1);
     }
+    if (tid == 32 && !ok && raw_issued > 0) tc::mbar_drain(&bars[B_RAW], (raw_issued - 1) & 1);
     asm volatile("cp.async.wait_group 0;\n" ::);
   } else {
     // ============================ state chain (128 threads) ============================
@@ -622,8 +664,9 @@ __global__ void __launch_bounds__(NT, 1)
         hv[16 + e] = pack_h2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
       }
     };
-    // fp16 copy of S (the A operand of the chain's first products)
-    auto make_s16 = [&]() {
+    // fp16 copy of S (the A operand of the next chunk's first products) and S scaled in
+    // place by that chunk's decay e^{G_last} (before its state update), in one pass
+    auto s16_and_scale = [&](float egl) {
 #pragma unroll
       for (int cb = 0; cb < D; cb += 64) {
         uint32_t a[32], b[32], hv[32];
@@ -632,6 +675,13 @@ __global__ void __launch_bounds__(NT, 1)
         tc::tmem_wait_ld();
         pack64(a, b, hv);
         tc::tmem_st32(tmem + T_S16 + cb / 2 + lb, hv);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          a[e] = __float_as_uint(__uint_as_float(a[e]) * egl);
+          b[e] = __float_as_uint(__uint_as_float(b[e]) * egl);
+        }
+        tc::tmem_st32(tmem + T_S + cb + lb, a);
+        tc::tmem_st32(tmem + T_S + cb + 32 + lb, b);
       }
     };
     // S <- a state from global memory (row v), or zero; and its fp16 copy
@@ -678,7 +728,6 @@ __global__ void __launch_bounds__(NT, 1)
       const float* NQ = gate(slot, G_NQ);
       const float* NK = gate(slot, G_NK);
       unsigned char* yts = yt(slot);
-      unsigned char* pb = pbt(slot);
       const bool more = c0 + C < len;  // another chunk of this segment follows
       const bool need_state = !BRANCH || more;
       // ---- C0: operands of chunk k ready; a question starts from its request's S_P ----
@@ -712,7 +761,8 @@ __global__ void __launch_bounds__(NT, 1)
         // e^{G_{r-1} - G_s} n_k,s u_s y_k,s^T
         const int r_ck = ck - pos0 - c0;
         if (r_ck >= 1 && r_ck <= n) {
-          const float gr = G[r_ck - 1];
+          // S holds S0, or S0 e^{G_last} when the previous chunk already scaled it
+          const float gr = G[r_ck - 1], s_fac = expf(c0 == 0 ? gr : gr - G[C - 1]);
 #pragma unroll 1
           for (int cb = 0; cb < D; cb += 32) {
             uint32_t s32[32];
@@ -720,7 +770,7 @@ __global__ void __launch_bounds__(NT, 1)
             tc::tmem_wait_ld();
             float acc[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = expf(gr) * __uint_as_float(s32[e]);
+            for (int e = 0; e < 32; ++e) acc[e] = s_fac * __uint_as_float(s32[e]);
             const unsigned char* ybox = yts + (cb >> 6) * 16384;
 #pragma unroll 1
             for (int s = 0; s < r_ck; ++s) {
@@ -784,7 +834,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc::tmem_st32(tmem + T_X + q * 32 + lb, v32);
       }
-      if (need_state) {
+      if (need_state && c0 == 0) {  // later chunks of the segment: scaled at the end of the one before
         const float egl = EG[C - 1];
 #pragma unroll
         for (int cb = 0; cb < D; cb += 32) {
@@ -805,7 +855,7 @@ __global__ void __launch_bounds__(NT, 1)
         tc::tc_fence_after();
         constexpr uint32_t id5 = tc::idesc_fp16(128, 64, 0, 0);
         constexpr uint32_t id6 = tc::idesc_fp16(128, 128, 0, 1);
-        const uint64_t dp = tc::sdesc_sw128(tc::smem_u32(pb), 16, 1024);
+        const uint64_t dp = tc::sdesc_sw128(tc::smem_u32(pbt(slot)), 16, 1024);
         const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(yts + C * 128), 16384, 1024);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks)
@@ -817,10 +867,10 @@ __global__ void __launch_bounds__(NT, 1)
                            id6, 1u);
         tc::mma_commit(&bars[B_MB]);
       }
-      // ---- C3: output rows, staged 32 tokens at a time in this slot's P tile (read by the
-      //      products just completed).  Thread v holds column v; lane pairs swap values so
-      //      that each shared-memory store carries two neighbouring columns of one token; odd
-      //      rows are rotated by 64 bytes so the two tokens of one store use different banks.
+      // ---- C3: output rows.  Thread v holds column v of the chunk's 64 x 128 output; lane
+      //      pairs swap values so that each store carries two neighbouring columns of one
+      //      token (the even lane token t, the odd lane token t+1): a warp writes two
+      //      64-byte row pieces per store.
       if (!(ok = cwait(B_MB, k & 1))) break;
       tc::tc_fence_after();
       {
@@ -833,30 +883,20 @@ __global__ void __launch_bounds__(NT, 1)
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            // even lane: (token t, columns v, v+1); odd lane: (token t+1, columns v-1, v)
             const float mine_t = __uint_as_float(v32[e]), mine_t1 = __uint_as_float(v32[e + 1]);
             const float other = __shfl_xor_sync(0xffffffffu, odd ? mine_t : mine_t1, 1);
-            const int t = e + (odd ? 1 : 0);
+            const int t = q * 32 + e + (odd ? 1 : 0);
             const __nv_bfloat162 pr =
                 odd ? __floats2bfloat162_rn(other, mine_t1) : __floats2bfloat162_rn(mine_t, other);
-            *reinterpret_cast<__nv_bfloat162*>(pb + t * (D * 2) + ((v0 * 2 + (t & 1) * 64) & (D * 2 - 1))) = pr;
+            if (t < n)
+              *reinterpret_cast<__nv_bfloat162*>(p.o + (static_cast<int64_t>(start + c0 + t) * H + h) * D + v0) = pr;
           }
-          role_sync(2, NCH);
-          const int cq = ct & 15;  // 16-byte piece of a 256-byte row
-#pragma unroll
-          for (int pass = 0; pass < 4; ++pass) {
-            const int t = pass * 8 + (ct >> 4);
-            if (q * 32 + t < n) {
-              const uint4 val =
-                  *reinterpret_cast<const uint4*>(pb + t * (D * 2) + ((cq * 16 + (t & 1) * 64) & (D * 2 - 1)));
-              *reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(start + c0 + q * 32 + t) * H + h) * D + cq * 8) =
-                  val;
-            }
-          }
-          role_sync(2, NCH);
         }
       }
-      if (more) make_s16();  // the next chunk's products read S through its fp16 copy
+      if (more) {  // the next chunk of this segment: its decay is known once its gates are
+        if (!(ok = cwait(B_GATE, (k + 1) & 1))) break;
+        s16_and_scale(gate(slot ^ 1, G_EG)[C - 1]);
+      }
       tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::mbar_arrive(&bars[B_EPI0 + slot]);

@@ -14,6 +14,7 @@
 namespace fork {
 
 static thread_local int t_last_cuda_error = 0;
+constexpr int kSortMax = 4096;  // work lists up to this length are launched longest first
 
 int cuda_rc(cudaError_t e) {
   if (e == cudaSuccess) return FORK_OK;
@@ -97,17 +98,35 @@ __device__ long long block_scan(int n, F val, G store) {
 }
 
 // One block: validation, request and segment tables, question rows, work list.
+// dev_counts = 0: desc = [R P | R n | Nq q_len | R prefix | R ckpt] with R, Nq given;
+// dev_counts = 1: desc = [R, Nq | max_req P | max_req n | max_q q_len | max_req prefix |
+// max_req ckpt], the counts read here (nothing on the host depends on them).
 __global__ void __launch_bounds__(1024) meta_tables_kernel(const int32_t* __restrict__ desc, int R,
-                                                           int Nq, int32_t* __restrict__ meta,
+                                                           int Nq, int dev_counts, int32_t* __restrict__ meta,
                                                            MetaLayout L, int tile) {
-  const int32_t* P = desc;
-  const int32_t* n = desc + R;
-  const int32_t* ql = desc + 2 * R;
-  const int32_t* pl = desc + 2 * R + Nq;
-  const int32_t* ck = desc + 3 * R + Nq;
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
+  const int32_t *P, *n, *ql, *pl, *ck;
+  int over = 0;
+  if (dev_counts) {
+    R = desc[0];
+    Nq = desc[1];
+    over = (R < 0 || R > L.max_req || Nq < 0 || Nq > L.max_q) ? 1 : 0;
+    if (over) R = Nq = 0;
+    P = desc + 2;
+    n = P + L.max_req;
+    ql = n + L.max_req;
+    pl = ql + L.max_q;
+    ck = pl + L.max_req;
+  } else {
+    P = desc;
+    n = desc + R;
+    ql = desc + 2 * R;
+    pl = desc + 2 * R + Nq;
+    ck = desc + 3 * R + Nq;
+  }
   __syncthreads();
+  if (over && threadIdx.x == 0) s_bad = FORK_STATUS_CAPACITY;
 
   // ---- validation --------------------------------------------------------
   int bad = 0;
@@ -220,6 +239,51 @@ __global__ void __launch_bounds__(1024) meta_tables_kernel(const int32_t* __rest
                                  }
                                });
   if (threadIdx.x == 0) meta[H_NWORK] = static_cast<int32_t>(nwork);
+  __syncthreads();
+
+  // ---- launch order: longest first ------------------------------------------
+  // A work item's cost is its number of visible keys under full attention (the
+  // position after its last query); items are launched in non-increasing cost,
+  // ties in list order, so the long items start first and short ones fill the
+  // tail.  Each item's result does not depend on the order.
+  int32_t* order = meta + L.work_order;
+  const int nw = static_cast<int>(nwork);
+  __shared__ unsigned long long keys[kSortMax];
+  if (nw > kSortMax) {
+    for (int w = threadIdx.x; w < nw; w += blockDim.x) order[w] = w;
+    return;
+  }
+  int np2 = 1;
+  while (np2 < nw) np2 <<= 1;
+  for (int w = threadIdx.x; w < np2; w += blockDim.x) {
+    unsigned long long key = 0ull;
+    if (w < nw) {
+      const int s = work_seg[w], off = work_off[w];
+      const int cost = meta[L.seg_pos0 + s] + off + min(tile, seg_len[s] - off);
+      key = (static_cast<unsigned long long>(cost) << 32) | (0xFFFFFFFFu - static_cast<unsigned>(w));
+    }
+    keys[w] = key;
+  }
+  __syncthreads();
+  // bitonic sort, descending
+  for (int size = 2; size <= np2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < np2; i += blockDim.x) {
+        const int jx = i ^ stride;
+        if (jx > i) {
+          const bool desc = (i & size) == 0;
+          const unsigned long long a = keys[i], b = keys[jx];
+          if (desc ? (a < b) : (a > b)) {
+            keys[i] = b;
+            keys[jx] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int w = threadIdx.x; w < nw; w += blockDim.x)
+    order[w] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<unsigned>(keys[w] & 0xFFFFFFFFull));
 }
 
 // Per-token arrays: block b < nseg writes segment b's tokens; the last block
@@ -271,8 +335,9 @@ __global__ void __launch_bounds__(1024) meta_check_kernel(int32_t* __restrict__ 
     }
     if (nseg > 0 && meta[L.seg_start] != 0) bad = 1;
     for (int w = threadIdx.x; w < nwork; w += blockDim.x) {
-      const int s = meta[L.work_seg + w], off = meta[L.work_off + w];
+      const int s = meta[L.work_seg + w], off = meta[L.work_off + w], o = meta[L.work_order + w];
       if (s < 0 || s >= nseg || off < 0 || off % tile != 0 || off >= meta[L.seg_len + s]) bad = 1;
+      if (o < 0 || o >= nwork) bad = 1;
     }
     for (int x = threadIdx.x; x < L.T_cap; x += blockDim.x) {
       const int j = meta[L.tok_req + x], c = meta[L.tok_branch + x], t = meta[L.tok_pos + x];
@@ -323,7 +388,26 @@ extern "C" int fork_build_meta(const fork_meta* m, const int32_t* d_desc, int32_
   if ((rc = check_device()) != FORK_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* meta = static_cast<int32_t*>(m->d_buf);
-  meta_tables_kernel<<<1, 1024, 0, s>>>(d_desc, R, Nq, meta, L, m->tile_tokens);
+  meta_tables_kernel<<<1, 1024, 0, s>>>(d_desc, R, Nq, 0, meta, L, m->tile_tokens);
+  meta_tokens_kernel<<<L.max_seg + 1, 256, 0, s>>>(meta, L);
+  if (flags & FORK_CHECKS) meta_check_kernel<<<1, 1024, 0, s>>>(meta, L);
+  return cuda_rc(cudaGetLastError());
+}
+
+extern "C" size_t fork_desc_capacity_words(int32_t max_req, int32_t max_q) {
+  if (max_req < 1 || max_req > (1 << 16) || max_q < 0 || max_q > (1 << 18)) return 0;
+  return static_cast<size_t>(2) + 4 * static_cast<size_t>(max_req) + static_cast<size_t>(max_q);
+}
+
+extern "C" int fork_build_meta_dev(const fork_meta* m, const int32_t* d_desc, uint32_t flags, void* stream) {
+  MetaLayout L;
+  int rc = check_meta(m, &L);
+  if (rc != FORK_OK) return rc;
+  if (!d_desc) return FORK_EINVAL;
+  if ((rc = check_device()) != FORK_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* meta = static_cast<int32_t*>(m->d_buf);
+  meta_tables_kernel<<<1, 1024, 0, s>>>(d_desc, 0, 0, 1, meta, L, m->tile_tokens);
   meta_tokens_kernel<<<L.max_seg + 1, 256, 0, s>>>(meta, L);
   if (flags & FORK_CHECKS) meta_check_kernel<<<1, 1024, 0, s>>>(meta, L);
   return cuda_rc(cudaGetLastError());

@@ -61,6 +61,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fork_meta_bytes": (sz, [i32, i32, i32]),
         "fork_meta_init": (ctypes.c_int, [MP, vp, sz, i32, i32, i32, i32]),
         "fork_build_meta": (ctypes.c_int, [MP, vp, i32, i32, u32, vp]),
+        "fork_desc_capacity_words": (sz, [i32, i32]),
+        "fork_build_meta_dev": (ctypes.c_int, [MP, vp, u32, vp]),
         "fork_read_status": (ctypes.c_int, [MP, ctypes.POINTER(i32), vp]),
         "fork_last_cuda_error": (ctypes.c_int, []),
         "fork_attn_workspace_bytes": (sz, [i32, i32, i32, i32, i32, f32, u32]),
@@ -134,6 +136,15 @@ def fork_meta_bytes(T_cap: int, max_req: int, max_q: int) -> int:
 
 def fork_build_meta(meta: Meta, desc: torch.Tensor, R: int, Nq: int, flags: int = 0, stream=None):
     _check("fork_build_meta", load().fork_build_meta(meta.ref, _ptr(desc), R, Nq, flags, _stream(stream)))
+
+
+def fork_desc_capacity_words(max_req: int, max_q: int) -> int:
+    return load().fork_desc_capacity_words(max_req, max_q)
+
+
+def fork_build_meta_dev(meta: Meta, desc: torch.Tensor, flags: int = 0, stream=None):
+    """Metadata from a fixed-capacity device descriptor (counts read on the device)."""
+    _check("fork_build_meta_dev", load().fork_build_meta_dev(meta.ref, _ptr(desc), flags, _stream(stream)))
 
 
 def fork_read_status(meta: Meta, stream=None) -> int:

@@ -27,7 +27,7 @@ def offsets(T_cap: int, max_req: int, max_q: int):
                                     "seg_trunk_start", "seg_trunk_len", "seg_state_idx")]
     plan += [(k, max_req) for k in ("req_trunk_len", "req_prefix_len", "req_prefix_off", "req_ckpt_pos",
                                     "req_trunk_start", "req_first_q", "req_n_q")]
-    plan += [("q_last", max(max_q, 1)), ("work_seg", max_work), ("work_off", max_work)]
+    plan += [("q_last", max(max_q, 1)), ("work_seg", max_work), ("work_off", max_work), ("work_order", max_work)]
     for name, n in plan:
         out[name] = (o, n)
         o = _align(o + n)

@@ -64,6 +64,19 @@ def _layout(rnd: Round):
     return trunk_rows, trunk_start, q_start, first_q, prefix_off
 
 
+def shard_rows(rnd: Round, requests: Sequence[int]) -> Tuple[np.ndarray, List[int]]:
+    """Stream rows of `rnd` that form the sub-round of `requests` (in its stream order:
+    the chosen trunks, then their questions), and the global question indices."""
+    trunk_rows, trunk_start, q_start, first_q, _ = _layout(rnd)
+    qids: List[int] = []
+    for j in requests:
+        qids.extend(range(int(first_q[j]), int(first_q[j]) + int(rnd.n_q[j])))
+    rows = [np.arange(trunk_start[j], trunk_start[j] + trunk_rows[j]) for j in requests]
+    rows += [np.arange(q_start[i], q_start[i] + int(rnd.q_len[i])) for i in qids]
+    rows = np.concatenate(rows).astype(np.int64) if rows else np.zeros(0, np.int64)
+    return rows, qids
+
+
 def shard_round(rnd: Round, requests: Sequence[int], T_cap: int = None) -> Tuple[Round, List[int]]:
     """The sub-round made of `requests` (indices into `rnd`, in request order).
 
@@ -77,14 +90,8 @@ def shard_round(rnd: Round, requests: Sequence[int], T_cap: int = None) -> Tuple
     if sorted(req) != req or len(set(req)) != len(req) or any(j < 0 or j >= rnd.R for j in req):
         raise ValueError("requests must be distinct indices in increasing order")
     cap = rnd.T_cap if T_cap is None else int(T_cap)
-    trunk_rows, trunk_start, q_start, first_q, prefix_off = _layout(rnd)
-    qids: List[int] = []
-    for j in req:
-        qids.extend(range(int(first_q[j]), int(first_q[j]) + int(rnd.n_q[j])))
-    # stream rows of the sub-round, in order: trunks, then questions
-    rows = [np.arange(trunk_start[j], trunk_start[j] + trunk_rows[j]) for j in req]
-    rows += [np.arange(q_start[i], q_start[i] + int(rnd.q_len[i])) for i in qids]
-    rows = np.concatenate(rows).astype(np.int64) if rows else np.zeros(0, np.int64)
+    prefix_off = _layout(rnd)[4]
+    rows, qids = shard_rows(rnd, req)  # stream rows of the sub-round, in order: trunks, then questions
     if rows.shape[0] > cap:
         raise ValueError(f"shard of {rows.shape[0]} tokens exceeds capacity {cap}")
 
@@ -109,6 +116,25 @@ def shard_round(rnd: Round, requests: Sequence[int], T_cap: int = None) -> Tuple
                 rnd.prefix_len[req].copy(), rnd.ckpt_pos[req].copy(), n_opt, cap, rnd.attn_shapes,
                 rnd.gdn_shape, layers, rnd.w_opt[opt_rows].copy(), opt_off, prefix=prefix)
     return sub, qids
+
+
+def split_to_fit(rnd: Round, cap: int) -> Tuple[List[List[int]], List[int]]:
+    """Split a round at request boundaries into groups of requests whose streams each
+    hold at most `cap` tokens (requests balanced by tokens, largest first, over the
+    fewest groups that fit).  Requests longer than `cap` on their own are returned
+    apart (they run without a capacity bucket)."""
+    tok = request_tokens(rnd)
+    big = [j for j in range(rnd.R) if tok[j] > cap]
+    rest = [j for j in range(rnd.R) if tok[j] <= cap]
+    if not rest:
+        return [], big
+    n = max(1, -(-int(tok[rest].sum()) // cap))
+    while True:
+        parts = assign_requests(tok[rest], n)
+        groups = [[rest[i] for i in part] for part in parts if part]
+        if all(int(tok[g].sum()) <= cap for g in groups):
+            return groups, big
+        n += 1
 
 
 def scatter_probabilities(rnd: Round, parts) -> np.ndarray:

@@ -331,6 +331,8 @@ def custom_round(trunk_len, n_q, q_len, *, attn_shapes, gdn_shape, T_cap, seed=0
     n = np.asarray(n_q, dtype=np.int32)
     ql = np.asarray(q_len, dtype=np.int32)
     R = P.shape[0]
+    if int(n.sum()) != ql.shape[0] or n.shape[0] != R:
+        raise ValueError("question counts do not match the question lengths")
     if n_opt is None:
         no = rng.integers(2, 8, size=ql.shape[0], endpoint=True).astype(np.int32)
     else:
