@@ -331,8 +331,18 @@ def main():
     from tree_forked_hybrid_gb300 import roofline as RL
     from tree_forked_hybrid_gb300.runner import DeviceRound
 
-    # every rank runs its own round (requests shard across GPUs with no exchange)
-    rnd = wl.make_round(WORKLOAD_ID, seed=WORKLOAD_ID + 1000 * rank)
+    # one round; with N GPUs it holds N times the requests and each rank runs its shard
+    # (requests balanced by tokens; no exchange on the data path, the option
+    # probabilities are gathered to rank 0 afterwards)
+    shard = None
+    if ws > 1:
+        from tree_forked_hybrid_gb300 import shard as S
+        shapes = wl.draw_round_shapes(WORKLOAD_ID, ws, seed=WORKLOAD_ID)
+        req, P, n, ql, no, qids = S.shard_shapes(*shapes, ws, rank)
+        rnd = wl.make_round(WORKLOAD_ID, seed=WORKLOAD_ID + 1000 * rank, trunk_len=P, n_q=n, q_len=ql, n_opt=no)
+        shard = {"shapes": shapes, "qids": qids, "requests": req}
+    else:
+        rnd = wl.make_round(WORKLOAD_ID)
     dr = DeviceRound(rnd, device=f"cuda:{local}")
     stream = torch.cuda.current_stream()
     calls = [("meta", dr.step_meta)] + [(f"attn_{a.name}", (lambda n=a.name: dr.step_attn(n)))
@@ -449,6 +459,11 @@ def main():
             out["graph_replay"] = graph_timing(torch, args, local)
         except Exception as exc:  # reported, never fatal for the main line
             out["graph_replay"] = {"error": f"{type(exc).__name__}: {exc}"}
+    if shard is not None:
+        out["sharding"] = gather_shards(dist, dr, rnd, shard, rank, ws)
+        out["config"]["sharding"] = (f"one round of {shard['shapes'][0].shape[0]} requests "
+                                     f"({int(shard['shapes'][0].sum() + shard['shapes'][2].sum())} tokens) split at "
+                                     f"request boundaries over {ws} GPUs; per-rank values drawn from the rank's seed")
     if rank == 0 and ws == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(rnd)
     if rank == 0:
@@ -456,6 +471,27 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def gather_shards(dist, dr, rnd, shard, rank, ws):
+    """Gather every rank's option probabilities to rank 0 in the whole round's layout and
+    check each question's distribution sums to one."""
+    from tree_forked_hybrid_gb300 import shard as S
+    P, n, ql, no = shard["shapes"]
+    p = dr.p[:int(rnd.opt_off[-1])].cpu().numpy()
+    parts = [None] * ws
+    dist.all_gather_object(parts, (shard["qids"], p))
+    if rank != 0:
+        return None
+    whole = type("WholeRound", (), {})()
+    whole.Nq = int(ql.shape[0])
+    whole.n_opt = no
+    whole.opt_off = np.concatenate([[0], np.cumsum(no)]).astype(np.int64)
+    pall = S.scatter_probabilities(whole, parts)
+    sums = np.add.reduceat(pall, whole.opt_off[:-1]) if whole.Nq else np.zeros(0)
+    return {"requests": int(P.shape[0]), "questions": whole.Nq,
+            "rank_requests": [len(x[0]) for x in parts],
+            "max_abs_sum_minus_1": float(np.abs(sums - 1.0).max()) if whole.Nq else 0.0}
 
 
 def readout_mlp_timing(torch, dr, rnd, stream, peaks, reps=20):

@@ -300,6 +300,20 @@ int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D, int32_t F
                      const float* g2, const uint16_t* w_opt, const int32_t* opt_off, float* p,
                      void* workspace, size_t ws_bytes, uint32_t flags, void* stream);
 
+/* The same pointwise block on every stream row (the cost the selective readout
+ * avoids; onedev "어떻게 쓰나"): for each row r < T,
+ *   z_r = bf16(rmsnorm(h_r + W_down a_r) * g2),  a_r = bf16(silu(W_gate n_r) * (W_up n_r)),
+ *   n_r = bf16(rmsnorm(h_r) * g1);
+ * fork_readout(m, z, ...) then gives eq. (1) from the questions' rows of z.
+ *   z [T_cap, D] bf16 (pad rows not written); other arguments as for
+ *   fork_readout_mlp; workspace of fork_pointwise_rows_workspace_bytes(T_cap,
+ *   D, F) bytes (the same three buffers for T_cap rows). */
+size_t fork_pointwise_rows_workspace_bytes(int32_t T_cap, int32_t D, int32_t F);
+int fork_pointwise_rows(const fork_meta* m, const uint16_t* h, int32_t D, int32_t F, const float* g1,
+                        const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                        const float* g2, uint16_t* z, void* workspace, size_t ws_bytes, uint32_t flags,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -728,6 +728,7 @@ __global__ void __launch_bounds__(NT, 1)
       const float* NQ = gate(slot, G_NQ);
       const float* NK = gate(slot, G_NK);
       unsigned char* yts = yt(slot);
+      unsigned char* pb = pbt(slot);
       const bool more = c0 + C < len;  // another chunk of this segment follows
       const bool need_state = !BRANCH || more;
       // ---- C0: operands of chunk k ready; a question starts from its request's S_P ----
@@ -855,7 +856,7 @@ __global__ void __launch_bounds__(NT, 1)
         tc::tc_fence_after();
         constexpr uint32_t id5 = tc::idesc_fp16(128, 64, 0, 0);
         constexpr uint32_t id6 = tc::idesc_fp16(128, 128, 0, 1);
-        const uint64_t dp = tc::sdesc_sw128(tc::smem_u32(pbt(slot)), 16, 1024);
+        const uint64_t dp = tc::sdesc_sw128(tc::smem_u32(pb), 16, 1024);
         const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(yts + C * 128), 16384, 1024);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks)
@@ -867,10 +868,10 @@ __global__ void __launch_bounds__(NT, 1)
                            id6, 1u);
         tc::mma_commit(&bars[B_MB]);
       }
-      // ---- C3: output rows.  Thread v holds column v of the chunk's 64 x 128 output; lane
-      //      pairs swap values so that each store carries two neighbouring columns of one
-      //      token (the even lane token t, the odd lane token t+1): a warp writes two
-      //      64-byte row pieces per store.
+      // ---- C3: output rows, staged 32 tokens at a time in this slot's P tile (read by the
+      //      products just completed).  Thread v holds column v; lane pairs swap values so
+      //      that each shared-memory store carries two neighbouring columns of one token; odd
+      //      rows are rotated by 64 bytes so the two tokens of one store use different banks.
       if (!(ok = cwait(B_MB, k & 1))) break;
       tc::tc_fence_after();
       {
@@ -883,14 +884,27 @@ __global__ void __launch_bounds__(NT, 1)
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
+            // even lane: (token t, columns v, v+1); odd lane: (token t+1, columns v-1, v)
             const float mine_t = __uint_as_float(v32[e]), mine_t1 = __uint_as_float(v32[e + 1]);
             const float other = __shfl_xor_sync(0xffffffffu, odd ? mine_t : mine_t1, 1);
-            const int t = q * 32 + e + (odd ? 1 : 0);
+            const int t = e + (odd ? 1 : 0);
             const __nv_bfloat162 pr =
                 odd ? __floats2bfloat162_rn(other, mine_t1) : __floats2bfloat162_rn(mine_t, other);
-            if (t < n)
-              *reinterpret_cast<__nv_bfloat162*>(p.o + (static_cast<int64_t>(start + c0 + t) * H + h) * D + v0) = pr;
+            *reinterpret_cast<__nv_bfloat162*>(pb + t * (D * 2) + ((v0 * 2 + (t & 1) * 64) & (D * 2 - 1))) = pr;
           }
+          role_sync(2, NCH);
+          const int cq = ct & 15;  // 16-byte piece of a 256-byte row
+#pragma unroll
+          for (int pass = 0; pass < 4; ++pass) {
+            const int t = pass * 8 + (ct >> 4);
+            if (q * 32 + t < n) {
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(pb + t * (D * 2) + ((cq * 16 + (t & 1) * 64) & (D * 2 - 1)));
+              *reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(start + c0 + q * 32 + t) * H + h) * D + cq * 8) =
+                  val;
+            }
+          }
+          role_sync(2, NCH);
         }
       }
       if (more) {  // the next chunk of this segment: its decay is known once its gates are

@@ -53,15 +53,22 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 }  // namespace
 
-// n_i = bf16(rmsnorm(h_{q_last(i)}) * g1) into row i of A [Mpad, D]
+// Rows of the block: the questions' last rows (selective readout), or every stream row.
+__device__ __forceinline__ int ro_rows(const int32_t* meta, int all) { return all ? meta[H_T] : meta[H_NQ]; }
+__device__ __forceinline__ int ro_src(const int32_t* meta, const MetaLayout& L, int all, int i) {
+  return all ? i : meta[L.q_last + i];
+}
+
+// n_i = bf16(rmsnorm(h_{row(i)}) * g1) into row i of A [Mpad, D]
 __global__ void __launch_bounds__(256) ro_norm_kernel(const int32_t* __restrict__ meta, MetaLayout L,
                                                       const uint16_t* __restrict__ h, int D,
-                                                      const float* __restrict__ g1, uint16_t* __restrict__ A) {
+                                                      const float* __restrict__ g1, uint16_t* __restrict__ A,
+                                                      int all) {
   __shared__ float red[8];
   if (meta[H_VALID] == 0) return;
   const int i = blockIdx.x;
-  if (i >= meta[H_NQ]) return;
-  const uint16_t* x = h + static_cast<int64_t>(meta[L.q_last + i]) * D;
+  if (i >= ro_rows(meta, all)) return;
+  const uint16_t* x = h + static_cast<int64_t>(ro_src(meta, L, all, i)) * D;
   float ss = 0.f;
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
     const float v = bf2f(x[d]);
@@ -82,12 +89,12 @@ __global__ void __launch_bounds__(128) ro_gemm_kernel(const int32_t* __restrict_
                                                       const uint16_t* __restrict__ W0,
                                                       const uint16_t* __restrict__ W1,
                                                       uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32,
-                                                      const uint16_t* __restrict__ h) {
+                                                      const uint16_t* __restrict__ h, int all) {
   constexpr int NW = GLU ? 2 : 1;
   __shared__ __align__(16) uint16_t As[2][kMT][kLD];
   __shared__ __align__(16) uint16_t Ws[2][NW][kNT][kLD];
   if (meta[H_VALID] == 0) return;
-  const int nq = meta[H_NQ];
+  const int nq = ro_rows(meta, all);
   const int m0 = blockIdx.y * kMT, n0 = blockIdx.x * kNT;
   if (m0 >= nq) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(128) ro_gemm_kernel(const int32_t* __restrict_
         *reinterpret_cast<uint32_t*>(out_bf16 + static_cast<int64_t>(row) * N + col) = pack2(s0 * u0, s1 * u1);
       } else {
         const uint32_t hv =
-            *reinterpret_cast<const uint32_t*>(h + static_cast<int64_t>(meta[L.q_last + row]) * N + col);
+            *reinterpret_cast<const uint32_t*>(h + static_cast<int64_t>(ro_src(meta, L, all, row)) * N + col);
         float2 y;
         y.x = c0 + bf2f(static_cast<uint16_t>(hv & 0xffffu));
         y.y = c1 + bf2f(static_cast<uint16_t>(hv >> 16));
@@ -215,6 +222,20 @@ __global__ void __launch_bounds__(256) ro_final_kernel(const int32_t* __restrict
   }
 }
 
+// z_r = bf16(rmsnorm(y_r) * g2) for every stream row r (the block on all rows)
+__global__ void __launch_bounds__(256) ro_znorm_kernel(const int32_t* __restrict__ meta, const float* __restrict__ Y,
+                                                       int D, const float* __restrict__ g2, uint16_t* __restrict__ z) {
+  __shared__ float red[8];
+  if (meta[H_VALID] == 0) return;
+  const int r = blockIdx.x;
+  if (r >= meta[H_T]) return;
+  const float* y = Y + static_cast<int64_t>(r) * D;
+  float ss = 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) ss += y[d] * y[d];
+  const float inv = 1.f / sqrtf(block_sum(ss, red) / static_cast<float>(D) + kEps);
+  for (int d = threadIdx.x; d < D; d += blockDim.x) z[static_cast<int64_t>(r) * D + d] = f2bf(y[d] * inv * g2[d]);
+}
+
 struct RoWs {
   size_t a1, a2, y, total;
 };
@@ -262,13 +283,48 @@ extern "C" int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D
   float* y = reinterpret_cast<float*>(ws + w.y);
   const int32_t* meta = static_cast<const int32_t*>(m->d_buf);
   const int mt = (m->max_q + kMT - 1) / kMT;
-  ro_norm_kernel<<<m->max_q, 256, 0, s>>>(meta, L, h, D, g1, a1);
-  ro_gemm_kernel<true><<<dim3(F / kNT, mt), 128, 0, s>>>(meta, L, a1, D, F, w_gate, w_up, a2, nullptr, nullptr);
-  ro_gemm_kernel<false><<<dim3(D / kNT, mt), 128, 0, s>>>(meta, L, a2, F, D, w_down, nullptr, nullptr, y, h);
+  ro_norm_kernel<<<m->max_q, 256, 0, s>>>(meta, L, h, D, g1, a1, 0);
+  ro_gemm_kernel<true><<<dim3(F / kNT, mt), 128, 0, s>>>(meta, L, a1, D, F, w_gate, w_up, a2, nullptr, nullptr, 0);
+  ro_gemm_kernel<false><<<dim3(D / kNT, mt), 128, 0, s>>>(meta, L, a2, F, D, w_down, nullptr, nullptr, y, h, 0);
   const int zbytes = D * 4;
   if (zbytes > 48 * 1024 &&
       cuda_rc(cudaFuncSetAttribute(ro_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, zbytes)) != FORK_OK)
     return FORK_ECUDA;
   ro_final_kernel<<<m->max_q, 256, zbytes, s>>>(meta, y, D, g2, w_opt, opt_off, p);
+  return cuda_rc(cudaGetLastError());
+}
+
+extern "C" size_t fork_pointwise_rows_workspace_bytes(int32_t T_cap, int32_t D, int32_t F) {
+  if (T_cap < 1 || D < 64 || D % 64 != 0 || D > 8192 || F < 64 || F % 64 != 0 || F > 65536) return 0;
+  return ro_ws(T_cap, D, F).total;
+}
+
+extern "C" int fork_pointwise_rows(const fork_meta* m, const uint16_t* h, int32_t D, int32_t F, const float* g1,
+                                   const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                                   const float* g2, uint16_t* z, void* workspace, size_t ws_bytes, uint32_t flags,
+                                   void* stream) {
+  (void)flags;
+  MetaLayout L;
+  int rc = check_meta(m, &L);
+  if (rc != FORK_OK) return rc;
+  if (!h || !g1 || !w_gate || !w_up || !w_down || !g2 || !z || !workspace) return FORK_EINVAL;
+  if (D < 64 || D % 64 != 0 || D > 8192 || F < 64 || F % 64 != 0 || F > 65536) return FORK_EINVAL;
+  if (!is_aligned16(h) || !is_aligned16(w_gate) || !is_aligned16(w_up) || !is_aligned16(w_down) ||
+      !is_aligned16(z) || !is_aligned16(workspace))
+    return FORK_EINVAL;
+  const RoWs w = ro_ws(L.T_cap, D, F);
+  if (ws_bytes < w.total) return FORK_EINVAL;
+  if ((rc = check_device()) != FORK_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  uint16_t* a1 = reinterpret_cast<uint16_t*>(ws + w.a1);
+  uint16_t* a2 = reinterpret_cast<uint16_t*>(ws + w.a2);
+  float* y = reinterpret_cast<float*>(ws + w.y);
+  const int32_t* meta = static_cast<const int32_t*>(m->d_buf);
+  const int mt = (L.T_cap + kMT - 1) / kMT;
+  ro_norm_kernel<<<L.T_cap, 256, 0, s>>>(meta, L, h, D, g1, a1, 1);
+  ro_gemm_kernel<true><<<dim3(F / kNT, mt), 128, 0, s>>>(meta, L, a1, D, F, w_gate, w_up, a2, nullptr, nullptr, 1);
+  ro_gemm_kernel<false><<<dim3(D / kNT, mt), 128, 0, s>>>(meta, L, a2, F, D, w_down, nullptr, nullptr, y, h, 1);
+  ro_znorm_kernel<<<L.T_cap, 256, 0, s>>>(meta, y, D, g2, z);
   return cuda_rc(cudaGetLastError());
 }

@@ -77,6 +77,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fork_readout": (ctypes.c_int, [MP, vp, i32, vp, vp, vp, u32, vp]),
         "fork_readout_mlp_workspace_bytes": (sz, [i32, i32, i32]),
         "fork_readout_mlp": (ctypes.c_int, [MP, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, u32, vp]),
+        "fork_pointwise_rows_workspace_bytes": (sz, [i32, i32, i32]),
+        "fork_pointwise_rows": (ctypes.c_int, [MP, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, u32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -207,3 +209,15 @@ def fork_readout_mlp(meta: Meta, h, D: int, F: int, g1, w_gate, w_up, w_down, g2
     _check("fork_readout_mlp", load().fork_readout_mlp(
         meta.ref, _ptr(h), D, F, _ptr(g1), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(g2), _ptr(w_opt),
         _ptr(opt_off), _ptr(p), _ptr(workspace), ws_bytes, flags, _stream(stream)))
+
+
+def fork_pointwise_rows_workspace_bytes(T_cap: int, D: int, F: int) -> int:
+    return load().fork_pointwise_rows_workspace_bytes(T_cap, D, F)
+
+
+def fork_pointwise_rows(meta: Meta, h, D: int, F: int, g1, w_gate, w_up, w_down, g2, z, workspace, flags: int = 0,
+                        stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fork_pointwise_rows", load().fork_pointwise_rows(
+        meta.ref, _ptr(h), D, F, _ptr(g1), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(g2), _ptr(z),
+        _ptr(workspace), ws_bytes, flags, _stream(stream)))

@@ -153,3 +153,15 @@ def scatter_probabilities(rnd: Round, parts) -> np.ndarray:
     if not seen.all():
         raise ValueError("some questions came from no rank")
     return p
+
+
+def shard_shapes(P: np.ndarray, n: np.ndarray, ql: np.ndarray, no: np.ndarray, world: int, rank: int):
+    """This rank's requests of a round given by its shapes (trunk lengths P, question
+    counts n, question lengths ql, option counts no), balanced by stream tokens over
+    `world` ranks: (requests, their P, n, question lengths, option counts, global
+    question indices)."""
+    first = np.concatenate([[0], np.cumsum(n)]).astype(np.int64)
+    tok = [int(P[j]) + int(ql[first[j]:first[j + 1]].sum()) for j in range(P.shape[0])]
+    req = assign_requests(tok, world)[rank]
+    qids = [i for j in req for i in range(int(first[j]), int(first[j + 1]))]
+    return (req, P[req].copy(), n[req].copy(), ql[qids].copy(), no[qids].copy(), qids)

@@ -284,6 +284,28 @@ def make_round(wid: int, seed: Optional[int] = None, *, trunk_len=None, n_q=None
     return rnd
 
 
+def draw_round_shapes(wid: int, copies: int, seed: int):
+    """Request and question shapes of a round of workload ``wid`` with ``copies`` times
+    its requests, drawn from the same distributions (trunk lengths, question counts,
+    question lengths, option counts); no layer values.  Used to shard one large round
+    over several GPUs."""
+    rng = np.random.default_rng(seed)
+    if wid == 1:
+        R, Pr, nr, qr = 32, (256, 512), (1, 4), (16, 48)
+    elif wid == 2:
+        R, Pr, nr, qr = 8, (256, 400), (48, 48), (12, 32)
+    elif wid == 3:
+        R, Pr, nr, qr = 4, (4096, 6144), (8, 20), (32, 64)
+    else:
+        raise ValueError(wid)
+    R *= copies
+    P = rng.integers(Pr[0], Pr[1], size=R, endpoint=True).astype(np.int32)
+    n = rng.integers(nr[0], nr[1], size=R, endpoint=True).astype(np.int32)
+    ql = rng.integers(qr[0], qr[1], size=int(n.sum()), endpoint=True).astype(np.int32)
+    no = rng.integers(2, 8, size=int(n.sum()), endpoint=True).astype(np.int32)
+    return P, n, ql, no
+
+
 def make_resume_round(round_a: Round, m: int = RESUME_M, n_new: int = RESUME_NEW,
                       n_questions: int = 64, T_cap: int = RESUME_TCAP_B) -> Round:
     """Workload 4, round B: request 0 of ``round_a`` shares its first ``m``
