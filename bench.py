@@ -308,8 +308,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' lines")
-    ap.add_argument("--readout-mlp", action="store_true",
-                    help="also time the selective-readout block (norm, SwiGLU MLP, final norm, eq. (1))")
+    ap.add_argument("--no-block", action="store_true",
+                    help="skip the hybrid block timing (pointwise block on the question rows vs every row)")
     ap.add_argument("--no-graph", action="store_true",
                     help="skip the short-request round timed eagerly and as one CUDA graph replay")
     args = ap.parse_args()
@@ -402,8 +402,8 @@ def main():
                 "frac_of_sustained": ach / peaks["bf16_tflops_sustained"]}
         if top == "attn_attn" and kernel_alone:
             ka = f / (kernel_alone / 1e3) / 1e12
-            roof["kernel_alone"] = {"kernel": "attn_tc_kernel (same round, keys not rotated: the same visible "
-                                              "pairs and FLOPs)",
+            roof["kernel_alone"] = {"kernel": "fork_attn without the rotary embedding: fp16 values and "
+                                              "attn_tc_kernel (same round: the same visible pairs and FLOPs)",
                                     "ms": kernel_alone, "achieved": ka, "peak": peaks["bf16_tflops"],
                                     "frac": ka / peaks["bf16_tflops"],
                                     "peak_note": f"bf16 dense burst ({peaks['source']}); timed alone after the "
@@ -449,11 +449,11 @@ def main():
                                            main_entry)
         except Exception as exc:  # reported, never fatal for the main line
             out["per_config"] = {"error": f"{type(exc).__name__}: {exc}"}
-    if args.readout_mlp:
+    if not args.no_block and ws == 1:
         try:
-            out["readout_mlp"] = readout_mlp_timing(torch, dr, rnd, stream, peaks)
+            out["hybrid_block"] = hybrid_block_timing(torch, dr, rnd, stream, peaks)
         except Exception as exc:  # reported, never fatal for the main line
-            out["readout_mlp"] = {"error": f"{type(exc).__name__}: {exc}"}
+            out["hybrid_block"] = {"error": f"{type(exc).__name__}: {exc}"}
     if not args.no_graph and ws == 1:
         try:
             out["graph_replay"] = graph_timing(torch, args, local)
@@ -494,10 +494,12 @@ def gather_shards(dist, dr, rnd, shard, rank, ws):
             "max_abs_sum_minus_1": float(np.abs(sums - 1.0).max()) if whole.Nq else 0.0}
 
 
-def readout_mlp_timing(torch, dr, rnd, stream, peaks, reps=20):
-    """The selective-readout block on this round's question rows (D = H*dv, F = 2D):
-    mean CUDA-event time, against the HBM roofline of its weight bytes."""
-    import numpy as np
+def hybrid_block_timing(torch, dr, rnd, stream, peaks, reps=5):
+    """The last layer's pointwise block on the question rows only (fork_readout_mlp, the
+    selective readout) against the same block on every stream row (fork_pointwise_rows,
+    then eq. (1) from the questions' rows): CUDA-event times of the block alone and of the
+    hybrid block (GDN mixer calls + block), and the readout block's HBM roofline fraction
+    (its weight bytes)."""
     from tree_forked_hybrid_gb300 import fork as F
     from tree_forked_hybrid_gb300 import workloads as wl
     D = rnd.D
@@ -506,27 +508,44 @@ def readout_mlp_timing(torch, dr, rnd, stream, peaks, reps=20):
     dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dr.device)
     W = {k: dev(v) for k, v in wts.items()}
     ws = torch.empty(F.fork_readout_mlp_workspace_bytes(dr.max_q, D, Fw), dtype=torch.uint8, device=dr.device)
-    p = torch.empty_like(dr.p)
+    wsa = torch.empty(F.fork_pointwise_rows_workspace_bytes(rnd.T_cap, D, Fw), dtype=torch.uint8, device=dr.device)
+    z = torch.empty((rnd.T_cap, D), dtype=torch.bfloat16, device=dr.device)
+    p_sel = torch.empty_like(dr.p)
+    p_all = torch.empty_like(dr.p)
 
-    def call():
+    def selective():
         F.fork_readout_mlp(dr.meta, dr.gdn_out, D, Fw, W["g1"], W["w_gate"], W["w_up"], W["w_down"], W["g2"],
-                           dr.w_opt, dr.opt_off, p, ws, 0, stream)
+                           dr.w_opt, dr.opt_off, p_sel, ws, 0, stream)
 
-    for _ in range(3):
-        call()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
-    nbytes = 3 * D * Fw * 2 + rnd.Nq * D * 2 + int(rnd.opt_off[-1]) * D * 2
-    gbs = nbytes / (ms / 1e3) / 1e9
-    return {"block": f"Nq={rnd.Nq} rows, D={D}, F={Fw}", "ms": ms, "bytes": nbytes, "achieved_gbs": gbs,
-            "frac_hbm": gbs / peaks["hbm_gbs"], "flops": 6 * rnd.Nq * D * Fw}
+    def all_rows():
+        F.fork_pointwise_rows(dr.meta, dr.gdn_out, D, Fw, W["g1"], W["w_gate"], W["w_up"], W["w_down"], W["g2"],
+                              z, wsa, 0, stream)
+        F.fork_readout(dr.meta, z, D, dr.w_opt, dr.opt_off, p_all, 0, stream)
+
+    def mixer():
+        dr.step_gdn_trunk(stream)
+        dr.step_gdn_branches(stream)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        return latency_stats(step_times(torch, fn, stream, reps))["median"]
+
+    t_sel, t_all, t_mix = timed(selective), timed(all_rows), timed(mixer)
+    if dr.status() != 0:
+        raise RuntimeError(f"device status {dr.status():#x}")
+    off = rnd.opt_off
+    a, b = p_sel.cpu().numpy(), p_all.cpu().numpy()
+    tv = max(0.5 * float(np.abs(a[off[i]:off[i + 1]] - b[off[i]:off[i + 1]]).sum()) for i in range(rnd.Nq)) \
+        if rnd.Nq else 0.0
+    nbytes = 3 * D * Fw * 2 + rnd.Nq * D * 2 + int(off[-1]) * D * 2
+    gbs = nbytes / (t_sel / 1e3) / 1e9
+    return {"block": f"pre-norm SwiGLU MLP + residual + final RMSNorm, D={D}, F={Fw}; Nq={rnd.Nq} question rows "
+                     f"of T={rnd.T}",
+            "selective_block_ms": t_sel, "all_rows_block_ms": t_all,
+            "hybrid_selective_ms": t_mix + t_sel, "hybrid_all_rows_ms": t_mix + t_all,
+            "saving": 1.0 - (t_mix + t_sel) / (t_mix + t_all), "tv_selective_vs_all_rows": tv,
+            "selective_hbm": {"bytes": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}}
 
 
 def graph_timing(torch, args, local, wid=1):
@@ -556,8 +575,8 @@ def graph_timing(torch, args, local, wid=1):
 
 
 def attn_kernel_alone(torch, dr, rnd, stream, reps=10):
-    """Mean duration (ms) of the attention kernel alone for the full-attention layer:
-    fork_attn with the rotation off launches only attn_tc_kernel, which does the same
+    """Mean duration (ms) of the full-attention layer's call without the rotary
+    embedding: the value conversion to fp16 and attn_tc_kernel, which does the same
     visible-pair work as in the step.  Writes a scratch output."""
     import math
     from tree_forked_hybrid_gb300 import fork as F
@@ -567,10 +586,12 @@ def attn_kernel_alone(torch, dr, rnd, stream, reps=10):
     a = a[0]
     inp = dr.inputs[a.name]
     out = torch.empty_like(dr.attn_out[a.name])
+    nb = F.fork_attn_workspace_bytes(rnd.T_cap, 0, a.Hq, a.Hkv, a.d, 0.0, dr.flags)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dr.device) if nb else None
 
     def call():
         F.fork_attn(dr.meta, inp["q"], inp["k"], inp["v"], out, a.Hq, a.Hkv, a.d, a.window, 0.0,
-                    1.0 / math.sqrt(a.d), None, None, None, dr.flags, stream)
+                    1.0 / math.sqrt(a.d), None, None, ws, dr.flags, stream)
 
     for _ in range(3):
         call()

@@ -164,10 +164,13 @@ int fork_read_status(const fork_meta* m, int32_t* h_status, void* stream);
  * rotary positions they would have alone).
  * ------------------------------------------------------------------------ */
 
-/* Workspace bytes fork_attn needs with these flags: rotated keys of the
- * stream, rotated prefix keys, two small rotary tables, and with FORK_WARP_MMA
- * also rotated queries (the default kernel rotates its query tiles in shared
- * memory).  0 when rope_theta == 0. */
+/* Workspace bytes fork_attn needs with these flags: with the rotary embedding,
+ * rotated keys of the stream and of the prefix and two small rotary tables
+ * (with FORK_WARP_MMA also rotated queries: the default kernel rotates its query
+ * tiles in shared memory); for the default kernel, the values of the stream and
+ * of the prefix as fp16 (its PV product multiplies fp16 exponentials by fp16
+ * values; inputs beyond the fp16 range, |v| > 65504, are not supported).
+ * 0 only for FORK_WARP_MMA without the rotary embedding. */
 size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq, int32_t Hkv,
                                  int32_t d, float rope_theta, uint32_t flags);
 
@@ -201,10 +204,9 @@ int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k, const ui
  * that loads the library keeps allocated until the process exits.
  *   - Returns FORK_ECAPACITY when fork_attn_workspace_bytes(T_cap,
  *     prefix_rows, Hq, Hkv, d, rope_theta, flags) exceeds
- *     FORK_NOALLOC_SCRATCH_BYTES (e.g. T_cap = 16384 with 16 q-heads,
- *     4 kv-heads, d = 128 fits (about 17 MB: rotated keys and tables);
- *     T_cap = 32768 with 8 kv-heads does not, nor T_cap = 16384 with
- *     FORK_WARP_MMA, which also needs rotated queries).
+ *     FORK_NOALLOC_SCRATCH_BYTES (e.g. T_cap = 8192 with 16 q-heads,
+ *     4 kv-heads, d = 128 fits (about 17 MB: rotated keys, fp16 values and
+ *     tables); T_cap = 16384 with the same heads does not).
  *   - Calls no allocating routine (the array is the one piece of state the
  *     library keeps between calls).  The first call on a device looks up the
  *     array's device address (and loads the module there); make that first

@@ -12,6 +12,8 @@
 #include <cmath>
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "fork_attn.cuh"
 
 namespace fork {
@@ -177,21 +179,50 @@ static bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t
 }
 
 struct AttnWs {
-  size_t qr, kr, pkr, hi, lo, total;
+  size_t qr, kr, pkr, hi, lo, vh, pvh, total;
 };
 
-// Rotated keys (stream, prefix), the two rotary tables and, for the warp-MMA kernel only,
-// rotated queries (the tcgen05 kernel rotates its query tiles in shared memory).
-static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hkv, int64_t d, bool warp_mma) {
+// With the rotary embedding: rotated keys (stream, prefix), the two rotary tables and, for
+// the warp-MMA kernel only, rotated queries (the tcgen05 kernel rotates its query tiles in
+// shared memory).  For the tcgen05 kernel: the values as fp16 (stream, prefix), its PV
+// operand (the exponentials stay fp16).
+static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hkv, int64_t d, bool warp_mma,
+                      bool rope) {
   AttnWs w;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t kv = static_cast<size_t>(T_cap) * Hkv * d * 2, pkv = static_cast<size_t>(prefix_rows) * Hkv * d * 2;
   w.qr = 0;
-  w.kr = al(w.qr + (warp_mma ? static_cast<size_t>(T_cap) * Hq * d * 2 : 0));
-  w.pkr = al(w.kr + static_cast<size_t>(T_cap) * Hkv * d * 2);
-  w.hi = al(w.pkr + static_cast<size_t>(prefix_rows) * Hkv * d * 2);
-  w.lo = al(w.hi + static_cast<size_t>(rope_hi_rows(T_cap + prefix_rows)) * (d / 2) * 8);
-  w.total = al(w.lo + static_cast<size_t>(64) * (d / 2) * 8);
+  w.kr = al(w.qr + (rope && warp_mma ? static_cast<size_t>(T_cap) * Hq * d * 2 : 0));
+  w.pkr = al(w.kr + (rope ? kv : 0));
+  w.hi = al(w.pkr + (rope ? pkv : 0));
+  w.lo = al(w.hi + (rope ? static_cast<size_t>(rope_hi_rows(T_cap + prefix_rows)) * (d / 2) * 8 : 0));
+  w.vh = al(w.lo + (rope ? static_cast<size_t>(64) * (d / 2) * 8 : 0));
+  w.pvh = al(w.vh + (warp_mma ? 0 : kv));
+  w.total = al(w.pvh + (warp_mma ? 0 : pkv));
   return w;
+}
+
+// Values of the stream rows [0, T) and of the prefix rows as fp16 (8 elements per thread).
+__global__ void __launch_bounds__(256) v_half_kernel(const int32_t* __restrict__ meta, const uint16_t* __restrict__ v,
+                                                     const uint16_t* __restrict__ pv, uint16_t* __restrict__ vh,
+                                                     uint16_t* __restrict__ pvh, int64_t row_elems, int prefix_rows) {
+  if (meta[H_VALID] == 0) return;
+  const int64_t n_stream = static_cast<int64_t>(meta[H_T]) * row_elems / 8;
+  const int64_t n_all = n_stream + static_cast<int64_t>(prefix_rows) * row_elems / 8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_all;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool st = i < n_stream;
+    const uint4 x = st ? reinterpret_cast<const uint4*>(v)[i] : reinterpret_cast<const uint4*>(pv)[i - n_stream];
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2 hh = __floats2half2_rn(bf2f(static_cast<uint16_t>(w[e] & 0xffffu)), bf2f(static_cast<uint16_t>(w[e] >> 16)));
+      o[e] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    const uint4 y = make_uint4(o[0], o[1], o[2], o[3]);
+    if (st) reinterpret_cast<uint4*>(vh)[i] = y; else reinterpret_cast<uint4*>(pvh)[i - n_stream] = y;
+  }
 }
 
 }  // namespace fork
@@ -201,8 +232,7 @@ using namespace fork;
 extern "C" size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq,
                                             int32_t Hkv, int32_t d, float rope_theta, uint32_t flags) {
   if (T_cap < 1 || prefix_rows < 0 || Hkv < 1 || Hq < Hkv || (d != 64 && d != 128)) return 0;
-  if (rope_theta == 0.f) return 0;
-  return attn_ws(T_cap, prefix_rows, Hq, Hkv, d, (flags & FORK_WARP_MMA) != 0).total;
+  return attn_ws(T_cap, prefix_rows, Hq, Hkv, d, (flags & FORK_WARP_MMA) != 0, rope_theta != 0.f).total;
 }
 
 extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k,
@@ -252,10 +282,10 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   p.stall = (flags & FORK_TEST_STALL) ? 1 : 0;
   p.wait_ns = wait_ns_of(m);
 
+  const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hq, Hkv, d, warp_mma, rope_theta != 0.f);
+  if (w.total > 0 && (!workspace || ws_bytes < w.total || !is_aligned16(workspace))) return FORK_EINVAL;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
   if (rope_theta != 0.f) {
-    const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hq, Hkv, d, warp_mma);
-    if (!workspace || ws_bytes < w.total || !is_aligned16(workspace)) return FORK_EINVAL;
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
     uint16_t* qr = reinterpret_cast<uint16_t*>(ws + w.qr);
     uint16_t* kr = reinterpret_cast<uint16_t*>(ws + w.kr);
     uint16_t* pkr = reinterpret_cast<uint16_t*>(ws + w.pkr);
@@ -289,6 +319,18 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     p.rotate_q = warp_mma ? 0 : 1;
     p.rope_theta = 0.f;  // keys rotated; queries rotated above or by the attention kernel
   }
+  const uint16_t* vtc = v;  // values read by the tcgen05 kernel: fp16 copies
+  const uint16_t* pvtc = prefix_v;
+  if (!warp_mma) {
+    uint16_t* vh = reinterpret_cast<uint16_t*>(ws + w.vh);
+    uint16_t* pvh = reinterpret_cast<uint16_t*>(ws + w.pvh);
+    const int64_t row_elems = static_cast<int64_t>(Hkv) * d;
+    const int64_t n8 = (static_cast<int64_t>(L.T_cap) + p.prefix_rows) * row_elems / 8;
+    const int blocks = static_cast<int>(std::min<int64_t>((n8 + 255) / 256, 8 * sm_count()));
+    v_half_kernel<<<std::max(blocks, 1), 256, 0, s>>>(p.meta, v, prefix_v, vh, pvh, row_elems, p.prefix_rows);
+    vtc = vh;
+    pvtc = pvh;
+  }
   if (cuda_rc(cudaGetLastError()) != FORK_OK) return FORK_ECUDA;
   const int grid_x = static_cast<int>(std::min<int64_t>(
       L.max_work, (L.T_cap + m->tile_tokens - 1) / m->tile_tokens + L.max_seg));
@@ -296,12 +338,12 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     return d == 64 ? launch_attn_mma<64>(p, grid_x, s) : launch_attn_mma<128>(p, grid_x, s);
   alignas(128) CUtensorMap maps[5];
   const uint16_t* pk = p.prefix_rows > 0 ? p.prefix_k : p.k;
-  const uint16_t* pv = p.prefix_rows > 0 ? p.prefix_v : p.v;
+  const uint16_t* pv = p.prefix_rows > 0 ? pvtc : vtc;
   const int prow = p.prefix_rows > 0 ? p.prefix_rows : L.T_cap;
   const bool two = G * m->tile_tokens == 256;
   const int tile = 128 / G;  // tokens of one 128-row query tile
   if (!make_map(&maps[0], p.q, d, Hq, L.T_cap, G, tile) ||
-      !make_map(&maps[1], p.k, d, Hkv, L.T_cap, 1, 128) || !make_map(&maps[2], v, d, Hkv, L.T_cap, 1, 128) ||
+      !make_map(&maps[1], p.k, d, Hkv, L.T_cap, 1, 128) || !make_map(&maps[2], vtc, d, Hkv, L.T_cap, 1, 128) ||
       !make_map(&maps[3], pk, d, Hkv, prow, 1, 128) || !make_map(&maps[4], pv, d, Hkv, prow, 1, 128))
     return FORK_ECUDA;
   return d == 64 ? launch_attn_tc<64>(p, maps, grid_x, two, s) : launch_attn_tc<128>(p, maps, grid_x, two, s);

@@ -68,15 +68,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 2^a, 2^b of two scores on the SFU in one half-precision pair operation (2^-inf = 0).
-// The arguments are at most 2^8 (the running maximum lags by at most that) and P is
-// rounded to bf16 afterwards, so the half-precision argument and result lose nothing
-// that the bf16 P keeps; returns the pair in fp32.
-__device__ __forceinline__ float2 exp2_pair(float a, float b) {
+// 2^a, 2^b of two scores on the SFU in one half-precision pair operation (2^-inf = 0),
+// returned as an fp16 pair (lower half = a): the P operand of the PV product, whose
+// values are fp16 too.  The arguments are at most 8 (the running maximum lags by at most
+// that), so the results stay below 256.
+__device__ __forceinline__ uint32_t exp2_pair(float a, float b) {
   const __half2 x = __floats2half2_rn(a, b);
   uint32_t y;
   asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(*reinterpret_cast<const uint32_t*>(&x)));
-  return __half22float2(*reinterpret_cast<const __half2*>(&y));
+  return y;
+}
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ===================== MMA issuer =====================
     constexpr uint32_t idesc_qk = tc::idesc_bf16(128, kKeys, 0, 0);
-    constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, 0, 1);
+    constexpr uint32_t idesc_pv = tc::idesc_fp16(128, D, 0, 1);  // P and V fp16
     // descriptors are built once; the start-address field (16-byte units) is then
     // advanced by constants: +2 per 32-byte k step, +kBox/16 per box
     const uint64_t dq = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
@@ -495,25 +500,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = resc ? mt : m_used;
         const float base = (m_new == -INFINITY) ? 0.f : m_new;
         const float factor = resc ? exp2f(m_used - base) : 1.f;  // 0 when nothing was accumulated
-        // p = 2^(s*scale*log2e - base), summed with independent partial sums, packed to
-        // bf16 pairs (key order) into the first 64 columns of S_t
-        float ps[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+        // p = 2^(s*scale*log2e - base) as fp16 pairs (key order) into the first 64 columns
+        // of S_t; the row sum adds 8 pairs per fp16 accumulator (each below 2^11), then in fp32
+        float rs = 0.f;
 #pragma unroll
         for (int h2 = 0; h2 < 4; ++h2) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int cc = h2 * 32 + 2 * e;
-            const float2 ab = exp2_pair(fmaf(sv[cc], sl2, -base), fmaf(sv[cc + 1], sl2, -base));
-            ps[(2 * e) & 7] += ab.x;
-            ps[(2 * e + 1) & 7] += ab.y;
-            pk[e] = pack_bf16(ab.x, ab.y);
+            pk[e] = exp2_pair(fmaf(sv[cc], sl2, -base), fmaf(sv[cc + 1], sl2, -base));
           }
           tc::tmem_st16(ts + h2 * 16, pk);
+          uint32_t acc2[2];
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            acc2[a] = pk[8 * a];
+#pragma unroll
+            for (int e = 1; e < 8; ++e) acc2[a] = hadd2(acc2[a], pk[8 * a + e]);
+          }
+          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&acc2[0]));
+          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&acc2[1]));
+          rs += (f0.x + f0.y) + (f1.x + f1.y);
         }
-        const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         l = l * factor + rs;
         m_used = m_new;
         // O_t holds the products of key tiles < f (all complete: S_t(f) was committed after

@@ -47,9 +47,10 @@ namespace fork {
 namespace {
 constexpr int D = 128;
 constexpr int C = 64;
-constexpr int NP = 384;        // prep threads (12 warps)
+constexpr int NCV = 128;       // conv group (4 warps)
+constexpr int NSV = 256;       // solve group (8 warps)
 constexpr int NCH = 128;       // chain threads (4 warps)
-constexpr int NT = NP + NCH;
+constexpr int NT = NCV + NSV + NCH;
 constexpr int KW = 4;
 constexpr int HR = C + KW - 1;  // raw rows staged per chunk
 constexpr int LDC = C + 4;      // plain 64-wide fp32 tiles
@@ -85,7 +86,7 @@ static_assert(Lay::YT % 1024 == 0 && Lay::YV % 1024 == 0 && Lay::WT % 1024 == 0 
               "128-byte-swizzled tiles start on 1024-byte boundaries");
 static_assert(HR * 128 <= Lay::RAWH, "raw rows");
 
-enum { B_RAW = 0, B_M1, B_MW, B_PREP, B_GATE, B_MA, B_MB, B_EPI0, B_EPI1, B_FINP, B_FINC, B_STALL, B_N };
+enum { B_RAW = 0, B_CONV, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_FINP, B_FINC, B_STALL, B_N };
 enum { G_G = 0, G_EG, G_GL, G_ETA, G_IG, G_NQ, G_NK };
 
 // SFU approximations: 2^x, 1/sqrt(x) (relative error ~2^-22), tanh (~2^-11)
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(NT, 1)
   if (tid == 0) {
     // B_STALL is completed by nothing (FORK_TEST_STALL)
     for (int b = 0; b < B_N; ++b)
-      tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1) ? NCH : (b == B_GATE ? 32 : 1));
+      tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1) ? NCH : 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -256,20 +257,19 @@ __global__ void __launch_bounds__(NT, 1)
     return s;
   };
 
-  if (warp < NP / 32) {
-    // ============================ prep (384 threads) ============================
-    auto pwait = [&](int b, uint32_t par) -> bool {
-      return role_and(1, NP, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
+  if (warp < NCV / 32) {
+    // ============================ conv group (128 threads) ============================
+    auto cvwait = [&](int b, uint32_t par) -> bool {
+      return role_and(1, NCV, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
     };
-    // conv mapping: stream st, 8-channel group cg (channels 8cg..8cg+7), block of 8 tokens
-    // tb; the 16 lanes of a half warp hold the 128 channels of the same 8 tokens
-    const int st = tid >> 7, cg = tid & 15, tb = (tid >> 4) & 7;
-    const float4* cw4 = reinterpret_cast<const float4*>(p.conv_w) + ((static_cast<int64_t>(st) * H + h) * D + 8 * cg);
+    // thread = 8-channel group cg (channels 8cg..8cg+7) x block of 8 tokens tb; the 16
+    // lanes of a half warp hold the 128 channels of the same 8 tokens
+    const int cg = tid & 15, tb = (tid >> 4) & 7;
     const CUtensorMap* maps[3] = {&qmap, &kmap, &vmap};
     int raw_issued = 0;
     auto issue_loads = [&](int s, int cc) {
       const int st0 = seg_start(s), ln = seg_len(s);
-      if (tid == 32) {  // (thread 0 issues the products meanwhile)
+      if (tid == 0) {
         tc::fence_proxy_async_smem();  // the rows were last read (and patched) by threads
         tc::mbar_expect_tx(&bars[B_RAW], 6 * HR * 128);
 #pragma unroll
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(NT, 1)
                             st0 + cc - (KW - 1));
       }
       ++raw_issued;
-      if (tid < 2 * C) {
+      {
         const int uu = tid & (C - 1);
         const bool valid = cc + uu < ln;
         const float* src =
@@ -289,15 +289,10 @@ __global__ void __launch_bounds__(NT, 1)
       }
       asm volatile("cp.async.commit_group;\n" ::);
     };
-    if (tid == 32) {
+    if (tid == 0) {
       tc::prefetch_tmap(&qmap);
       tc::prefetch_tmap(&kmap);
       tc::prefetch_tmap(&vmap);
-    }
-    // blocks (0,1) and (2,3) of the fp32 T stay zero (the two-level products read them)
-    for (int e = tid; e < C * C; e += NP) {
-      const int t = e >> 6, s = e & 63;
-      if ((s >> 4) == (t >> 4) + 1 && (t >> 4) % 2 == 0) tm[t * LDC + s] = 0.f;
     }
     bool ok = true;
     int si = first_seg(seg_first), c0 = 0, k = 0;
@@ -314,28 +309,27 @@ __global__ void __launch_bounds__(NT, 1)
       float* NQ = gate(slot, G_NQ);
       float* NK = gate(slot, G_NK);
       unsigned char* yts = yt(slot);
-      unsigned char* pb = pbt(slot);
       int nsi = si, nc0 = c0 + C;
       if (nc0 >= len) {
         nsi = first_seg(si + 1);
         nc0 = 0;
       }
-      // ---- P0: this chunk's rows and gates have landed; history rows of a segment start;
-      //      the slot's tiles are free once the chain has finished chunk k-2
-      if (!(ok = pwait(B_RAW, (raw_issued - 1) & 1))) break;
+      // this chunk's rows and gates have landed; history rows of a segment start; the
+      // slot's tiles are free once the chain has finished chunk k-2
+      if (!(ok = cvwait(B_RAW, (raw_issued - 1) & 1))) break;
       asm volatile("cp.async.wait_group 0;\n" ::);
       if (c0 == 0) {
-        for (int e = tid; e < 3 * (KW - 1) * D; e += NP) {
+        for (int e = tid; e < 3 * (KW - 1) * D; e += NCV) {
           const int s3 = e / ((KW - 1) * D), i = (e / D) % (KW - 1), c = e % D;
           const uint16_t hv =
               hist ? hist[((static_cast<int64_t>(j * (KW - 1) + i) * 3 + s3) * H + h) * D + c] : uint16_t(0);
           *reinterpret_cast<uint16_t*>(raw + (s3 * 2 + (c >> 6)) * Lay::RAWH + sw(i, (c & 63) >> 3) + (c & 7) * 2) = hv;
         }
       }
-      if (k >= 2 && !(ok = pwait(B_EPI0 + slot, ((k - 2) >> 1) & 1))) break;
-      role_sync(1, NP);
-      // ---- P1: gates (warp 0; SFU log and exp: the cumulative log gate is off by at most
-      //      ~3e-5 over a chunk, far below the fp16 rounding of the operands it scales) ----
+      if (k >= 2 && !(ok = cvwait(B_EPI0 + slot, ((k - 2) >> 1) & 1))) break;
+      role_sync(1, NCV);
+      // gates (warp 0; SFU log and exp: the cumulative log gate is off by at most ~3e-5
+      // over a chunk, far below the fp16 rounding of the operands it scales)
       if (warp == 0) {
         const int a0 = 2 * lane, a1 = a0 + 1;
         const float l0 = a0 < n ? __logf(ga[a0]) : 0.f, l1 = a1 < n ? __logf(ga[a1]) : 0.f;
@@ -356,12 +350,14 @@ __global__ void __launch_bounds__(NT, 1)
         ETA[a1] = a1 < n ? ge[a1] : 0.f;
         IG[a0] = __expf(-g0);  // used only when no G of the chunk is below -80 (no overflow)
         IG[a1] = __expf(-g1);
-        tc::mbar_arrive(&bars[B_GATE]);  // the chain scales S by this chunk's decay early
       }
-      //      conv + SiLU: thread = (stream, 8 channels, 8 tokens), a sliding window of raw
-      //      rows (positions u-3..u for token u); fp16 rows into the operand tiles; the
-      //      norms n_q, n_k from sums of squares over the 16 lanes of a token block
-      {
+      // ---- conv + SiLU, stream by stream: thread = (8 channels, 8 tokens), a sliding
+      //      window of raw rows (positions u-3..u for token u); fp16 rows into the operand
+      //      tiles; the norms n_q, n_k from sums of squares over the 16 lanes of a token
+      //      block.  Y_v waits until the solve group's products have read the previous one.
+      for (int st = 0; st < 3 && ok; ++st) {
+        if (st == 2 && k >= 1 && !(ok = cvwait(B_MW, (k - 1) & 1))) break;
+        const float4* cw4 = reinterpret_cast<const float4*>(p.conv_w) + ((static_cast<int64_t>(st) * H + h) * D + 8 * cg);
         const unsigned char* rb = raw + (st * 2 + (cg >> 3)) * Lay::RAWH;
         const int jc = cg & 7;
         unsigned char* dst = st == 2 ? yv + (cg >> 3) * 8192 : yts + (cg >> 3) * 16384;
@@ -417,12 +413,48 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
       }
+      if (!ok) break;
       tc::fence_proxy_async_smem();
-      role_sync(1, NP);
-      // ---- P2: next chunk's loads (the raw buffer is free); [Y_q; Y_k] Y_k^T on the tensor
-      //      cores; meanwhile the norms n_q, n_k ----------------------------------------------
+      role_sync(1, NCV);
+      if (tid == 0) tc::mbar_arrive(&bars[B_CONV]);
+      // the raw rows and the gates' staging are free: next chunk's loads
       if (nsi < seg_end) issue_loads(nsi, nc0);
-      if (tid == 0) {
+      ++k;
+      si = nsi;
+      c0 = nc0;
+    }
+    // drain: a raw-row load still in flight after an abort (the last one issued: its phase
+    // is the barrier's last)
+    if (tid == 0 && !ok && raw_issued > 0) tc::mbar_drain(&bars[B_RAW], (raw_issued - 1) & 1);
+    asm volatile("cp.async.wait_group 0;\n" ::);
+  } else if (warp < (NCV + NSV) / 32) {
+    // ============================ solve group (256 threads) ============================
+    const int stid = tid - NCV;
+    auto swait = [&](int b, uint32_t par) -> bool {
+      return role_and(3, NSV, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
+    };
+    // blocks (0,1) and (2,3) of the fp32 T stay zero (the two-level products read them)
+    for (int e = stid; e < C * C; e += NSV) {
+      const int t = e >> 6, s = e & 63;
+      if ((s >> 4) == (t >> 4) + 1 && (t >> 4) % 2 == 0) tm[t * LDC + s] = 0.f;
+    }
+    bool ok = true;
+    int si = first_seg(seg_first), c0 = 0, k = 0;
+    while (ok && si < seg_end) {
+      const int len = seg_len(si);
+      const int slot = k & 1;
+      float* G = gate(slot, G_G);
+      float* EG = gate(slot, G_EG);
+      float* ETA = gate(slot, G_ETA);
+      float* IG = gate(slot, G_IG);
+      float* NQ = gate(slot, G_NQ);
+      float* NK = gate(slot, G_NK);
+      unsigned char* yts = yt(slot);
+      unsigned char* pb = pbt(slot);
+      // ---- S0: the conv group has produced this chunk's rows, gates and norms; [Y_q; Y_k]
+      //      Y_k^T on the tensor cores --------------------------------------------------
+      if (!(ok = swait(B_CONV, k & 1))) break;
+      if (stid == 0) {
         tc::tc_fence_after();
         constexpr uint32_t id1 = tc::idesc_fp16(128, 64, 0, 0);
         const uint64_t da = tc::sdesc_sw128(tc::smem_u32(yts), 16, 1024);
@@ -434,12 +466,11 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc::mma_commit(&bars[B_M1]);
       }
-      role_sync(1, NP);
-      // ---- P3: P (q rows) and A (k rows) from [Y_q; Y_k] Y_k^T, warps 0-7 ---------------
-      if (!(ok = pwait(B_M1, k & 1))) break;
+      // ---- S1: P (q rows) and A (k rows) from [Y_q; Y_k] Y_k^T ------------------------
+      if (!(ok = swait(B_M1, k & 1))) break;
       tc::tc_fence_after();
-      if (warp < 8) {
-        const int ch = warp >> 2;  // column half
+      {
+        const int ch = (warp - 4) >> 2;  // column half
         const int r = q4 * 32 + lane;
         const int u0 = ch * 32;
         uint32_t v32[32];
@@ -484,10 +515,10 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       tc::tc_fence_before();
-      role_sync(1, NP);
-      // ---- P4: T = (I + A)^{-1} (fp32): diagonal 16x16 blocks, then the others ----------
-      if (tid < 64) {
-        const int bi = tid >> 4, c = tid & 15, base = bi * 16;
+      role_sync(3, NSV);
+      // ---- S2: T = (I + A)^{-1} (fp32): diagonal 16x16 blocks, then the others ----------
+      if (stid < 64) {
+        const int bi = stid >> 4, c = stid & 15, base = bi * 16;
         float xv[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -502,7 +533,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int r = 0; r < 16; ++r) tm[(base + r) * LDC + base + c] = xv[r];
       }
-      role_sync(1, NP);
+      role_sync(3, NSV);
       // Off-diagonal blocks of T in two levels (T_ij = -T_ii A_ij T_jj for a 2 x 2 block
       // lower-triangular matrix): first the 16 x 16 blocks (1,0) and (3,2), then the 32 x 32
       // block T_BA = -T_BB (A_BA T_AA) with T_AA, T_BB the two 32 x 32 diagonal blocks.
@@ -535,17 +566,17 @@ __global__ void __launch_bounds__(NT, 1)
       };
       {
         // level 1: 64 threads, product pr in {0, 1} -> blocks (2pr+1, 2pr); rows 2rp, 2rp+1
-        const int pr = tid >> 5, rp = (tid >> 2) & 7, c4 = (tid & 3) * 4;
+        const int pr = stid >> 5, rp = (stid >> 2) & 7, c4 = (stid & 3) * 4;
         const int bi = 2 * pr + 1, bj = 2 * pr;
         float* yb = tm + 32 + pr * 16;  // Y = A_ij T_jj [16][16] in T's upper-right quarter (free)
-        if (tid < 64) {
+        if (stid < 64) {
           float4 acc[4] = {};
           blk(acc, 2, am + (bi * 16 + 2 * rp) * LDC + bj * 16, tm + (bj * 16) * LDC + bj * 16 + c4, 16);
 #pragma unroll
           for (int i = 0; i < 2; ++i) *reinterpret_cast<float4*>(yb + (2 * rp + i) * LDC + c4) = acc[i];
         }
-        role_sync(1, NP);
-        if (tid < 64) {
+        role_sync(3, NSV);
+        if (stid < 64) {
           float4 acc[4] = {};
           blk(acc, 2, tm + (bi * 16 + 2 * rp) * LDC + bi * 16, yb + c4, 16);
 #pragma unroll
@@ -553,19 +584,19 @@ __global__ void __launch_bounds__(NT, 1)
             *reinterpret_cast<float4*>(tm + (bi * 16 + 2 * rp + i) * LDC + bj * 16 + c4) =
                 make_float4(-acc[i].x, -acc[i].y, -acc[i].z, -acc[i].w);
         }
-        role_sync(1, NP);
+        role_sync(3, NSV);
       }
       {
         // level 2: 64 threads, rows 4rq..4rq+3 x columns c4..c4+3 of the 32 x 32 blocks
-        const int rq = tid >> 3, c4 = (tid & 7) * 4;
-        if (tid < 64) {
+        const int rq = stid >> 3, c4 = (stid & 7) * 4;
+        if (stid < 64) {
           float4 acc[4] = {};
           blk(acc, 4, am + (32 + 4 * rq) * LDC, tm + c4, 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(tm + (4 * rq + i) * LDC + 32 + c4) = acc[i];
         }
-        role_sync(1, NP);
-        if (tid < 64) {
+        role_sync(3, NSV);
+        if (stid < 64) {
           float4 acc[4] = {};
           blk(acc, 4, tm + (32 + 4 * rq) * LDC + 32, tm + 32 + c4, 32);
 #pragma unroll
@@ -573,10 +604,10 @@ __global__ void __launch_bounds__(NT, 1)
             *reinterpret_cast<float4*>(tm + (32 + 4 * rq + i) * LDC + c4) =
                 make_float4(-acc[i].x, -acc[i].y, -acc[i].z, -acc[i].w);
         }
-        role_sync(1, NP);
+        role_sync(3, NSV);
       }
-      // ---- P5: T diag(eta e^G n_k) and T diag(eta) as fp16 tiles (row t, 8 columns each) ----
-      for (int e = tid; e < C * 8; e += NP) {
+      // ---- S3: T diag(eta e^G n_k) and T diag(eta) as fp16 tiles (row t, 8 columns each) ----
+      for (int e = stid; e < C * 8; e += NSV) {
         const int t = e >> 3, g = e & 7;
         const float4 a = *reinterpret_cast<const float4*>(tm + t * LDC + 8 * g);
         const float4 b = *reinterpret_cast<const float4*>(tm + t * LDC + 8 * g + 4);
@@ -596,10 +627,10 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
-      role_sync(1, NP);
-      // ---- P6: W^T = Y_k^T T'^T into the product columns, U~^T = Y_v^T T''^T into this
+      role_sync(3, NSV);
+      // ---- S4: W^T = Y_k^T T'^T into the product columns, U~^T = Y_v^T T''^T into this
       //      slot's U columns (free: the chain finished chunk k-2) ------------------------
-      if (tid == 0) {
+      if (stid == 0) {
         tc::tc_fence_after();
         constexpr uint32_t id4 = tc::idesc_fp16(128, 64, 1, 0);
         const uint64_t dyk = tc::sdesc_sw128(tc::smem_u32(yts + C * 128), 16384, 1024);
@@ -614,13 +645,13 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc::mma_commit(&bars[B_MW]);
       }
-      // ---- P7: -W (fp16) into its tile, free once the chain's products of chunk k-1 that
-      //      read it are done (warps 0-7: lane = channel c, 32 tokens each) ------------------
-      if (!(ok = pwait(B_MW, k & 1))) break;
-      if (k >= 1 && !(ok = pwait(B_MA, (k - 1) & 1))) break;
+      // ---- S5: -W (fp16) into its tile, free once the chain's products of chunk k-1 that
+      //      read it are done (lane = channel c, 32 tokens per thread) ----------------------
+      if (!(ok = swait(B_MW, k & 1))) break;
+      if (k >= 1 && !(ok = swait(B_MA, (k - 1) & 1))) break;
       tc::tc_fence_after();
-      if (warp < 8) {
-        const int ch = warp >> 2;
+      {
+        const int ch = (warp - 4) >> 2;
         const int c = q4 * 32 + lane;
         uint32_t v32[32];
         tc::tmem_ld32(tmem + T_M1 + ch * 32 + lb, v32);
@@ -635,23 +666,23 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
-      role_sync(1, NP);
-      if (tid == 0) tc::mbar_arrive(&bars[B_PREP]);
+      role_sync(3, NSV);
+      if (stid == 0) tc::mbar_arrive(&bars[B_PREP]);
       ++k;
-      si = nsi;
-      c0 = nc0;
+      c0 += C;
+      if (c0 >= len) {
+        si = first_seg(si + 1);
+        c0 = 0;
+      }
     }
-    // drain: own MMAs, and a raw-row load still in flight after an abort (the last one
-    // issued: its phase is the barrier's last)
-    if (tid == 0) {
+    // drain: own MMAs
+    if (stid == 0) {
       tc::mma_commit(&bars[B_FINP]);
       tc::mbar_drain(&bars[B_FINP], 0);
     }
-    if (tid == 32 && !ok && raw_issued > 0) tc::mbar_drain(&bars[B_RAW], (raw_issued - 1) & 1);
-    asm volatile("cp.async.wait_group 0;\n" ::);
   } else {
     // ============================ state chain (128 threads) ============================
-    const int ct = tid - NP;
+    const int ct = tid - NCV - NSV;
     const int v = q4 * 32 + lane;  // row of S (v index) = TMEM lane
     auto cwait = [&](int b, uint32_t par) -> bool {
       return role_and(2, NCH, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
@@ -908,7 +939,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       if (more) {  // the next chunk of this segment: its decay is known once its gates are
-        if (!(ok = cwait(B_GATE, (k + 1) & 1))) break;
+        if (!(ok = cwait(B_CONV, (k + 1) & 1))) break;
         s16_and_scale(gate(slot ^ 1, G_EG)[C - 1]);
       }
       tc::tmem_wait_st();

@@ -141,10 +141,12 @@ class DeviceRound:
         return F.fork_read_status(self.meta)
 
     def launches_per_round(self) -> int:
-        n = 2  # metadata: tables + tokens
+        n = 3 if self.flags & F.FORK_CHECKS else 2  # metadata: tables + tokens (+ checks)
         for a in self.rnd.attn_shapes:
-            # rotary tables + keys (+ queries for the warp-MMA kernel) + attention
-            n += (4 if self.flags & F.FORK_WARP_MMA else 3) if a.rope_theta else 1
+            if self.flags & F.FORK_WARP_MMA:
+                n += 4 if a.rope_theta else 1  # rotary tables + keys + queries + attention
+            else:
+                n += 4 if a.rope_theta else 2  # rotary tables + keys, fp16 values, attention
         return n + 3  # gdn trunk, gdn branches, readout
 
 
