@@ -16,17 +16,20 @@
 // Y itself.
 //
 // One CTA = one trunk (call 1) or a group of up to kQG questions of one request
-// (call 2) x one head; d = 128.  16 warps:
-//   warps 0-11  prep of chunk k+1 (everything above the line "U = ..."):
-//               raw q/k/v rows by TMA (the chunk and the three rows before it, 128-byte
-//               swizzled), thread = (stream, 8 channels, 8 tokens): causal conv + SiLU
-//               with the weights in registers, fp16 rows into the operand tiles, the
-//               L2 norms from sums of squares reduced over a half warp;
-//               gates; [Y_q; Y_k] Y_k^T on the tensor cores -> P (fp16) and A (fp32);
-//               T = (I + A)^{-1} in fp32 (16x16 diagonal blocks by forward substitution,
-//               the rest in two levels); T diag(eta e^G n_k) and T diag(eta) as fp16
-//               tiles; W^T = Y_k^T (T diag(eta e^G n_k))^T and U~^T = Y_v^T (T diag(eta))^T
-//               on the tensor cores; -W as an fp16 tile.
+// (call 2) x one head; d = 128.  16 warps in three roles that work on consecutive chunks
+// (two slots of row tiles, so the roles overlap):
+//   warps 0-3   conv of chunk k+1: raw q/k rows and then v rows by TMA (the chunk and the
+//               three rows before it, 128-byte swizzled; the next chunk's q/k rows are
+//               requested as soon as this chunk's are read), thread = (8 channels,
+//               8 tokens): causal conv + SiLU over a sliding window of unpacked rows with
+//               the weights in registers, fp16 rows into the operand tiles, the L2 norms
+//               from sums of squares reduced over a half warp; the raw gates by cp.async.
+//   warps 4-11  solve of chunk k+1 (everything above the line "U = ..."): the gates
+//               (first warp, while the tensor cores run); [Y_q; Y_k] Y_k^T on the tensor
+//               cores -> P (fp16) and A (fp32); T = (I + A)^{-1} in fp32 (16x16 diagonal
+//               blocks by forward substitution, the rest in two levels); T diag(eta e^G
+//               n_k) and T diag(eta) as fp16 tiles; W^T = Y_k^T (T diag(eta e^G n_k))^T and
+//               U~^T = Y_v^T (T diag(eta))^T on the tensor cores; -W as an fp16 tile.
 //   warps 12-15 state chain of chunk k (thread = TMEM lane = row v of S): U^T = U~^T -
 //               S W^T and X = S Y_q^T (A operand: an fp16 copy of S in tensor memory);
 //               U^T to fp16 twice (plain, and scaled by Gamma_last n_k for the update); X
@@ -56,9 +59,12 @@ constexpr int HR = C + KW - 1;  // raw rows staged per chunk
 constexpr int LDC = C + 4;      // plain 64-wide fp32 tiles
 constexpr int kQG = 4;          // questions per CTA in the branch call
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S (fp32), its fp16 copy, two U slots, X, the prep's product
+// TMEM columns: S (fp32), its fp16 copy, two U slots, X, the prep's product, two scaled
+// fp16 copies of U^T
 constexpr uint32_t T_S = 0, T_S16 = 128, T_X = 320, T_M1 = 384;
 __device__ __forceinline__ uint32_t t_u(int slot) { return 192u + 64u * slot; }
+// U^T diag(Gamma_last n_k) as fp16 pairs (A operand of the state update), per slot
+__device__ __forceinline__ uint32_t t_ug(int slot) { return 448u + 32u * slot; }
 
 struct Lay {
   static constexpr int RAWH = 9216;               // one 64-channel half of a stream's raw rows (HR used)
@@ -72,8 +78,8 @@ struct Lay {
   static constexpr int TPP = TP + 8192;           // T diag(eta)         [64][128 B]
   static constexpr int AM = TPP + 8192;           // A fp32 [64][LDC]
   static constexpr int TM = AM + C * LDC * 4;     // T fp32 [64][LDC]
-  static constexpr int GA = TM + C * LDC * 4;     // raw alpha, eta of the next chunk [2][64]
-  static constexpr int GS = GA + 2 * C * 4;       // per slot [G, EG, GL, ETA, IG, NQ, NK][64]
+  static constexpr int GA = TM + C * LDC * 4;     // raw alpha, eta per slot [2][2][64]
+  static constexpr int GS = GA + 2 * 2 * C * 4;   // per slot [G, EG, GL, ETA, IG, NQ, NK][64]
   static constexpr int SEG = GS + 2 * 7 * C * 4;  // this CTA's segments: start, len, pos0
   static constexpr int BAR = SEG + 64;
   static constexpr int BYTES = BAR + 256;
@@ -86,7 +92,8 @@ static_assert(Lay::YT % 1024 == 0 && Lay::YV % 1024 == 0 && Lay::WT % 1024 == 0 
               "128-byte-swizzled tiles start on 1024-byte boundaries");
 static_assert(HR * 128 <= Lay::RAWH, "raw rows");
 
-enum { B_RAW = 0, B_CONV, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_FINP, B_FINC, B_STALL, B_N };
+enum { B_RAWQK = 0, B_RAWV, B_CONV, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_PF0, B_PF1, B_FINP, B_FINC, B_STALL,
+       B_GATE, B_N };
 enum { G_G = 0, G_EG, G_GL, G_ETA, G_IG, G_NQ, G_NK };
 
 // SFU approximations: 2^x, 1/sqrt(x) (relative error ~2^-22), tanh (~2^-11)
@@ -126,17 +133,6 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-// 32 consecutive fp32 values (16-byte aligned) into registers with 8 vector loads
-__device__ __forceinline__ void ld32f(const float* src, float* dst) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 v = reinterpret_cast<const float4*>(src)[q];
-    dst[4 * q] = v.x;
-    dst[4 * q + 1] = v.y;
-    dst[4 * q + 2] = v.z;
-    dst[4 * q + 3] = v.w;
-  }
-}
 // barrier over the `n` threads of one role; returns true iff every one of them passed ok
 __device__ __forceinline__ bool role_and(int id, int n, bool ok) {
   uint32_t r;
@@ -212,8 +208,7 @@ __global__ void __launch_bounds__(NT, 1)
   unsigned char* tpp = sm + Lay::TPP;
   float* am = reinterpret_cast<float*>(sm + Lay::AM);
   float* tm = reinterpret_cast<float*>(sm + Lay::TM);
-  float* ga = reinterpret_cast<float*>(sm + Lay::GA);
-  float* ge = ga + C;
+  float* ga = reinterpret_cast<float*>(sm + Lay::GA);  // [slot][alpha, eta][64]
   int* segt = reinterpret_cast<int*>(sm + Lay::SEG);  // [kQG][3], read instead of the metadata
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Lay::BAR + B_N * 8);
@@ -225,7 +220,7 @@ __global__ void __launch_bounds__(NT, 1)
   if (tid == 0) {
     // B_STALL is completed by nothing (FORK_TEST_STALL)
     for (int b = 0; b < B_N; ++b)
-      tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1) ? NCH : 1);
+      tc::mbar_init(&bars[b], (b == B_EPI0 || b == B_EPI1 || b == B_PF0 || b == B_PF1) ? NCH : b == B_GATE ? 32 : 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -264,30 +259,40 @@ __global__ void __launch_bounds__(NT, 1)
     };
     // thread = 8-channel group cg (channels 8cg..8cg+7) x block of 8 tokens tb; the 16
     // lanes of a half warp hold the 128 channels of the same 8 tokens
-    const int cg = tid & 15, tb = (tid >> 4) & 7;
+    const int cg = tid & 15, tb = tid >> 4;
     const CUtensorMap* maps[3] = {&qmap, &kmap, &vmap};
-    int raw_issued = 0;
-    auto issue_loads = [&](int s, int cc) {
-      const int st0 = seg_start(s), ln = seg_len(s);
+    int qk_issued = 0, v_issued = 0;
+    // raw rows (the chunk and the three before it; rows outside the tensor read as zero) of
+    // streams [s_lo, s_hi) of a chunk, on barrier b
+    auto issue_rows = [&](int s, int cc, int s_lo, int s_hi, int b) {
       if (tid == 0) {
         tc::fence_proxy_async_smem();  // the rows were last read (and patched) by threads
-        tc::mbar_expect_tx(&bars[B_RAW], 6 * HR * 128);
-#pragma unroll
-        for (int s3 = 0; s3 < 3; ++s3)
+        tc::mbar_expect_tx(&bars[b], (s_hi - s_lo) * 2 * HR * 128);
+        for (int s3 = s_lo; s3 < s_hi; ++s3)
 #pragma unroll
           for (int half = 0; half < 2; ++half)
-            tc::tma_load_3d(raw + (s3 * 2 + half) * Lay::RAWH, maps[s3], &bars[B_RAW], half * 64, h,
-                            st0 + cc - (KW - 1));
+            tc::tma_load_3d(raw + (s3 * 2 + half) * Lay::RAWH, maps[s3], &bars[b], half * 64, h,
+                            seg_start(s) + cc - (KW - 1));
       }
-      ++raw_issued;
-      {
-        const int uu = tid & (C - 1);
-        const bool valid = cc + uu < ln;
-        const float* src =
-            (tid < C ? p.alpha : p.eta) + (static_cast<int64_t>(st0 + (valid ? cc + uu : 0)) * H + h);
-        cp_async4(tid < C ? &ga[uu] : &ge[uu], src, valid);
-      }
+    };
+    // the raw gates of a chunk into its staging slot (read by the solve group)
+    auto issue_gates = [&](int s, int cc, int gslot) {
+      const int st0 = seg_start(s), ln = seg_len(s);
+      const int uu = tid & (C - 1);
+      const bool valid = cc + uu < ln;
+      const float* src = (tid < C ? p.alpha : p.eta) + (static_cast<int64_t>(st0 + (valid ? cc + uu : 0)) * H + h);
+      cp_async4(ga + gslot * 2 * C + (tid < C ? 0 : C) + uu, src, valid);
       asm volatile("cp.async.commit_group;\n" ::);
+    };
+    // history rows of a segment start for streams [s_lo, s_hi): raw inputs before the segment
+    // (the request's conv window for a question or a resumed trunk, else zero)
+    auto patch_history = [&](int s_lo, int s_hi) {
+      for (int e = tid; e < (s_hi - s_lo) * (KW - 1) * D; e += NCV) {
+        const int s3 = s_lo + e / ((KW - 1) * D), i = (e / D) % (KW - 1), c = e % D;
+        const uint16_t hv =
+            hist ? hist[((static_cast<int64_t>(j * (KW - 1) + i) * 3 + s3) * H + h) * D + c] : uint16_t(0);
+        *reinterpret_cast<uint16_t*>(raw + (s3 * 2 + (c >> 6)) * Lay::RAWH + sw(i, (c & 63) >> 3) + (c & 7) * 2) = hv;
+      }
     };
     if (tid == 0) {
       tc::prefetch_tmap(&qmap);
@@ -296,16 +301,17 @@ __global__ void __launch_bounds__(NT, 1)
     }
     bool ok = true;
     int si = first_seg(seg_first), c0 = 0, k = 0;
-    if (si < seg_end) issue_loads(si, 0);
+    if (si < seg_end) {
+      issue_rows(si, 0, 0, 2, B_RAWQK);
+      issue_rows(si, 0, 2, 3, B_RAWV);
+      issue_gates(si, 0, 0);
+      ++qk_issued;
+      ++v_issued;
+    }
     while (ok && si < seg_end) {
       const int len = seg_len(si);
       const int n = min(C, len - c0);
       const int slot = k & 1;
-      float* G = gate(slot, G_G);
-      float* EG = gate(slot, G_EG);
-      float* GL = gate(slot, G_GL);
-      float* ETA = gate(slot, G_ETA);
-      float* IG = gate(slot, G_IG);
       float* NQ = gate(slot, G_NQ);
       float* NK = gate(slot, G_NK);
       unsigned char* yts = yt(slot);
@@ -314,49 +320,30 @@ __global__ void __launch_bounds__(NT, 1)
         nsi = first_seg(si + 1);
         nc0 = 0;
       }
-      // this chunk's rows and gates have landed; history rows of a segment start; the
-      // slot's tiles are free once the chain has finished chunk k-2
-      if (!(ok = cvwait(B_RAW, (raw_issued - 1) & 1))) break;
-      asm volatile("cp.async.wait_group 0;\n" ::);
-      if (c0 == 0) {
-        for (int e = tid; e < 3 * (KW - 1) * D; e += NCV) {
-          const int s3 = e / ((KW - 1) * D), i = (e / D) % (KW - 1), c = e % D;
-          const uint16_t hv =
-              hist ? hist[((static_cast<int64_t>(j * (KW - 1) + i) * 3 + s3) * H + h) * D + c] : uint16_t(0);
-          *reinterpret_cast<uint16_t*>(raw + (s3 * 2 + (c >> 6)) * Lay::RAWH + sw(i, (c & 63) >> 3) + (c & 7) * 2) = hv;
-        }
-      }
+      // this chunk's q, k rows have landed; history rows of a segment start; the slot's tiles
+      // are free once the chain's products of chunk k-2 are done
+      if (!(ok = cvwait(B_RAWQK, (qk_issued - 1) & 1))) break;
+      if (c0 == 0) patch_history(0, 2);
       if (k >= 2 && !(ok = cvwait(B_EPI0 + slot, ((k - 2) >> 1) & 1))) break;
       role_sync(1, NCV);
-      // gates (warp 0; SFU log and exp: the cumulative log gate is off by at most ~3e-5
-      // over a chunk, far below the fp16 rounding of the operands it scales)
-      if (warp == 0) {
-        const int a0 = 2 * lane, a1 = a0 + 1;
-        const float l0 = a0 < n ? __logf(ga[a0]) : 0.f, l1 = a1 < n ? __logf(ga[a1]) : 0.f;
-        float xx = l0 + l1;
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, xx, o);
-          if (lane >= o) xx += y;
-        }
-        const float g1 = xx, g0 = xx - l1;
-        const float glast = __shfl_sync(0xffffffffu, xx, 31);
-        G[a0] = g0;
-        G[a1] = g1;
-        EG[a0] = __expf(g0);
-        EG[a1] = __expf(g1);
-        GL[a0] = __expf(glast - g0);
-        GL[a1] = __expf(glast - g1);
-        ETA[a0] = a0 < n ? ge[a0] : 0.f;
-        ETA[a1] = a1 < n ? ge[a1] : 0.f;
-        IG[a0] = __expf(-g0);  // used only when no G of the chunk is below -80 (no overflow)
-        IG[a1] = __expf(-g1);
-      }
       // ---- conv + SiLU, stream by stream: thread = (8 channels, 8 tokens), a sliding
-      //      window of raw rows (positions u-3..u for token u); fp16 rows into the operand
-      //      tiles; the norms n_q, n_k from sums of squares over the 16 lanes of a token
-      //      block.  Y_v waits until the solve group's products have read the previous one.
+      //      window of raw rows (positions u-3..u for token u), each row unpacked once;
+      //      fp16 rows into the operand tiles; the norms n_q, n_k from sums of squares over
+      //      the 16 lanes of a token block.  Y_v waits until the solve group's products
+      //      have read the previous one.
       for (int st = 0; st < 3 && ok; ++st) {
-        if (st == 2 && k >= 1 && !(ok = cvwait(B_MW, (k - 1) & 1))) break;
+        if (st == 2) {
+          // the q, k rows are read: next chunk's q, k loads; then this chunk's v rows
+          role_sync(1, NCV);
+          if (nsi < seg_end) {
+            issue_rows(nsi, nc0, 0, 2, B_RAWQK);
+            ++qk_issued;
+          }
+          if (!(ok = cvwait(B_RAWV, (v_issued - 1) & 1))) break;
+          if (c0 == 0) patch_history(2, 3);
+          if (k >= 1 && !(ok = cvwait(B_MW, (k - 1) & 1))) break;
+          role_sync(1, NCV);
+        }
         const float4* cw4 = reinterpret_cast<const float4*>(p.conv_w) + ((static_cast<int64_t>(st) * H + h) * D + 8 * cg);
         const unsigned char* rb = raw + (st * 2 + (cg >> 3)) * Lay::RAWH;
         const int jc = cg & 7;
@@ -371,26 +358,34 @@ __global__ void __launch_bounds__(NT, 1)
           cw[e][2] = w.z;
           cw[e][3] = w.w;
         }
-        uint4 xw[KW];
+        float xw[KW][8];  // unpacked raw rows u-3..u of the 8 channels
+        auto unpack = [&](int row, float* x) {
+          const uint4 r4 = *reinterpret_cast<const uint4*>(rb + sw(row, jc));
 #pragma unroll
-        for (int i = 0; i < KW - 1; ++i) xw[i + 1] = *reinterpret_cast<const uint4*>(rb + sw(u0 + i, jc));
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t word = word_of(r4, q);
+            x[2 * q] = bf_lo(word);
+            x[2 * q + 1] = bf_hi(word);
+          }
+        };
+#pragma unroll
+        for (int i = 0; i < KW - 1; ++i) unpack(u0 + i, xw[i + 1]);
         float ssum[8];
 #pragma unroll
         for (int uu = 0; uu < 8; ++uu) {
           const int u = u0 + uu;
 #pragma unroll
-          for (int i = 0; i < KW - 1; ++i) xw[i] = xw[i + 1];
-          xw[KW - 1] = *reinterpret_cast<const uint4*>(rb + sw(u + KW - 1, jc));  // position u
+          for (int i = 0; i < KW - 1; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xw[i][e] = xw[i + 1][e];
+          unpack(u + KW - 1, xw[KW - 1]);  // position u
           float y[8];
           float sq = 0.f;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            float a = 0.f;
+            float a = cw[e][0] * xw[0][e];
 #pragma unroll
-            for (int i = 0; i < KW; ++i) {
-              const uint32_t word = word_of(xw[i], e >> 1);
-              a = fmaf(cw[e][i], (e & 1) ? bf_hi(word) : bf_lo(word), a);
-            }
+            for (int i = 1; i < KW; ++i) a = fmaf(cw[e][i], xw[i][e], a);
             y[e] = u < n ? silu(a) : 0.f;
             sq = fmaf(y[e], y[e], sq);
           }
@@ -414,18 +409,27 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       if (!ok) break;
+      asm volatile("cp.async.wait_group 0;\n" ::);  // this chunk's gates are staged
       tc::fence_proxy_async_smem();
       role_sync(1, NCV);
       if (tid == 0) tc::mbar_arrive(&bars[B_CONV]);
-      // the raw rows and the gates' staging are free: next chunk's loads
-      if (nsi < seg_end) issue_loads(nsi, nc0);
+      // the v rows are read: next chunk's v rows and gates (its gate slot was read by the
+      // solve group for chunk k-1, done before this chunk's conv could start)
+      if (nsi < seg_end) {
+        issue_rows(nsi, nc0, 2, 3, B_RAWV);
+        ++v_issued;
+        issue_gates(nsi, nc0, (k + 1) & 1);
+      }
       ++k;
       si = nsi;
       c0 = nc0;
     }
-    // drain: a raw-row load still in flight after an abort (the last one issued: its phase
-    // is the barrier's last)
-    if (tid == 0 && !ok && raw_issued > 0) tc::mbar_drain(&bars[B_RAW], (raw_issued - 1) & 1);
+    // drain: raw-row loads still in flight after an abort (the last ones issued: their
+    // phases are the barriers' last)
+    if (tid == 0 && !ok) {
+      if (qk_issued > 0) tc::mbar_drain(&bars[B_RAWQK], (qk_issued - 1) & 1);
+      if (v_issued > 0) tc::mbar_drain(&bars[B_RAWV], (v_issued - 1) & 1);
+    }
     asm volatile("cp.async.wait_group 0;\n" ::);
   } else if (warp < (NCV + NSV) / 32) {
     // ============================ solve group (256 threads) ============================
@@ -451,7 +455,7 @@ __global__ void __launch_bounds__(NT, 1)
       float* NK = gate(slot, G_NK);
       unsigned char* yts = yt(slot);
       unsigned char* pb = pbt(slot);
-      // ---- S0: the conv group has produced this chunk's rows, gates and norms; [Y_q; Y_k]
+      // ---- S0: the conv group has produced this chunk's rows, norms and raw gates; [Y_q; Y_k]
       //      Y_k^T on the tensor cores --------------------------------------------------
       if (!(ok = swait(B_CONV, k & 1))) break;
       if (stid == 0) {
@@ -466,11 +470,44 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc::mma_commit(&bars[B_M1]);
       }
-      // ---- S1: P (q rows) and A (k rows) from [Y_q; Y_k] Y_k^T ------------------------
-      if (!(ok = swait(B_M1, k & 1))) break;
+      // ---- S1: P (q rows) and A (k rows) from [Y_q; Y_k] Y_k^T; the P tile of this slot is
+      //      free once the chain has written out chunk k-2's rows (it stages them there)
+      // gates of this chunk (first solve warp, while the product runs; SFU log and exp: the
+      // cumulative log gate is off by at most ~3e-5 over a chunk, far below the fp16
+      // rounding of the operands it scales).  The gate slot is free once the chain has
+      // finished chunk k-2, which it signals after reading chunk k-1's gates: the gate
+      // barrier is never two phases ahead of the chain's waits on it.
+      bool gok = true;
+      if (stid < 32) {
+        if (k >= 2) gok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_PF0 + slot], ((k - 2) >> 1) & 1, abort, p.wait_ns));
+        if (gok) {
+          const float* gas = ga + slot * 2 * C;
+          const int n = min(C, len - c0);
+          const int a0 = 2 * lane, a1 = a0 + 1;
+          const float l0 = a0 < n ? __logf(gas[a0]) : 0.f, l1 = a1 < n ? __logf(gas[a1]) : 0.f;
+          float xx = l0 + l1;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, xx, o);
+            if (lane >= o) xx += y;
+          }
+          const float g1 = xx, g0 = xx - l1;
+          const float glast = __shfl_sync(0xffffffffu, xx, 31);
+          float* GL = gate(slot, G_GL);
+          *reinterpret_cast<float2*>(G + a0) = make_float2(g0, g1);
+          *reinterpret_cast<float2*>(EG + a0) = make_float2(__expf(g0), __expf(g1));
+          *reinterpret_cast<float2*>(GL + a0) = make_float2(__expf(glast - g0), __expf(glast - g1));
+          *reinterpret_cast<float2*>(ETA + a0) = make_float2(a0 < n ? gas[C + a0] : 0.f, a1 < n ? gas[C + a1] : 0.f);
+          // used only when no G of the chunk is below -80 (no overflow)
+          *reinterpret_cast<float2*>(IG + a0) = make_float2(__expf(-g0), __expf(-g1));
+          tc::mbar_arrive(&bars[B_GATE]);  // every lane: each releases its own stores
+        }
+      }
+      if (!(ok = role_and(3, NSV, gok && tc::mbar_wait(&bars[B_M1], k & 1, abort, p.wait_ns)))) break;
+      if (k >= 2 && !(ok = swait(B_PF0 + slot, ((k - 2) >> 1) & 1))) break;
       tc::tc_fence_after();
       {
-        const int ch = (warp - 4) >> 2;  // column half
+        const int ch = (warp - NCV / 32) >> 2;  // column half
         const int r = q4 * 32 + lane;
         const int u0 = ch * 32;
         uint32_t v32[32];
@@ -479,27 +516,24 @@ __global__ void __launch_bounds__(NT, 1)
         const int t = r < C ? r : r - C;
         const float gt = G[t] * kLog2e, egt = EG[t];
         // Gamma_ts = e^{G_t} e^{-G_s} while e^{-G} stays finite (G decreases along the
-        // chunk), else 2^{(G_t - G_s) log2 e} per element
-        const bool prod = G[C - 1] > -80.f;
-        float vals[32], nk[32];
-        ld32f(NK + u0, nk);
-        if (prod) {
-          ld32f(IG + u0, vals);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) vals[e] *= egt;
-        } else {
-          ld32f(G + u0, vals);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) vals[e] = ex2f(gt - vals[e] * kLog2e);
-        }
+        // chunk), else 2^{(G_t - G_s) log2 e} per element.
         // P_ts = n_q,t n_k,s Gamma_ts (Y_q Y_k^T)_ts (s <= t);
         // A_ts = eta_t n_k,t n_k,s Gamma_ts (Y_k Y_k^T)_ts (s < t)
+        const bool prod = G[C - 1] > -80.f;
         const float scale = r < C ? NQ[t] : ETA[t] * NK[t];
         const int lim = r < C ? t : t - 1;
+        float vals[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int s = u0 + e;
-          vals[e] = s <= lim ? scale * nk[e] * vals[e] * __uint_as_float(v32[e]) : 0.f;
+        for (int q = 0; q < 8; ++q) {
+          const float4 nk = *reinterpret_cast<const float4*>(NK + u0 + 4 * q);
+          const float4 gg = *reinterpret_cast<const float4*>((prod ? IG : G) + u0 + 4 * q);
+          const float nkv[4] = {nk.x, nk.y, nk.z, nk.w}, ggv[4] = {gg.x, gg.y, gg.z, gg.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e = 4 * q + i, s2 = u0 + e;
+            const float gam = prod ? egt * ggv[i] : ex2f(gt - ggv[i] * kLog2e);
+            vals[e] = s2 <= lim ? scale * nkv[i] * gam * __uint_as_float(v32[e]) : 0.f;
+          }
         }
         if (r < C) {
 #pragma unroll
@@ -651,7 +685,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (k >= 1 && !(ok = swait(B_MA, (k - 1) & 1))) break;
       tc::tc_fence_after();
       {
-        const int ch = (warp - 4) >> 2;
+        const int ch = (warp - NCV / 32) >> 2;
         const int c = q4 * 32 + lane;
         uint32_t v32[32];
         tc::tmem_ld32(tmem + T_M1 + ch * 32 + lb, v32);
@@ -687,61 +721,48 @@ __global__ void __launch_bounds__(NT, 1)
     auto cwait = [&](int b, uint32_t par) -> bool {
       return role_and(2, NCH, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
     };
-    // 64 fp32 values -> 32 words of fp16 pairs
-    auto pack64 = [&](const uint32_t* a, const uint32_t* b, uint32_t* hv) {
+    // 32 fp32 values -> 16 words of fp16 pairs
+    auto pack32 = [&](const uint32_t* a, uint32_t* hv) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        hv[e] = pack_h2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-        hv[16 + e] = pack_h2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
-      }
+      for (int e = 0; e < 16; ++e) hv[e] = pack_h2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
     };
     // fp16 copy of S (the A operand of the next chunk's first products) and S scaled in
     // place by that chunk's decay e^{G_last} (before its state update), in one pass
     auto s16_and_scale = [&](float egl) {
 #pragma unroll
-      for (int cb = 0; cb < D; cb += 64) {
-        uint32_t a[32], b[32], hv[32];
+      for (int cb = 0; cb < D; cb += 32) {
+        uint32_t a[32], hv[16];
         tc::tmem_ld32(tmem + T_S + cb + lb, a);
-        tc::tmem_ld32(tmem + T_S + cb + 32 + lb, b);
         tc::tmem_wait_ld();
-        pack64(a, b, hv);
-        tc::tmem_st32(tmem + T_S16 + cb / 2 + lb, hv);
+        pack32(a, hv);
+        tc::tmem_st16(tmem + T_S16 + cb / 2 + lb, hv);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          a[e] = __float_as_uint(__uint_as_float(a[e]) * egl);
-          b[e] = __float_as_uint(__uint_as_float(b[e]) * egl);
-        }
+        for (int e = 0; e < 32; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) * egl);
         tc::tmem_st32(tmem + T_S + cb + lb, a);
-        tc::tmem_st32(tmem + T_S + cb + 32 + lb, b);
       }
     };
     // S <- a state from global memory (row v), or zero; and its fp16 copy
     auto load_state = [&](const float* src) {
 #pragma unroll
-      for (int cb = 0; cb < D; cb += 64) {
-        uint32_t a[32], b[32], hv[32];
+      for (int cb = 0; cb < D; cb += 32) {
+        uint32_t a[32], hv[16];
         if (src) {
           const float4* s4 = reinterpret_cast<const float4*>(src + state_base + static_cast<int64_t>(v) * D + cb);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 f = s4[q], g2 = s4[8 + q];
+            const float4 f = s4[q];
             a[4 * q] = __float_as_uint(f.x);
             a[4 * q + 1] = __float_as_uint(f.y);
             a[4 * q + 2] = __float_as_uint(f.z);
             a[4 * q + 3] = __float_as_uint(f.w);
-            b[4 * q] = __float_as_uint(g2.x);
-            b[4 * q + 1] = __float_as_uint(g2.y);
-            b[4 * q + 2] = __float_as_uint(g2.z);
-            b[4 * q + 3] = __float_as_uint(g2.w);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = b[e] = 0u;
+          for (int e = 0; e < 32; ++e) a[e] = 0u;
         }
-        pack64(a, b, hv);
+        pack32(a, hv);
         tc::tmem_st32(tmem + T_S + cb + lb, a);
-        tc::tmem_st32(tmem + T_S + cb + 32 + lb, b);
-        tc::tmem_st32(tmem + T_S16 + cb / 2 + lb, hv);
+        tc::tmem_st16(tmem + T_S16 + cb / 2 + lb, hv);
       }
       tc::tmem_wait_st();
     };
@@ -826,28 +847,26 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
       }
-      {
-        // columns 0-31 of the slot: U^T (s = 0..63, two per column); 32-63: U^T diag(Gamma_last n_k)
-        uint32_t ua[32], ub[32], w32[32];
-        tc::tmem_ld32(tmem + t_u(slot) + lb, ua);
-        tc::tmem_ld32(tmem + t_u(slot) + 32 + lb, ub);
+      // U^T as fp16 pairs in place (columns 0-31 of the slot: s = 0..63, two per column) and
+      // U^T diag(Gamma_last n_k) as fp16 pairs into the slot's scaled copy; 32 columns at a time
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t u32[32], lo[16], hi[16];
+        tc::tmem_ld32(tmem + t_u(slot) + 32 * hh + lb, u32);
         tc::tmem_wait_ld();
+        const float4* gl4 = reinterpret_cast<const float4*>(GL + 32 * hh);
+        const float4* nk4 = reinterpret_cast<const float4*>(NK + 32 * hh);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          w32[e] = pack_h2(__uint_as_float(ua[2 * e]), __uint_as_float(ua[2 * e + 1]));
-          w32[16 + e] = pack_h2(__uint_as_float(ub[2 * e]), __uint_as_float(ub[2 * e + 1]));
-        }
-        tc::tmem_st32(tmem + t_u(slot) + lb, w32);
-        const float4* gl4 = reinterpret_cast<const float4*>(GL);
-        const float4* nk4 = reinterpret_cast<const float4*>(NK);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < 8; ++q) {
           const float4 g = gl4[q], nk = nk4[q];
-          const uint32_t* src = q < 8 ? ua + 4 * q : ub + 4 * (q - 8);
-          w32[2 * q] = pack_h2(__uint_as_float(src[0]) * g.x * nk.x, __uint_as_float(src[1]) * g.y * nk.y);
-          w32[2 * q + 1] = pack_h2(__uint_as_float(src[2]) * g.z * nk.z, __uint_as_float(src[3]) * g.w * nk.w);
+          lo[2 * q] = pack_h2(__uint_as_float(u32[4 * q]), __uint_as_float(u32[4 * q + 1]));
+          lo[2 * q + 1] = pack_h2(__uint_as_float(u32[4 * q + 2]), __uint_as_float(u32[4 * q + 3]));
+          hi[2 * q] = pack_h2(__uint_as_float(u32[4 * q]) * g.x * nk.x, __uint_as_float(u32[4 * q + 1]) * g.y * nk.y);
+          hi[2 * q + 1] =
+              pack_h2(__uint_as_float(u32[4 * q + 2]) * g.z * nk.z, __uint_as_float(u32[4 * q + 3]) * g.w * nk.w);
         }
-        tc::tmem_st32(tmem + t_u(slot) + 32 + lb, w32);
+        tc::tmem_st16(tmem + t_u(slot) + 16 * hh + lb, lo);  // the columns just read
+        tc::tmem_st16(tmem + t_ug(slot) + 16 * hh + lb, hi);
       }
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -895,7 +914,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (need_state)
 #pragma unroll
           for (int ks = 0; ks < C / 16; ++ks)
-            tc::mma_f16_ts(tmem + T_S, tmem + t_u(slot) + 32 + ks * 8, dk + static_cast<uint64_t>(ks * (2048 / 16)),
+            tc::mma_f16_ts(tmem + T_S, tmem + t_ug(slot) + ks * 8, dk + static_cast<uint64_t>(ks * (2048 / 16)),
                            id6, 1u);
         tc::mma_commit(&bars[B_MB]);
       }
@@ -905,6 +924,8 @@ __global__ void __launch_bounds__(NT, 1)
       //      rows are rotated by 64 bytes so the two tokens of one store use different banks.
       if (!(ok = cwait(B_MB, k & 1))) break;
       tc::tc_fence_after();
+      // the products of this chunk are done: its row tiles, gates and U slot are free
+      tc::mbar_arrive(&bars[B_EPI0 + slot]);
       {
         const bool odd = lane & 1;
         const int v0 = v & ~1;
@@ -939,12 +960,12 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       if (more) {  // the next chunk of this segment: its decay is known once its gates are
-        if (!(ok = cwait(B_CONV, (k + 1) & 1))) break;
+        if (!(ok = cwait(B_GATE, (k + 1) & 1))) break;
         s16_and_scale(gate(slot ^ 1, G_EG)[C - 1]);
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
-      tc::mbar_arrive(&bars[B_EPI0 + slot]);
+      tc::mbar_arrive(&bars[B_PF0 + slot]);  // the P tile (output staging) is free
       ++k;
       c0 += C;
       if (c0 >= len) {
