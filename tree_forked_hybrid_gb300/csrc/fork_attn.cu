@@ -203,16 +203,27 @@ static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hk
 }
 
 // Values of the stream rows [0, T) and of the prefix rows as fp16 (8 elements per thread).
+// The rows [T, min(T_cap, T + 128)) of the copy are set to zero: a key tile that starts
+// inside the stream reads at most 127 rows past its range, and rows past T are not the
+// caller's data (any bits), while the products need finite values there (p = 0 and
+// 0 * NaN is not 0).  Rows past T_cap read as zero from the tensor map.
 __global__ void __launch_bounds__(256) v_half_kernel(const int32_t* __restrict__ meta, const uint16_t* __restrict__ v,
                                                      const uint16_t* __restrict__ pv, uint16_t* __restrict__ vh,
-                                                     uint16_t* __restrict__ pvh, int64_t row_elems, int prefix_rows) {
+                                                     uint16_t* __restrict__ pvh, int64_t row_elems, int prefix_rows,
+                                                     int T_cap) {
   if (meta[H_VALID] == 0) return;
-  const int64_t n_stream = static_cast<int64_t>(meta[H_T]) * row_elems / 8;
-  const int64_t n_all = n_stream + static_cast<int64_t>(prefix_rows) * row_elems / 8;
+  const int T = meta[H_T];
+  const int64_t n_stream = static_cast<int64_t>(T) * row_elems / 8;
+  const int64_t n_zero = n_stream + static_cast<int64_t>(min(T_cap, T + 128) - T) * row_elems / 8;
+  const int64_t n_all = n_zero + static_cast<int64_t>(prefix_rows) * row_elems / 8;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_all;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (i >= n_stream && i < n_zero) {
+      reinterpret_cast<uint4*>(vh)[i] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
     const bool st = i < n_stream;
-    const uint4 x = st ? reinterpret_cast<const uint4*>(v)[i] : reinterpret_cast<const uint4*>(pv)[i - n_stream];
+    const uint4 x = st ? reinterpret_cast<const uint4*>(v)[i] : reinterpret_cast<const uint4*>(pv)[i - n_zero];
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     uint32_t o[4];
 #pragma unroll
@@ -221,7 +232,7 @@ __global__ void __launch_bounds__(256) v_half_kernel(const int32_t* __restrict__
       o[e] = *reinterpret_cast<const uint32_t*>(&hh);
     }
     const uint4 y = make_uint4(o[0], o[1], o[2], o[3]);
-    if (st) reinterpret_cast<uint4*>(vh)[i] = y; else reinterpret_cast<uint4*>(pvh)[i - n_stream] = y;
+    if (st) reinterpret_cast<uint4*>(vh)[i] = y; else reinterpret_cast<uint4*>(pvh)[i - n_zero] = y;
   }
 }
 
@@ -327,7 +338,8 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     const int64_t row_elems = static_cast<int64_t>(Hkv) * d;
     const int64_t n8 = (static_cast<int64_t>(L.T_cap) + p.prefix_rows) * row_elems / 8;
     const int blocks = static_cast<int>(std::min<int64_t>((n8 + 255) / 256, 8 * sm_count()));
-    v_half_kernel<<<std::max(blocks, 1), 256, 0, s>>>(p.meta, v, prefix_v, vh, pvh, row_elems, p.prefix_rows);
+    v_half_kernel<<<std::max(blocks, 1), 256, 0, s>>>(p.meta, v, prefix_v, vh, pvh, row_elems, p.prefix_rows,
+                                                      L.T_cap);
     vtc = vh;
     pvtc = pvh;
   }

@@ -14,14 +14,15 @@
 //
 // One CTA = one work item x one kv head = up to two 128-row query tiles
 // (rows = token x grouped head) that share every K/V tile, 10 warps:
-//   warp 8 (one lane)   TMA producer: both Q tiles once, then K and V tiles
+//   warp 1 (one lane)   TMA producer: both Q tiles once, then K and V tiles
 //                       into two 2-stage rings (K and V slots are freed by
 //                       their own readers);
-//   warp 9              MMA issuer (lane 0) and TMEM owner.  Per key tile j,
+//   warp 0              MMA issuer (lane 0) and TMEM owner.  Per key tile j,
 //                       for each query tile t: O_t += P_t(j-1) V(j-1), then
 //                       S_t = Q_t K(j)^T; the two tiles alternate so one
 //                       tile's softmax overlaps the other tile's products;
-//   warps 0-3 / 4-7     softmax of tile 0 / tile 1, one query row per thread:
+//   warps 2-5 / 6-9     softmax of tile 0 / tile 1, one query row per thread
+//                       (warp w reads TMEM lanes 32 (w mod 4) ..; row = tid mod 128):
 //                       S from TMEM, mask, online softmax in the log2 domain
 //                       (the running maximum only moves when it grows by more
 //                       than 2^8, so O is rescaled rarely), P as bf16 written
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 12; ++i) rtab[i] = tab[i];
     tc::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 0) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sK = smem + LY::K;
   unsigned char* sV = smem + LY::V;
 
-  if (warp == 8) {
+  if (warp == 1) {
     // ===================== TMA producer =====================
     if (lane == 0) {
       tc::prefetch_tmap(&qmap);
@@ -311,106 +312,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int f = max(0, issued - kVStages); f < issued; ++f)
         tc::mbar_drain(&bars[B_VFULL0 + f % kVStages], (f / kVStages) & 1);
     }
-  } else if (warp == 9) {
-    // ===================== MMA issuer =====================
-    constexpr uint32_t idesc_qk = tc::idesc_bf16(128, kKeys, 0, 0);
-    constexpr uint32_t idesc_pv = tc::idesc_fp16(128, D, 0, 1);  // P and V fp16
-    // descriptors are built once; the start-address field (16-byte units) is then
-    // advanced by constants: +2 per 32-byte k step, +kBox/16 per box
-    const uint64_t dq = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
-    const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
-    const uint64_t dv = tc::sdesc_sw128(tc::smem_u32(sV), kBox, 1024);
-    constexpr uint64_t kBoxU = kBox / 16, kStageU = NB * kBox / 16;
-    // every lane waits; the warp proceeds only if all of them saw the phase complete
-    auto wwait = [&](int b, uint32_t par) -> bool {
-      return __all_sync(0xffffffffu, tc::mbar_wait(&bars[b], par, abort, p.wait_ns)) != 0;
-    };
-    bool ok = !p.stall || wwait(B_STALL, 0);  // FORK_TEST_STALL: runs out, nothing is issued
-    ok = ok && wwait(p.rotate_q ? B_QROT : B_QFULL, 0);
-    const int last_tile = total - 1;
-    // V tile f ready for the PV products; a range that ends inside the tile is followed by
-    // rows that may be pad rows of the stream (any bits), zeroed here: their p is 0 but
-    // 0 * NaN would not be
-    auto v_ready = [&](int f) -> bool {
-      const int st = f % kVStages;
-      if (!wwait(B_VFULL0 + st, (f / kVStages) & 1)) return false;
-      const KT kt = key_tile(f);
-      const int valid_rows = kt.len - kt.t * kKeys;
-      if (kt.r != 0 && valid_rows < kKeys && kt.row0 + kt.t * kKeys + kKeys > meta[H_T]) {
-        // rows [valid_rows, 128) of this slot
-        for (int e = lane; e < (kKeys - valid_rows) * NB * 8; e += 32) {
-          const int r = valid_rows + e / (NB * 8), b = (e / 8) % NB, q = e % 8;
-          *reinterpret_cast<uint4*>(sV + (st * NB + b) * kBox + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
-        }
-        tc::fence_proxy_async_smem();
-      }
-      __syncwarp();
-      return true;
-    };
-    auto issue_pv = [&](int t, int f) {
-      const int st = f % kVStages;
-      const uint32_t a = tm_s(t);
+  } else if (warp == 0) {
+    // ===================== MMA issuer (lane 0 alone) =====================
+    // The loop is kept short: the issuing thread shares its scheduler with two softmax
+    // warps, and every instruction between two groups of products leaves the tensor
+    // cores idle.  Pad rows past the stream end are zero in the value copy, so V tiles
+    // need no fix-up here.
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_bf16(128, kKeys, 0, 0);
+      constexpr uint32_t idesc_pv = tc::idesc_fp16(128, D, 0, 1);  // P and V fp16
+      // descriptors are built once; the start-address field (16-byte units, low word) is
+      // then advanced by constants: +2 per 32-byte k step, +kBox/16 per box
+      const uint64_t dq = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
+      const uint64_t dk = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
+      const uint64_t dv = tc::sdesc_sw128(tc::smem_u32(sV), kBox, 1024);
+      constexpr uint64_t kBoxU = kBox / 16, kStageU = NB * kBox / 16;
+      auto wait = [&](int b, uint32_t par) -> bool { return tc::mbar_wait(&bars[b], par, abort, p.wait_ns); };
+      auto issue_pv = [&](int t, int f) {
+        const uint32_t a = tm_s(t);
+        const uint64_t d0 = dv + (f % kVStages) * kStageU;
 #pragma unroll
-      for (int step = 0; step < kKeys / 16; ++step)
-        mma_bf16_ts(tm_o(t), a + step * 8, dv + st * kStageU + step * (2048 / 16), idesc_pv,
-                    (f > 0 || step > 0) ? 1u : 0u);
-    };
-    auto issue_qk = [&](int t, int f) {
-      const int st = f & 1;
+        for (int step = 0; step < kKeys / 16; ++step)
+          mma_bf16_ts(tm_o(t), a + step * 8, d0 + step * (2048 / 16), idesc_pv, (f > 0 || step > 0) ? 1u : 0u);
+      };
+      auto issue_qk = [&](int t, int f) {
+        const uint64_t a0 = dq + t * NB * kBoxU, b0 = dk + (f & 1) * kStageU;
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
+        for (int b = 0; b < NB; ++b)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tm_s(t), dq + (t * NB + b) * kBoxU + k * 2, dk + st * kStageU + b * kBoxU + k * 2,
-                       idesc_qk, (b | k) ? 1u : 0u);
-    };
-    for (int f = 0; ok && f < total; ++f) {
-      const int st = f & 1;
-      if (!wwait(B_KFULL0 + st, (f >> 1) & 1)) { ok = false; break; }
-      if (f > 0 && !v_ready(f - 1)) { ok = false; break; }
-      for (int t = 0; t < ntiles; ++t) {
-        // P_t(f-1) is in the TMEM columns of S_t: the products read it before S_t is rewritten
-        // (tcgen05 MMAs of one thread execute in issue order)
-        if (f > 0) {
-          if (!wwait(B_PFULL0 + t, (f - 1) & 1)) { ok = false; break; }
-          tc::tc_fence_after();
-          if (lane == 0) {
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16(tm_s(t), a0 + b * kBoxU + k * 2, b0 + b * kBoxU + k * 2, idesc_qk, (b | k) ? 1u : 0u);
+      };
+      bool ok = !p.stall || wait(B_STALL, 0);  // FORK_TEST_STALL: runs out, nothing is issued
+      ok = ok && wait(p.rotate_q ? B_QROT : B_QFULL, 0);
+      for (int f = 0; ok && f < total; ++f) {
+        const int st = f & 1;
+        ok = wait(B_KFULL0 + st, (f >> 1) & 1) && (f == 0 || wait(B_VFULL0 + (f - 1) % kVStages, ((f - 1) / kVStages) & 1));
+        for (int t = 0; ok && t < ntiles; ++t) {
+          // P_t(f-1) is in the TMEM columns of S_t: the products read it before S_t is
+          // rewritten (tcgen05 MMAs of one thread execute in issue order)
+          if (f > 0) {
+            if (!(ok = wait(B_PFULL0 + t, (f - 1) & 1))) break;
+            tc::tc_fence_after();
             issue_pv(t, f - 1);
             // V_{f-1} has no reader after the last tile's PV products: its slot is
             // released before the next QK^T products are queued behind them
             if (t == ntiles - 1) tc::mma_commit(&bars[B_VEMPTY0 + (f - 1) % kVStages]);
           }
-        }
-        if (lane == 0) {
           issue_qk(t, f);
           tc::mma_commit(&bars[B_SFULL0 + t]);
         }
-        __syncwarp();
+        if (ok) tc::mma_commit(&bars[B_KEMPTY0 + st]);
       }
-      if (!ok) break;
-      if (lane == 0) tc::mma_commit(&bars[B_KEMPTY0 + st]);
-      __syncwarp();
-    }
-    if (ok && v_ready(last_tile)) {
-      for (int t = 0; t < ntiles; ++t) {
-        if (!wwait(B_PFULL0 + t, last_tile & 1)) break;
-        tc::tc_fence_after();
-        if (lane == 0) {
+      const int last_tile = total - 1;
+      if (ok && wait(B_VFULL0 + last_tile % kVStages, (last_tile / kVStages) & 1)) {
+        for (int t = 0; t < ntiles; ++t) {
+          if (!wait(B_PFULL0 + t, last_tile & 1)) break;
+          tc::tc_fence_after();
           issue_pv(t, last_tile);
           tc::mma_commit(&bars[B_OFULL0 + t]);
         }
-        __syncwarp();
       }
+      // every MMA issued by this thread has completed before TMEM is released (also after
+      // an abort: the products already issued finish by themselves)
+      tc::mma_commit(&bars[B_FIN]);
+      tc::mbar_drain(&bars[B_FIN], 0);
     }
-    // every MMA issued by this warp has completed before TMEM is released (also after an
-    // abort: the products already issued finish by themselves)
-    if (lane == 0) tc::mma_commit(&bars[B_FIN]);
-    __syncwarp();
-    tc::mbar_drain(&bars[B_FIN], 0);
     __syncwarp();
   } else {
-    // ===================== softmax warpgroups (tile t = warp / 4, row = tid % 128) ==========
-    const int t = warp >> 2;
+    // ===================== softmax warpgroups (tile t = (warp - 2) / 4, row = tid % 128) ====
+    const int t = (warp - 2) >> 2;
     if (p.rotate_q) {
       // rotary embedding of the query tiles in shared memory, thread = row, once they have
       // landed; the products read them after every thread's fence and arrival.  The row's
@@ -572,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   if (*abort && tid == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_TIMEOUT);
-  if (warp == 9) {
+  if (warp == 0) {
     __syncwarp();
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
