@@ -47,7 +47,8 @@ constexpr int kBox = 128 * 128;  // bytes of one 128-row x 64-element bf16 box
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescale = 8.f;  // move the running max only when it grows by > 2^8
-constexpr int kVStages = 2;      // V ring depth (a third slot measured no faster)
+constexpr int kVStages = 2;      // V ring depth = K ring depth (a third slot measured no faster)
+static_assert(kVStages == 2, "K and V tiles share the slot barriers");
 
 template <int D>
 struct TcLayout {
@@ -60,8 +61,9 @@ struct TcLayout {
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);  // one CTA per SM
 };
 
-enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_VFULL2, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
-           B_VEMPTY1, B_VEMPTY2, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_QROT,
+// B_KVFULLs: K and V tile f both landed in slot s = f mod 2 (one wait for the issuer)
+enum Bar { B_QFULL = 0, B_KVFULL0, B_KVFULL1, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
+           B_VEMPTY1, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_QROT,
            B_STALL, B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -239,12 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     tc::mbar_init(&bars[B_QFULL], 1);
-    for (int k = 0; k < kVStages; ++k) {
-      tc::mbar_init(&bars[B_VFULL0 + k], 1);
-      tc::mbar_init(&bars[B_VEMPTY0 + k], 1);
-    }
+    for (int k = 0; k < kVStages; ++k) tc::mbar_init(&bars[B_VEMPTY0 + k], 1);
     for (int k = 0; k < 2; ++k) {
-      tc::mbar_init(&bars[B_KFULL0 + k], 1);
+      tc::mbar_init(&bars[B_KVFULL0 + k], 1);
       tc::mbar_init(&bars[B_KEMPTY0 + k], 1);
       tc::mbar_init(&bars[B_SFULL0 + k], 1);
       tc::mbar_init(&bars[B_PFULL0 + k], 128);
@@ -288,29 +287,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_load_3d(sQ + (t * NB + b) * kBox, &qmap, &bars[B_QFULL], b * 64, g * G,
                           seg_start + off + t * tile);
       // K_f waits for the QK^T products of K_{f-2} (its slot's previous reader), V_f for
-      // the PV products of V_{f-kVStages}
+      // the PV products of V_{f-2}; both land on the slot's one barrier, whose phase also
+      // needs the arrival made after both copies were issued
       int issued = 0;
       for (int f = 0; f < total; ++f) {
-        const int st = f & 1, vs = f % kVStages;
+        const int st = f & 1;
         const KT kt = key_tile(f);
         const CUtensorMap* km = kt.r == 0 ? &pkmap : &kmap;
         const CUtensorMap* vm = kt.r == 0 ? &pvmap : &vmap;
         const int row = kt.row0 + kt.t * kKeys;
         if (f >= 2 && !tc::mbar_wait(&bars[B_KEMPTY0 + st], ((f >> 1) - 1) & 1, abort, p.wait_ns)) break;
-        tc::mbar_expect_tx(&bars[B_KFULL0 + st], NB * kBox);
-        for (int b = 0; b < NB; ++b) tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KFULL0 + st], b * 64, g, row);
-        if (f >= kVStages && !tc::mbar_wait(&bars[B_VEMPTY0 + vs], ((f / kVStages) - 1) & 1, abort, p.wait_ns))
-          break;
-        tc::mbar_expect_tx(&bars[B_VFULL0 + vs], NB * kBox);
-        for (int b = 0; b < NB; ++b) tc::tma_load_3d(sV + (vs * NB + b) * kBox, vm, &bars[B_VFULL0 + vs], b * 64, g, row);
+        tc::mbar_expect_tx_only(&bars[B_KVFULL0 + st], NB * kBox);
+        for (int b = 0; b < NB; ++b) tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KVFULL0 + st], b * 64, g, row);
         issued = f + 1;
+        const bool vok = f < 2 || tc::mbar_wait(&bars[B_VEMPTY0 + st], ((f >> 1) - 1) & 1, abort, p.wait_ns);
+        if (vok) {
+          tc::mbar_expect_tx_only(&bars[B_KVFULL0 + st], NB * kBox);
+          for (int b = 0; b < NB; ++b) tc::tma_load_3d(sV + (st * NB + b) * kBox, vm, &bars[B_KVFULL0 + st], b * 64, g, row);
+        }
+        tc::mbar_arrive(&bars[B_KVFULL0 + st]);  // after an abort: the phase ends with the K copy
+        if (!vok) break;
       }
-      // drain: the Q tiles and the last loads issued into each slot complete by themselves
-      // (no load is issued into a slot after them, so their phases are the slots' last)
+      // drain: the Q tiles and the last copies issued into each slot complete by themselves
+      // (no copy is issued into a slot after them, so their phases are the slots' last)
       tc::mbar_drain(&bars[B_QFULL], 0);
-      for (int f = max(0, issued - 2); f < issued; ++f) tc::mbar_drain(&bars[B_KFULL0 + (f & 1)], (f >> 1) & 1);
-      for (int f = max(0, issued - kVStages); f < issued; ++f)
-        tc::mbar_drain(&bars[B_VFULL0 + f % kVStages], (f / kVStages) & 1);
+      for (int f = max(0, issued - 2); f < issued; ++f) tc::mbar_drain(&bars[B_KVFULL0 + (f & 1)], (f >> 1) & 1);
     }
   } else if (warp == 0) {
     // ===================== MMA issuer (lane 0 alone) =====================
@@ -345,9 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = !p.stall || wait(B_STALL, 0);  // FORK_TEST_STALL: runs out, nothing is issued
       ok = ok && wait(p.rotate_q ? B_QROT : B_QFULL, 0);
+      // per key tile f: O_0 += P_0(f-1) V(f-1), S_0 = Q_0 K(f)^T, O_1 += P_1(f-1) V(f-1),
+      // S_1 = Q_1 K(f)^T.  The wait for K(f), V(f) sits after the first PV products rather
+      // than after QK^T products, whose operand reads fill shared memory and slow the wait.
       for (int f = 0; ok && f < total; ++f) {
         const int st = f & 1;
-        ok = wait(B_KFULL0 + st, (f >> 1) & 1) && (f == 0 || wait(B_VFULL0 + (f - 1) % kVStages, ((f - 1) / kVStages) & 1));
         for (int t = 0; ok && t < ntiles; ++t) {
           // P_t(f-1) is in the TMEM columns of S_t: the products read it before S_t is
           // rewritten (tcgen05 MMAs of one thread execute in issue order)
@@ -359,13 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // released before the next QK^T products are queued behind them
             if (t == ntiles - 1) tc::mma_commit(&bars[B_VEMPTY0 + (f - 1) % kVStages]);
           }
+          if (t == 0 && !(ok = wait(B_KVFULL0 + st, (f >> 1) & 1))) break;  // K(f) and V(f)
           issue_qk(t, f);
           tc::mma_commit(&bars[B_SFULL0 + t]);
         }
         if (ok) tc::mma_commit(&bars[B_KEMPTY0 + st]);
       }
       const int last_tile = total - 1;
-      if (ok && wait(B_VFULL0 + last_tile % kVStages, (last_tile / kVStages) & 1)) {
+      if (ok) {
         for (int t = 0; t < ntiles; ++t) {
           if (!wait(B_PFULL0 + t, last_tile & 1)) break;
           tc::tc_fence_after();
