@@ -18,12 +18,12 @@
 // One CTA = one trunk (call 1) or a group of up to kQG questions of one request
 // (call 2) x one head; d = 128.  16 warps in three roles that work on consecutive chunks
 // (two slots of row tiles, so the roles overlap):
-//   warps 0-3   conv of chunk k+1: raw q/k rows and then v rows by TMA (the chunk and the
-//               three rows before it, 128-byte swizzled; the next chunk's q/k rows are
-//               requested as soon as this chunk's are read), thread = (8 channels,
-//               8 tokens): causal conv + SiLU over a sliding window of unpacked rows with
-//               the weights in registers, fp16 rows into the operand tiles, the L2 norms
-//               from sums of squares reduced over a half warp; the raw gates by cp.async.
+//   warps 0-3   conv of chunk k+1 for q and k: raw rows by TMA (the chunk and the three
+//               rows before it, 128-byte swizzled; the next chunk's rows are requested as
+//               soon as this chunk's are read), thread = (8 channels, 8 tokens): causal
+//               conv + SiLU over a sliding window of unpacked rows with the weights in
+//               registers, fp16 rows into the operand tiles, the L2 norms from sums of
+//               squares reduced over a half warp; the raw gates by cp.async.
 //   warps 4-11  solve of chunk k+1 (everything above the line "U = ..."): the gates
 //               (first warp, while the tensor cores run); [Y_q; Y_k] Y_k^T on the tensor
 //               cores -> P (fp16) and A (fp32); T = (I + A)^{-1} in fp32 (16x16 diagonal
@@ -35,6 +35,8 @@
 //               U^T to fp16 twice (plain, and scaled by Gamma_last n_k for the update); X
 //               scaled by e^G n_q; S by e^{G_last}; then O^T = X + U^T P^T and
 //               S += (U^T diag(Gamma_last n_k)) Y_k; output rows; the fp16 copy of S.
+//               Between its chunks the chain makes Y_v of chunk k+1 (the same conv as
+//               above, on its own raw rows), which the solve group's U~ product waits for.
 // S (128 x 128 fp32) stays in tensor memory for the whole segment.  Operands are fp16
 // (10-bit mantissa, as TF32; the values stay far inside the fp16 range), products
 // accumulate in fp32, T is formed in fp32.  Every wait is bounded and agreed by the
@@ -93,7 +95,7 @@ static_assert(Lay::YT % 1024 == 0 && Lay::YV % 1024 == 0 && Lay::WT % 1024 == 0 
 static_assert(HR * 128 <= Lay::RAWH, "raw rows");
 
 enum { B_RAWQK = 0, B_RAWV, B_CONV, B_M1, B_MW, B_PREP, B_MA, B_MB, B_EPI0, B_EPI1, B_PF0, B_PF1, B_FINP, B_FINC, B_STALL,
-       B_GATE, B_N };
+       B_GATE, B_YV, B_N };
 enum { G_G = 0, G_EG, G_GL, G_ETA, G_IG, G_NQ, G_NK };
 
 // SFU approximations: 2^x, 1/sqrt(x) (relative error ~2^-22), tanh (~2^-11)
@@ -252,29 +254,109 @@ __global__ void __launch_bounds__(NT, 1)
     return s;
   };
 
+  // ---- raw rows and the causal conv, shared by the conv group (q, k) and the chain (v) ----
+  const CUtensorMap* maps[3] = {&qmap, &kmap, &vmap};
+  // raw rows (the chunk and the three before it; rows outside the tensor read as zero) of
+  // streams [s_lo, s_hi) of a chunk, on barrier b (one thread)
+  auto issue_rows = [&](int s, int cc, int s_lo, int s_hi, int b) {
+    tc::fence_proxy_async_smem();  // the rows were last read (and patched) by threads
+    tc::mbar_expect_tx(&bars[b], (s_hi - s_lo) * 2 * HR * 128);
+    for (int s3 = s_lo; s3 < s_hi; ++s3)
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+        tc::tma_load_3d(raw + (s3 * 2 + half) * Lay::RAWH, maps[s3], &bars[b], half * 64, h, seg_start(s) + cc - (KW - 1));
+  };
+  // history rows of a segment start for streams [s_lo, s_hi), by the 128 threads r of a
+  // role: raw inputs before the segment (the request's conv window for a question or a
+  // resumed trunk, else zero)
+  auto patch_history = [&](int r, int s_lo, int s_hi) {
+    for (int e = r; e < (s_hi - s_lo) * (KW - 1) * D; e += 128) {
+      const int s3 = s_lo + e / ((KW - 1) * D), i = (e / D) % (KW - 1), c = e % D;
+      const uint16_t hv =
+          hist ? hist[((static_cast<int64_t>(j * (KW - 1) + i) * 3 + s3) * H + h) * D + c] : uint16_t(0);
+      *reinterpret_cast<uint16_t*>(raw + (s3 * 2 + (c >> 6)) * Lay::RAWH + sw(i, (c & 63) >> 3) + (c & 7) * 2) = hv;
+    }
+  };
+  // conv + SiLU of stream st over a chunk with n valid tokens, by the 128 threads r of a
+  // role: thread = 8-channel group cg (channels 8cg..8cg+7) x block of 8 tokens tb (the 16
+  // lanes of a half warp hold the 128 channels of the same 8 tokens), a sliding window of
+  // raw rows (positions u-3..u for token u), each row unpacked once; fp16 rows into box
+  // (cg / 8) of `tile` (boxes of box_bytes, rows row0 + u); for q and k the norm
+  // (sum_c y^2 + 1e-6)^(-1/2) of each token into nrm, from sums of squares over the 16
+  // lanes of a token block
+  auto conv_stream = [&](int r, int st, int n, unsigned char* tile, int box_bytes, int row0, float* nrm) {
+    const int cg = r & 15, tb = r >> 4;
+    const float4* cw4 = reinterpret_cast<const float4*>(p.conv_w) + ((static_cast<int64_t>(st) * H + h) * D + 8 * cg);
+    const unsigned char* rb = raw + (st * 2 + (cg >> 3)) * Lay::RAWH;
+    const int jc = cg & 7;
+    unsigned char* dst = tile + (cg >> 3) * box_bytes;
+    const int u0 = tb * 8;
+    float cw[8][KW];  // the group's conv weights (8 channels x 4 taps), L1-resident
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float4 w = __ldg(cw4 + e);
+      cw[e][0] = w.x;
+      cw[e][1] = w.y;
+      cw[e][2] = w.z;
+      cw[e][3] = w.w;
+    }
+    float xw[KW][8];  // unpacked raw rows u-3..u of the 8 channels
+    auto unpack = [&](int row, float* x) {
+      const uint4 r4 = *reinterpret_cast<const uint4*>(rb + sw(row, jc));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t word = word_of(r4, q);
+        x[2 * q] = bf_lo(word);
+        x[2 * q + 1] = bf_hi(word);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < KW - 1; ++i) unpack(u0 + i, xw[i + 1]);
+    float ssum[8];
+#pragma unroll
+    for (int uu = 0; uu < 8; ++uu) {
+      const int u = u0 + uu;
+#pragma unroll
+      for (int i = 0; i < KW - 1; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xw[i][e] = xw[i + 1][e];
+      unpack(u + KW - 1, xw[KW - 1]);  // position u
+      float y[8];
+      float sq = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float a = cw[e][0] * xw[0][e];
+#pragma unroll
+        for (int i = 1; i < KW; ++i) a = fmaf(cw[e][i], xw[i][e], a);
+        y[e] = u < n ? silu(a) : 0.f;
+        sq = fmaf(y[e], y[e], sq);
+      }
+      ssum[uu] = sq;
+      *reinterpret_cast<uint4*>(dst + sw(row0 + u, jc)) =
+          make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
+    }
+    if (nrm) {
+#pragma unroll
+      for (int uu = 0; uu < 8; ++uu) {
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) ssum[uu] += __shfl_xor_sync(0xffffffffu, ssum[uu], o);
+      }
+      if (cg < 8) {
+        float sv = ssum[0];
+#pragma unroll
+        for (int uu = 1; uu < 8; ++uu)
+          if (cg == uu) sv = ssum[uu];
+        nrm[u0 + cg] = rsqrtf_(sv + 1e-6f);
+      }
+    }
+  };
+
   if (warp < NCV / 32) {
-    // ============================ conv group (128 threads) ============================
+    // ============================ conv group (128 threads): q, k ============================
     auto cvwait = [&](int b, uint32_t par) -> bool {
       return role_and(1, NCV, tc::mbar_wait(&bars[b], par, abort, p.wait_ns));
     };
-    // thread = 8-channel group cg (channels 8cg..8cg+7) x block of 8 tokens tb; the 16
-    // lanes of a half warp hold the 128 channels of the same 8 tokens
-    const int cg = tid & 15, tb = tid >> 4;
-    const CUtensorMap* maps[3] = {&qmap, &kmap, &vmap};
-    int qk_issued = 0, v_issued = 0;
-    // raw rows (the chunk and the three before it; rows outside the tensor read as zero) of
-    // streams [s_lo, s_hi) of a chunk, on barrier b
-    auto issue_rows = [&](int s, int cc, int s_lo, int s_hi, int b) {
-      if (tid == 0) {
-        tc::fence_proxy_async_smem();  // the rows were last read (and patched) by threads
-        tc::mbar_expect_tx(&bars[b], (s_hi - s_lo) * 2 * HR * 128);
-        for (int s3 = s_lo; s3 < s_hi; ++s3)
-#pragma unroll
-          for (int half = 0; half < 2; ++half)
-            tc::tma_load_3d(raw + (s3 * 2 + half) * Lay::RAWH, maps[s3], &bars[b], half * 64, h,
-                            seg_start(s) + cc - (KW - 1));
-      }
-    };
+    int qk_issued = 0;
     // the raw gates of a chunk into its staging slot (read by the solve group)
     auto issue_gates = [&](int s, int cc, int gslot) {
       const int st0 = seg_start(s), ln = seg_len(s);
@@ -284,36 +366,21 @@ __global__ void __launch_bounds__(NT, 1)
       cp_async4(ga + gslot * 2 * C + (tid < C ? 0 : C) + uu, src, valid);
       asm volatile("cp.async.commit_group;\n" ::);
     };
-    // history rows of a segment start for streams [s_lo, s_hi): raw inputs before the segment
-    // (the request's conv window for a question or a resumed trunk, else zero)
-    auto patch_history = [&](int s_lo, int s_hi) {
-      for (int e = tid; e < (s_hi - s_lo) * (KW - 1) * D; e += NCV) {
-        const int s3 = s_lo + e / ((KW - 1) * D), i = (e / D) % (KW - 1), c = e % D;
-        const uint16_t hv =
-            hist ? hist[((static_cast<int64_t>(j * (KW - 1) + i) * 3 + s3) * H + h) * D + c] : uint16_t(0);
-        *reinterpret_cast<uint16_t*>(raw + (s3 * 2 + (c >> 6)) * Lay::RAWH + sw(i, (c & 63) >> 3) + (c & 7) * 2) = hv;
-      }
-    };
     if (tid == 0) {
       tc::prefetch_tmap(&qmap);
       tc::prefetch_tmap(&kmap);
-      tc::prefetch_tmap(&vmap);
     }
     bool ok = true;
     int si = first_seg(seg_first), c0 = 0, k = 0;
     if (si < seg_end) {
-      issue_rows(si, 0, 0, 2, B_RAWQK);
-      issue_rows(si, 0, 2, 3, B_RAWV);
+      if (tid == 0) issue_rows(si, 0, 0, 2, B_RAWQK);
       issue_gates(si, 0, 0);
       ++qk_issued;
-      ++v_issued;
     }
     while (ok && si < seg_end) {
       const int len = seg_len(si);
       const int n = min(C, len - c0);
       const int slot = k & 1;
-      float* NQ = gate(slot, G_NQ);
-      float* NK = gate(slot, G_NK);
       unsigned char* yts = yt(slot);
       int nsi = si, nc0 = c0 + C;
       if (nc0 >= len) {
@@ -323,113 +390,31 @@ __global__ void __launch_bounds__(NT, 1)
       // this chunk's q, k rows have landed; history rows of a segment start; the slot's tiles
       // are free once the chain's products of chunk k-2 are done
       if (!(ok = cvwait(B_RAWQK, (qk_issued - 1) & 1))) break;
-      if (c0 == 0) patch_history(0, 2);
+      if (c0 == 0) patch_history(tid, 0, 2);
       if (k >= 2 && !(ok = cvwait(B_EPI0 + slot, ((k - 2) >> 1) & 1))) break;
       role_sync(1, NCV);
-      // ---- conv + SiLU, stream by stream: thread = (8 channels, 8 tokens), a sliding
-      //      window of raw rows (positions u-3..u for token u), each row unpacked once;
-      //      fp16 rows into the operand tiles; the norms n_q, n_k from sums of squares over
-      //      the 16 lanes of a token block.  Y_v waits until the solve group's products
-      //      have read the previous one.
-      for (int st = 0; st < 3 && ok; ++st) {
-        if (st == 2) {
-          // the q, k rows are read: next chunk's q, k loads; then this chunk's v rows
-          role_sync(1, NCV);
-          if (nsi < seg_end) {
-            issue_rows(nsi, nc0, 0, 2, B_RAWQK);
-            ++qk_issued;
-          }
-          if (!(ok = cvwait(B_RAWV, (v_issued - 1) & 1))) break;
-          if (c0 == 0) patch_history(2, 3);
-          if (k >= 1 && !(ok = cvwait(B_MW, (k - 1) & 1))) break;
-          role_sync(1, NCV);
-        }
-        const float4* cw4 = reinterpret_cast<const float4*>(p.conv_w) + ((static_cast<int64_t>(st) * H + h) * D + 8 * cg);
-        const unsigned char* rb = raw + (st * 2 + (cg >> 3)) * Lay::RAWH;
-        const int jc = cg & 7;
-        unsigned char* dst = st == 2 ? yv + (cg >> 3) * 8192 : yts + (cg >> 3) * 16384;
-        const int u0 = tb * 8;
-        float cw[8][KW];  // the group's conv weights (8 channels x 4 taps), L1-resident
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 w = __ldg(cw4 + e);
-          cw[e][0] = w.x;
-          cw[e][1] = w.y;
-          cw[e][2] = w.z;
-          cw[e][3] = w.w;
-        }
-        float xw[KW][8];  // unpacked raw rows u-3..u of the 8 channels
-        auto unpack = [&](int row, float* x) {
-          const uint4 r4 = *reinterpret_cast<const uint4*>(rb + sw(row, jc));
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t word = word_of(r4, q);
-            x[2 * q] = bf_lo(word);
-            x[2 * q + 1] = bf_hi(word);
-          }
-        };
-#pragma unroll
-        for (int i = 0; i < KW - 1; ++i) unpack(u0 + i, xw[i + 1]);
-        float ssum[8];
-#pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
-          const int u = u0 + uu;
-#pragma unroll
-          for (int i = 0; i < KW - 1; ++i)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xw[i][e] = xw[i + 1][e];
-          unpack(u + KW - 1, xw[KW - 1]);  // position u
-          float y[8];
-          float sq = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float a = cw[e][0] * xw[0][e];
-#pragma unroll
-            for (int i = 1; i < KW; ++i) a = fmaf(cw[e][i], xw[i][e], a);
-            y[e] = u < n ? silu(a) : 0.f;
-            sq = fmaf(y[e], y[e], sq);
-          }
-          ssum[uu] = sq;
-          *reinterpret_cast<uint4*>(dst + sw(st == 1 ? C + u : u, jc)) =
-              make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
-        }
-        if (st < 2) {
-#pragma unroll
-          for (int uu = 0; uu < 8; ++uu) {
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) ssum[uu] += __shfl_xor_sync(0xffffffffu, ssum[uu], o);
-          }
-          if (cg < 8) {
-            float sv = ssum[0];
-#pragma unroll
-            for (int uu = 1; uu < 8; ++uu)
-              if (cg == uu) sv = ssum[uu];
-            (st == 0 ? NQ : NK)[u0 + cg] = rsqrtf_(sv + 1e-6f);
-          }
-        }
+      conv_stream(tid, 0, n, yts, 16384, 0, gate(slot, G_NQ));
+      conv_stream(tid, 1, n, yts, 16384, C, gate(slot, G_NK));
+      // the q, k rows are read: next chunk's loads
+      role_sync(1, NCV);
+      if (nsi < seg_end) {
+        if (tid == 0) issue_rows(nsi, nc0, 0, 2, B_RAWQK);
+        ++qk_issued;
       }
-      if (!ok) break;
       asm volatile("cp.async.wait_group 0;\n" ::);  // this chunk's gates are staged
       tc::fence_proxy_async_smem();
       role_sync(1, NCV);
       if (tid == 0) tc::mbar_arrive(&bars[B_CONV]);
-      // the v rows are read: next chunk's v rows and gates (its gate slot was read by the
-      // solve group for chunk k-1, done before this chunk's conv could start)
-      if (nsi < seg_end) {
-        issue_rows(nsi, nc0, 2, 3, B_RAWV);
-        ++v_issued;
-        issue_gates(nsi, nc0, (k + 1) & 1);
-      }
+      // next chunk's gates (its gate slot was read by the solve group for chunk k-1, done
+      // before this chunk's conv could start)
+      if (nsi < seg_end) issue_gates(nsi, nc0, (k + 1) & 1);
       ++k;
       si = nsi;
       c0 = nc0;
     }
     // drain: raw-row loads still in flight after an abort (the last ones issued: their
-    // phases are the barriers' last)
-    if (tid == 0 && !ok) {
-      if (qk_issued > 0) tc::mbar_drain(&bars[B_RAWQK], (qk_issued - 1) & 1);
-      if (v_issued > 0) tc::mbar_drain(&bars[B_RAWV], (v_issued - 1) & 1);
-    }
+    // phases are the barrier's last)
+    if (tid == 0 && !ok && qk_issued > 0) tc::mbar_drain(&bars[B_RAWQK], (qk_issued - 1) & 1);
     asm volatile("cp.async.wait_group 0;\n" ::);
   } else if (warp < (NCV + NSV) / 32) {
     // ============================ solve group (256 threads) ============================
@@ -675,9 +660,17 @@ __global__ void __launch_bounds__(NT, 1)
         for (int ks = 0; ks < C / 16; ++ks) {
           const uint64_t ao = static_cast<uint64_t>(ks * (2048 / 16)), bo = static_cast<uint64_t>(ks * 2);
           tc::mma_bf16(tmem + T_M1, dyk + ao, dtp + bo, id4, ks > 0);
-          tc::mma_bf16(tmem + t_u(slot), dyv + ao, dtpp + bo, id4, ks > 0);
         }
-        tc::mma_commit(&bars[B_MW]);
+        // Y_v of this chunk comes from the chain (a failed wait raises the abort flag: the
+        // group's next wait gives up too)
+        if (tc::mbar_wait(&bars[B_YV], k & 1, abort, p.wait_ns)) {
+#pragma unroll
+          for (int ks = 0; ks < C / 16; ++ks) {
+            const uint64_t ao = static_cast<uint64_t>(ks * (2048 / 16)), bo = static_cast<uint64_t>(ks * 2);
+            tc::mma_bf16(tmem + t_u(slot), dyv + ao, dtpp + bo, id4, ks > 0);
+          }
+          tc::mma_commit(&bars[B_MW]);
+        }
       }
       // ---- S5: -W (fp16) into its tile, free once the chain's products of chunk k-1 that
       //      read it are done (lane = channel c, 32 tokens per thread) ----------------------
@@ -766,10 +759,46 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc::tmem_wait_st();
     };
+    // Y_v of each chunk is made here, between the chain's own chunks (the conv group makes
+    // Y_q and Y_k): raw v rows requested one chunk ahead, conv + SiLU into the Y_v tile once
+    // the solve group's products of the previous chunk have read it (they complete before
+    // that chunk's operands are signalled ready)
+    int v_issued = 0;
+    auto v_rows = [&](int s, int cc) {
+      if (ct == 0) issue_rows(s, cc, 2, 3, B_RAWV);
+      ++v_issued;
+    };
+    auto v_conv = [&](int s, int cc) -> bool {
+      if (!cwait(B_RAWV, (v_issued - 1) & 1)) return false;
+      if (cc == 0) {
+        patch_history(ct, 2, 3);
+        role_sync(2, NCH);
+      }
+      conv_stream(ct, 2, min(C, seg_len(s) - cc), yv, 8192, 0, nullptr);
+      tc::fence_proxy_async_smem();
+      role_sync(2, NCH);
+      if (ct == 0) tc::mbar_arrive(&bars[B_YV]);
+      return true;
+    };
+    auto next_chunk = [&](int& s, int& cc) {
+      cc += C;
+      if (cc >= seg_len(s)) {
+        s = first_seg(s + 1);
+        cc = 0;
+      }
+    };
+    if (ct == 0) tc::prefetch_tmap(&vmap);
     if (!BRANCH) load_state(S0);
     bool ok = !p.stall || cwait(B_STALL, 0);  // FORK_TEST_STALL: runs out, nothing is issued
     bool s_is_start = !BRANCH;  // branch call: S holds S_P[j] (no question has updated it)
     int si = first_seg(seg_first), c0 = 0, k = 0;
+    if (ok && si < seg_end) {
+      v_rows(si, 0);
+      ok = v_conv(si, 0);
+      int s2 = si, c2 = 0;
+      next_chunk(s2, c2);
+      if (ok && s2 < seg_end) v_rows(s2, c2);
+    }
     while (ok && si < seg_end) {
       const int start = seg_start(si), len = seg_len(si), pos0 = seg_pos0(si);
       const int n = min(C, len - c0);
@@ -967,10 +996,13 @@ __global__ void __launch_bounds__(NT, 1)
       tc::tc_fence_before();
       tc::mbar_arrive(&bars[B_PF0 + slot]);  // the P tile (output staging) is free
       ++k;
-      c0 += C;
-      if (c0 >= len) {
-        si = first_seg(si + 1);
-        c0 = 0;
+      next_chunk(si, c0);
+      // Y_v of the next chunk; then the raw v rows of the one after it
+      if (si < seg_end) {
+        if (!(ok = v_conv(si, c0))) break;
+        int s2 = si, c2 = c0;
+        next_chunk(s2, c2);
+        if (s2 < seg_end) v_rows(s2, c2);
       }
     }
     if (ok && !BRANCH) {
@@ -990,6 +1022,8 @@ __global__ void __launch_bounds__(NT, 1)
     if (ct == 0) {
       tc::mma_commit(&bars[B_FINC]);
       tc::mbar_drain(&bars[B_FINC], 0);
+      // raw v rows still in flight after an abort (the last ones issued)
+      if (!ok && v_issued > 0) tc::mbar_drain(&bars[B_RAWV], (v_issued - 1) & 1);
     }
   }
 
