@@ -179,13 +179,13 @@ static bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t
 }
 
 struct AttnWs {
-  size_t qr, kr, pkr, hi, lo, vh, pvh, total;
+  size_t qr, kr, pkr, hi, lo, vh, pvh, ctr, total;
 };
 
 // With the rotary embedding: rotated keys (stream, prefix), the two rotary tables and, for
 // the warp-MMA kernel only, rotated queries (the tcgen05 kernel rotates its query tiles in
 // shared memory).  For the tcgen05 kernel: the values as fp16 (stream, prefix), its PV
-// operand (the exponentials stay fp16).
+// operand (the exponentials stay fp16), and the counter of claimed work items.
 static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hkv, int64_t d, bool warp_mma,
                       bool rope) {
   AttnWs w;
@@ -198,11 +198,13 @@ static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hk
   w.lo = al(w.hi + (rope ? static_cast<size_t>(rope_hi_rows(T_cap + prefix_rows)) * (d / 2) * 8 : 0));
   w.vh = al(w.lo + (rope ? static_cast<size_t>(64) * (d / 2) * 8 : 0));
   w.pvh = al(w.vh + (warp_mma ? 0 : kv));
-  w.total = al(w.pvh + (warp_mma ? 0 : pkv));
+  w.ctr = al(w.pvh + (warp_mma ? 0 : pkv));
+  w.total = al(w.ctr + (warp_mma ? 0 : 4));
   return w;
 }
 
-// Values of the stream rows [0, T) and of the prefix rows as fp16 (8 elements per thread).
+// Values of the stream rows [0, T) and of the prefix rows as fp16 (8 elements per thread);
+// also zeroes the counter through which the attention kernel's CTAs claim work items.
 // The rows [T, min(T_cap, T + 128)) of the copy are set to zero: a key tile that starts
 // inside the stream reads at most 127 rows past its range, and rows past T are not the
 // caller's data (any bits), while the products need finite values there (p = 0 and
@@ -210,7 +212,8 @@ static AttnWs attn_ws(int64_t T_cap, int64_t prefix_rows, int64_t Hq, int64_t Hk
 __global__ void __launch_bounds__(256) v_half_kernel(const int32_t* __restrict__ meta, const uint16_t* __restrict__ v,
                                                      const uint16_t* __restrict__ pv, uint16_t* __restrict__ vh,
                                                      uint16_t* __restrict__ pvh, int64_t row_elems, int prefix_rows,
-                                                     int T_cap) {
+                                                     int T_cap, int* __restrict__ work_ctr) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *work_ctr = 0;  // the attention kernel's item counter
   if (meta[H_VALID] == 0) return;
   const int T = meta[H_T];
   const int64_t n_stream = static_cast<int64_t>(T) * row_elems / 8;
@@ -292,6 +295,7 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   p.checks = (flags & FORK_CHECKS) ? 1 : 0;
   p.stall = (flags & FORK_TEST_STALL) ? 1 : 0;
   p.wait_ns = wait_ns_of(m);
+  p.work_ctr = nullptr;
 
   const AttnWs w = attn_ws(L.T_cap, prefix_rows, Hq, Hkv, d, warp_mma, rope_theta != 0.f);
   if (w.total > 0 && (!workspace || ws_bytes < w.total || !is_aligned16(workspace))) return FORK_EINVAL;
@@ -338,8 +342,9 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     const int64_t row_elems = static_cast<int64_t>(Hkv) * d;
     const int64_t n8 = (static_cast<int64_t>(L.T_cap) + p.prefix_rows) * row_elems / 8;
     const int blocks = static_cast<int>(std::min<int64_t>((n8 + 255) / 256, 8 * sm_count()));
+    p.work_ctr = reinterpret_cast<int*>(ws + w.ctr);
     v_half_kernel<<<std::max(blocks, 1), 256, 0, s>>>(p.meta, v, prefix_v, vh, pvh, row_elems, p.prefix_rows,
-                                                      L.T_cap);
+                                                      L.T_cap, p.work_ctr);
     vtc = vh;
     pvtc = pvh;
   }

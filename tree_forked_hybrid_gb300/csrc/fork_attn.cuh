@@ -37,6 +37,7 @@ struct AttnParams {
   int checks;                // FORK_CHECKS
   int stall;                 // FORK_TEST_STALL (tcgen05 path)
   uint64_t wait_ns;          // limit of a bounded wait
+  int* work_ctr;             // tcgen05 path: work items claimed so far (zeroed before the kernel)
 };
 
 // FORK_CHECKS: work item w's segment, its offset, its request and its trunk range lie

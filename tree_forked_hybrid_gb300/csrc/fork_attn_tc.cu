@@ -56,15 +56,16 @@ struct TcLayout {
   static constexpr int Q = 0;                        // 2 query tiles
   static constexpr int K = Q + 2 * NB * kBox;        // 2 stages
   static constexpr int V = K + 2 * NB * kBox;        // 2 stages
-  static constexpr int BAR = V + kVStages * NB * kBox;
-  static constexpr int BYTES = BAR + 256;
+  static constexpr int BAR = V + kVStages * NB * kBox;  // barriers, TMEM address, abort flag, tables
+  static constexpr int BYTES = BAR + 2048;
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);  // one CTA per SM
 };
 
 // B_KVFULLs: K and V tile f both landed in slot s = f mod 2 (one wait for the issuer)
-enum Bar { B_QFULL = 0, B_KVFULL0, B_KVFULL1, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0,
-           B_VEMPTY1, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_FIN, B_QROT,
-           B_STALL, B_COUNT };
+enum Bar { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KEMPTY0, B_KEMPTY1, B_VEMPTY0, B_VEMPTY1, B_SFULL0,
+           B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_OFREE0, B_OFREE1, B_FIN, B_QROT, B_STALL,
+           B_ITEMF0, B_ITEMF1, B_ITEMF2, B_ITEMF3, B_ITEME0, B_ITEME1, B_ITEME2, B_ITEME3, B_COUNT };
+constexpr int kItemRing = 4;  // claimed work items handed from the producer to the other roles
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -114,6 +115,7 @@ struct TcParams {
   int Hq, Hkv, G, prefix_rows, window, two_tiles, rotate_q, rope_hi_rows, checks, stall;
   float scale_log2;
   uint64_t wait_ns;
+  int* work_ctr;  // work items claimed after the first gridDim.x (zeroed before the launch)
 };
 
 // Rotary embedding of one query row held in a 128-byte-swizzled tile (boxes of 64
@@ -156,6 +158,79 @@ __device__ __forceinline__ void rotate_q_row(unsigned char* tile, int row, int t
   }
 }
 
+// One work item of a call: entry r of the longest-first order x kv head g.  Its query
+// tokens, and its key ranges in fixed slots: 0 prefix rows kept outside the stream, 1
+// trunk, 2 own branch (an absent range has length 0).  Every role of a CTA computes it
+// from the tables by itself.
+struct AttnItem {
+  int ok, status;  // status: the bit to raise when the item is skipped (ok == 0)
+  int g, seg_start, off, n_all, ntiles, tx_min, total;
+  int row0[3], len[3], pos0[3], lo[3], cnt[3];
+};
+
+__device__ __forceinline__ AttnItem attn_item(const int32_t* meta, const MetaLayout& L, const TcParams& p, int q) {
+  AttnItem it;
+  const int r = q / p.Hkv;
+  it.g = q - r * p.Hkv;
+  it.ok = 0;
+  it.status = 0;
+  it.total = 0;
+  const int w = meta[L.work_order + r];
+  if (p.checks && !attn_item_in_bounds(meta, L, w)) {
+    it.status = FORK_STATUS_CHECK;
+    return it;
+  }
+  const int s = meta[L.work_seg + w];
+  it.off = meta[L.work_off + w];
+  it.seg_start = meta[L.seg_start + s];
+  const int seg_len = meta[L.seg_len + s];
+  const int seg_pos0 = meta[L.seg_pos0 + s];
+  const int j = meta[L.seg_req + s];
+  const int c = meta[L.seg_branch + s];
+  const int tile = kRows / p.G;
+  it.n_all = min(p.two_tiles ? 2 * tile : tile, seg_len - it.off);
+  it.ntiles = it.n_all > tile ? 2 : 1;
+  it.tx_min = seg_pos0 + it.off;
+  const int tx_max = it.tx_min + it.n_all - 1;
+  const int pl = meta[L.req_prefix_len + j];
+  const int poff = pl > 0 ? meta[L.req_prefix_off + j] : 0;
+  if (pl > 0 && poff + pl > p.prefix_rows) {
+    it.status = FORK_STATUS_BAD_PREFIX;
+    return it;
+  }
+  it.row0[0] = poff;
+  it.len[0] = pl;
+  it.pos0[0] = 0;
+  it.row0[1] = meta[L.seg_trunk_start + s];
+  it.len[1] = meta[L.seg_trunk_len + s];
+  it.pos0[1] = pl;
+  it.row0[2] = it.seg_start;
+  it.len[2] = c > 0 ? seg_len : 0;
+  it.pos0[2] = seg_pos0;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    it.lo[k] = 0;
+    it.cnt[k] = 0;
+    if (it.len[k] > 0) {
+      const int umax = min(it.len[k] - 1, tx_max - it.pos0[k]);
+      const int umin = p.window > 0 ? max(0, it.tx_min - p.window + 1 - it.pos0[k]) : 0;
+      if (umax >= umin) {
+        it.lo[k] = umin / kKeys;
+        it.cnt[k] = umax / kKeys - it.lo[k] + 1;
+      }
+    }
+    it.total += it.cnt[k];
+  }
+  it.ok = it.total > 0;  // always, for a valid item (a token sees itself)
+  return it;
+}
+
+// Persistent kernel: one CTA per SM takes work items in longest-first order: item
+// blockIdx.x first, then the next unclaimed one (an atomic counter, read by the producer,
+// which hands each item index to the other roles through a small ring in shared memory).  TMEM, barriers and tensor-map prefetches are set up once; the
+// loads run on into the next item as slots free up, and the next item's query tiles land
+// while the current item's last products and output rows finish.  Barrier phases follow
+// running counts (key tiles F, items, per-tile S and O), identical in every role.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -170,91 +245,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* meta = p.meta;
   const MetaLayout& L = p.L;
   if (meta[H_VALID] == 0) return;
-  if (static_cast<int>(blockIdx.x) >= meta[H_NWORK]) return;
-  const int w = meta[L.work_order + blockIdx.x];  // longest items first
-  const int g = blockIdx.y;
+  const int n_items = meta[H_NWORK] * p.Hkv;
+  if (static_cast<int>(blockIdx.x) >= n_items) return;
   const int G = p.G;
   const int tile = kRows / G;  // tokens per MMA tile
-  if (p.checks && !attn_item_in_bounds(meta, L, w)) {
-    if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_CHECK);
-    return;
-  }
-  const int s = meta[L.work_seg + w];
-  const int off = meta[L.work_off + w];
-  const int seg_start = meta[L.seg_start + s];
-  const int seg_len = meta[L.seg_len + s];
-  const int seg_pos0 = meta[L.seg_pos0 + s];
-  const int j = meta[L.seg_req + s];
-  const int c = meta[L.seg_branch + s];
-  const int n_all = min(p.two_tiles ? 2 * tile : tile, seg_len - off);  // tokens of this work item
-  const int ntiles = n_all > tile ? 2 : 1;
-  const int tx_min = seg_pos0 + off;
-  const int tx_max = seg_pos0 + off + n_all - 1;
-
-  // ---- key ranges in fixed slots: 0 prefix rows, 1 trunk, 2 own branch --------------
-  // (an absent range has length 0; fixed slots keep every range variable in registers)
-  const int pl = meta[L.req_prefix_len + j];
-  const int poff = pl > 0 ? meta[L.req_prefix_off + j] : 0;
-  if (pl > 0 && poff + pl > p.prefix_rows) {
-    if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
-    return;
-  }
-  const int r_row0_0 = poff, r_len_0 = pl, r_pos0_0 = 0;
-  const int r_row0_1 = meta[L.seg_trunk_start + s], r_len_1 = meta[L.seg_trunk_len + s], r_pos0_1 = pl;
-  const int r_row0_2 = seg_start, r_len_2 = c > 0 ? seg_len : 0, r_pos0_2 = seg_pos0;
-  auto tiles = [&](int len, int pos0, int& lo_t, int& cnt_t) {
-    lo_t = 0;
-    cnt_t = 0;
-    if (len <= 0) return;
-    const int umax = min(len - 1, tx_max - pos0);
-    const int umin = p.window > 0 ? max(0, tx_min - p.window + 1 - pos0) : 0;
-    if (umax >= umin) {
-      lo_t = umin / kKeys;
-      cnt_t = umax / kKeys - lo_t + 1;
-    }
-  };
-  int lo0, cnt0, lo1, cnt1, lo2, cnt2;
-  tiles(r_len_0, r_pos0_0, lo0, cnt0);
-  tiles(r_len_1, r_pos0_1, lo1, cnt1);
-  tiles(r_len_2, r_pos0_2, lo2, cnt2);
-  const int total = cnt0 + cnt1 + cnt2;
-  if (total == 0) return;  // cannot happen for a valid tile (a token sees itself)
-  // flat key-tile index f -> range slot r, first key row, length, first position, tile t
-  struct KT {
-    int r, row0, len, pos0, t;
-  };
-  auto key_tile = [&](int f) -> KT {
-    if (f < cnt0) return {0, r_row0_0, r_len_0, r_pos0_0, lo0 + f};
-    f -= cnt0;
-    if (f < cnt1) return {1, r_row0_1, r_len_1, r_pos0_1, lo1 + f};
-    f -= cnt1;
-    return {2, r_row0_2, r_len_2, r_pos0_2, lo2 + f};
-  };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::BAR + B_COUNT * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + LY::BAR + B_COUNT * 8 + 8);
-  // per range slot: first tile, tile count, length, first position (read by the softmax
-  // warps, which keep no range variables in registers)
-  int* rtab = reinterpret_cast<int*>(smem + LY::BAR + B_COUNT * 8 + 16);
+  // per softmax warp: the current item's range table (first tile, tile count, length,
+  // first position per slot), read in the key-tile loop instead of holding registers
+  int* rtab_all = reinterpret_cast<int*>(smem + LY::BAR + B_COUNT * 8 + 16);
+  // claimed work items (AttnItem, ok == 0 marks the end), written by the producer
+  AttnItem* ring = reinterpret_cast<AttnItem*>(smem + LY::BAR + B_COUNT * 8 + 16 + 8 * 12 * 4);
+  static_assert(B_COUNT * 8 + 16 + 8 * 12 * 4 + kItemRing * sizeof(AttnItem) <= 2048, "barrier region");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     tc::mbar_init(&bars[B_QFULL], 1);
-    for (int k = 0; k < kVStages; ++k) tc::mbar_init(&bars[B_VEMPTY0 + k], 1);
+    tc::mbar_init(&bars[B_QEMPTY], 1);
     for (int k = 0; k < 2; ++k) {
       tc::mbar_init(&bars[B_KVFULL0 + k], 1);
       tc::mbar_init(&bars[B_KEMPTY0 + k], 1);
+      tc::mbar_init(&bars[B_VEMPTY0 + k], 1);
       tc::mbar_init(&bars[B_SFULL0 + k], 1);
       tc::mbar_init(&bars[B_PFULL0 + k], 128);
       tc::mbar_init(&bars[B_OFULL0 + k], 1);
+      tc::mbar_init(&bars[B_OFREE0 + k], 128);
     }
     tc::mbar_init(&bars[B_FIN], 1);
     tc::mbar_init(&bars[B_QROT], 256);
     tc::mbar_init(&bars[B_STALL], 1);  // completed by nothing (FORK_TEST_STALL)
+    for (int k = 0; k < kItemRing; ++k) {
+      tc::mbar_init(&bars[B_ITEMF0 + k], 1);
+      tc::mbar_init(&bars[B_ITEME0 + k], 9);  // the issuer and the 8 softmax warps have read it
+    }
     *abort = 0;
-    const int tab[12] = {lo0, cnt0, r_len_0, r_pos0_0, lo1, cnt1, r_len_1, r_pos0_1, lo2, cnt2, r_len_2, r_pos0_2};
-    for (int i = 0; i < 12; ++i) rtab[i] = tab[i];
     tc::fence_mbar_init();
   }
   if (warp == 0) {
@@ -270,47 +296,87 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sQ = smem + LY::Q;
   unsigned char* sK = smem + LY::K;
   unsigned char* sV = smem + LY::V;
+  // flat key-tile index f of an item -> range slot r, first key row, length, first position, tile
+  struct KT {
+    int r, row0, len, pos0, t;
+  };
+  auto key_tile = [&](const AttnItem& it, int f) -> KT {
+    if (f < it.cnt[0]) return {0, it.row0[0], it.len[0], it.pos0[0], it.lo[0] + f};
+    f -= it.cnt[0];
+    if (f < it.cnt[1]) return {1, it.row0[1], it.len[1], it.pos0[1], it.lo[1] + f};
+    f -= it.cnt[1];
+    return {2, it.row0[2], it.len[2], it.pos0[2], it.lo[2] + f};
+  };
 
   if (warp == 1) {
-    // ===================== TMA producer =====================
+    // ===================== TMA producer (lane 0) =====================
     if (lane == 0) {
       tc::prefetch_tmap(&qmap);
       tc::prefetch_tmap(&kmap);
       tc::prefetch_tmap(&vmap);
-      if (pl > 0) {
+      if (p.prefix_rows > 0) {
         tc::prefetch_tmap(&pkmap);
         tc::prefetch_tmap(&pvmap);
       }
-      tc::mbar_expect_tx(&bars[B_QFULL], ntiles * NB * kBox);
-      for (int t = 0; t < ntiles; ++t)
-        for (int b = 0; b < NB; ++b)
-          tc::tma_load_3d(sQ + (t * NB + b) * kBox, &qmap, &bars[B_QFULL], b * 64, g * G,
-                          seg_start + off + t * tile);
-      // K_f waits for the QK^T products of K_{f-2} (its slot's previous reader), V_f for
-      // the PV products of V_{f-2}; both land on the slot's one barrier, whose phase also
-      // needs the arrival made after both copies were issued
-      int issued = 0;
-      for (int f = 0; f < total; ++f) {
-        const int st = f & 1;
-        const KT kt = key_tile(f);
-        const CUtensorMap* km = kt.r == 0 ? &pkmap : &kmap;
-        const CUtensorMap* vm = kt.r == 0 ? &pvmap : &vmap;
-        const int row = kt.row0 + kt.t * kKeys;
-        if (f >= 2 && !tc::mbar_wait(&bars[B_KEMPTY0 + st], ((f >> 1) - 1) & 1, abort, p.wait_ns)) break;
-        tc::mbar_expect_tx_only(&bars[B_KVFULL0 + st], NB * kBox);
-        for (int b = 0; b < NB; ++b) tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KVFULL0 + st], b * 64, g, row);
-        issued = f + 1;
-        const bool vok = f < 2 || tc::mbar_wait(&bars[B_VEMPTY0 + st], ((f >> 1) - 1) & 1, abort, p.wait_ns);
-        if (vok) {
-          tc::mbar_expect_tx_only(&bars[B_KVFULL0 + st], NB * kBox);
-          for (int b = 0; b < NB; ++b) tc::tma_load_3d(sV + (st * NB + b) * kBox, vm, &bars[B_KVFULL0 + st], b * 64, g, row);
+      auto wait = [&](int b, uint32_t par) -> bool { return tc::mbar_wait(&bars[b], par, abort, p.wait_ns); };
+      bool ok = true;
+      int F = 0, issued = 0, nq = 0, n = 0;
+      for (int q = blockIdx.x;; q = static_cast<int>(gridDim.x) + atomicAdd(p.work_ctr, 1)) {
+        AttnItem it;
+        if (q < n_items) {
+          it = attn_item(meta, L, p, q);
+          if (!it.ok) {  // skipped by every role: never handed on
+            if (it.status) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, it.status);
+            continue;
+          }
+        } else {
+          it.ok = 0;  // the end
         }
-        tc::mbar_arrive(&bars[B_KVFULL0 + st]);  // after an abort: the phase ends with the K copy
-        if (!vok) break;
+        // hand the item to the other roles through ring slot n mod 4, free once all of
+        // them have read the item four back
+        const int slot = n & (kItemRing - 1);
+        if (n >= kItemRing && !(ok = wait(B_ITEME0 + slot, ((n / kItemRing) - 1) & 1))) break;
+        ring[slot] = it;
+        tc::mbar_arrive(&bars[B_ITEMF0 + slot]);
+        ++n;
+        if (!it.ok) break;
+        // the query tiles, once the previous item's QK^T products have read theirs
+        if (nq > 0 && !(ok = wait(B_QEMPTY, (nq - 1) & 1))) break;
+        tc::mbar_expect_tx(&bars[B_QFULL], it.ntiles * NB * kBox);
+        for (int t = 0; t < it.ntiles; ++t)
+          for (int b = 0; b < NB; ++b)
+            tc::tma_load_3d(sQ + (t * NB + b) * kBox, &qmap, &bars[B_QFULL], b * 64, it.g * G,
+                            it.seg_start + it.off + t * tile);
+        ++nq;
+        // K_F waits for the QK^T products of K_{F-2} (its slot's previous reader), V_F for
+        // the PV products of V_{F-2}; both land on the slot's one barrier, whose phase also
+        // needs the arrival made after both copies were issued
+        for (int f = 0; f < it.total; ++f, ++F) {
+          const int st = F & 1;
+          const KT kt = key_tile(it, f);
+          const CUtensorMap* km = kt.r == 0 ? &pkmap : &kmap;
+          const CUtensorMap* vm = kt.r == 0 ? &pvmap : &vmap;
+          const int row = kt.row0 + kt.t * kKeys;
+          if (F >= 2 && !(ok = wait(B_KEMPTY0 + st, ((F >> 1) - 1) & 1))) break;
+          tc::mbar_expect_tx_only(&bars[B_KVFULL0 + st], NB * kBox);
+          for (int b = 0; b < NB; ++b)
+            tc::tma_load_3d(sK + (st * NB + b) * kBox, km, &bars[B_KVFULL0 + st], b * 64, it.g, row);
+          issued = F + 1;
+          const bool vok = F < 2 || wait(B_VEMPTY0 + st, ((F >> 1) - 1) & 1);
+          if (vok) {
+            tc::mbar_expect_tx_only(&bars[B_KVFULL0 + st], NB * kBox);
+            for (int b = 0; b < NB; ++b)
+              tc::tma_load_3d(sV + (st * NB + b) * kBox, vm, &bars[B_KVFULL0 + st], b * 64, it.g, row);
+          }
+          tc::mbar_arrive(&bars[B_KVFULL0 + st]);  // after an abort: the phase ends with the K copy
+          ok = vok;
+          if (!ok) break;
+        }
+        if (!ok) break;
       }
-      // drain: the Q tiles and the last copies issued into each slot complete by themselves
-      // (no copy is issued into a slot after them, so their phases are the slots' last)
-      tc::mbar_drain(&bars[B_QFULL], 0);
+      // drain: the last query tiles and the last copies issued into each slot complete by
+      // themselves (no copy is issued after them, so their phases are the barriers' last)
+      if (nq > 0) tc::mbar_drain(&bars[B_QFULL], (nq - 1) & 1);
       for (int f = max(0, issued - 2); f < issued; ++f) tc::mbar_drain(&bars[B_KVFULL0 + (f & 1)], (f >> 1) & 1);
     }
   } else if (warp == 0) {
@@ -329,15 +395,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv = tc::sdesc_sw128(tc::smem_u32(sV), kBox, 1024);
       constexpr uint64_t kBoxU = kBox / 16, kStageU = NB * kBox / 16;
       auto wait = [&](int b, uint32_t par) -> bool { return tc::mbar_wait(&bars[b], par, abort, p.wait_ns); };
-      auto issue_pv = [&](int t, int f) {
+      // O_t (+)= P_t V, V in slot vs; the first product of an item overwrites O_t
+      auto issue_pv = [&](int t, bool first, int vs) {
         const uint32_t a = tm_s(t);
-        const uint64_t d0 = dv + (f % kVStages) * kStageU;
+        const uint64_t d0 = dv + vs * kStageU;
 #pragma unroll
         for (int step = 0; step < kKeys / 16; ++step)
-          mma_bf16_ts(tm_o(t), a + step * 8, d0 + step * (2048 / 16), idesc_pv, (f > 0 || step > 0) ? 1u : 0u);
+          mma_bf16_ts(tm_o(t), a + step * 8, d0 + step * (2048 / 16), idesc_pv, (!first || step > 0) ? 1u : 0u);
       };
-      auto issue_qk = [&](int t, int f) {
-        const uint64_t a0 = dq + t * NB * kBoxU, b0 = dk + (f & 1) * kStageU;
+      auto issue_qk = [&](int t, int ks) {
+        const uint64_t a0 = dq + t * NB * kBoxU, b0 = dk + ks * kStageU;
 #pragma unroll
         for (int b = 0; b < NB; ++b)
 #pragma unroll
@@ -345,37 +412,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16(tm_s(t), a0 + b * kBoxU + k * 2, b0 + b * kBoxU + k * 2, idesc_qk, (b | k) ? 1u : 0u);
       };
       bool ok = !p.stall || wait(B_STALL, 0);  // FORK_TEST_STALL: runs out, nothing is issued
-      ok = ok && wait(p.rotate_q ? B_QROT : B_QFULL, 0);
-      // per key tile f: O_0 += P_0(f-1) V(f-1), S_0 = Q_0 K(f)^T, O_1 += P_1(f-1) V(f-1),
-      // S_1 = Q_1 K(f)^T.  The wait for K(f), V(f) sits after the first PV products rather
-      // than after QK^T products, whose operand reads fill shared memory and slow the wait.
-      for (int f = 0; ok && f < total; ++f) {
-        const int st = f & 1;
-        for (int t = 0; ok && t < ntiles; ++t) {
-          // P_t(f-1) is in the TMEM columns of S_t: the products read it before S_t is
-          // rewritten (tcgen05 MMAs of one thread execute in issue order)
-          if (f > 0) {
-            if (!(ok = wait(B_PFULL0 + t, (f - 1) & 1))) break;
-            tc::tc_fence_after();
-            issue_pv(t, f - 1);
-            // V_{f-1} has no reader after the last tile's PV products: its slot is
-            // released before the next QK^T products are queued behind them
-            if (t == ntiles - 1) tc::mma_commit(&bars[B_VEMPTY0 + (f - 1) % kVStages]);
+      int F = 0, nq = 0, nS[2] = {0, 0}, nO[2] = {0, 0};
+      // PV products of tile t for the item's key tile f (V in slot vs): P_t published; the
+      // first one of an item overwrites O_t, which the previous item's rows have read
+      auto pv = [&](int t, int f, int vs) -> bool {
+        if (!wait(B_PFULL0 + t, (nS[t] - 1) & 1)) return false;
+        if (f == 0 && nO[t] > 0 && !wait(B_OFREE0 + t, (nO[t] - 1) & 1)) return false;
+        tc::tc_fence_after();
+        issue_pv(t, f == 0, vs);
+        return true;
+      };
+      for (int n = 0; ok; ++n) {
+        const int slot = n & (kItemRing - 1);
+        if (!(ok = wait(B_ITEMF0 + slot, (n / kItemRing) & 1))) break;
+        const AttnItem it = ring[slot];
+        tc::mbar_arrive(&bars[B_ITEME0 + slot]);
+        if (!it.ok) break;
+        const int ntiles = it.ntiles, total = it.total;
+        if (!(ok = wait(p.rotate_q ? B_QROT : B_QFULL, nq & 1))) break;
+        ++nq;
+        // per key tile f: O_0 += P_0(f-1) V(f-1), S_0 = Q_0 K(f)^T, O_1 += P_1(f-1) V(f-1),
+        // S_1 = Q_1 K(f)^T.  The wait for K(f), V(f) sits after the first PV products
+        // rather than after QK^T products, whose operand reads fill shared memory and slow
+        // the wait.
+        for (int f = 0; ok && f < total; ++f, ++F) {
+          const int st = F & 1;
+          for (int t = 0; ok && t < ntiles; ++t) {
+            // P_t(f-1) is in the TMEM columns of S_t: the products read it before S_t is
+            // rewritten (tcgen05 MMAs of one thread execute in issue order)
+            if (f > 0) {
+              if (!(ok = pv(t, f - 1, st ^ 1))) break;
+              // V_{F-1} has no reader after the last tile's PV products: its slot is
+              // released before the next QK^T products are queued behind them
+              if (t == ntiles - 1) tc::mma_commit(&bars[B_VEMPTY0 + (st ^ 1)]);
+            }
+            if (t == 0 && !(ok = wait(B_KVFULL0 + st, (F >> 1) & 1))) break;  // K(F) and V(F)
+            issue_qk(t, st);
+            tc::mma_commit(&bars[B_SFULL0 + t]);
+            ++nS[t];
           }
-          if (t == 0 && !(ok = wait(B_KVFULL0 + st, (f >> 1) & 1))) break;  // K(f) and V(f)
-          issue_qk(t, f);
-          tc::mma_commit(&bars[B_SFULL0 + t]);
+          if (ok) tc::mma_commit(&bars[B_KEMPTY0 + st]);
         }
-        if (ok) tc::mma_commit(&bars[B_KEMPTY0 + st]);
-      }
-      const int last_tile = total - 1;
-      if (ok) {
-        for (int t = 0; t < ntiles; ++t) {
-          if (!wait(B_PFULL0 + t, last_tile & 1)) break;
-          tc::tc_fence_after();
-          issue_pv(t, last_tile);
+        if (!ok) break;
+        tc::mma_commit(&bars[B_QEMPTY]);  // the item's QK^T products were the last readers of Q
+        const int vs = (F - 1) & 1;
+        for (int t = 0; ok && t < ntiles; ++t) {
+          if (!(ok = pv(t, total - 1, vs))) break;
           tc::mma_commit(&bars[B_OFULL0 + t]);
+          ++nO[t];
         }
+        if (ok) tc::mma_commit(&bars[B_VEMPTY0 + vs]);
       }
       // every MMA issued by this thread has completed before TMEM is released (also after
       // an abort: the products already issued finish by themselves)
@@ -386,13 +472,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ===================== softmax warpgroups (tile t = (warp - 2) / 4, row = tid % 128) ====
     const int t = (warp - 2) >> 2;
-    if (p.rotate_q) {
-      // rotary embedding of the query tiles in shared memory, thread = row, once they have
-      // landed; the products read them after every thread's fence and arrival.  The row's
-      // two table rows (512 bytes each) are prefetched into L1 while the tiles load.
-      if (t < ntiles) {
-        const int tok = (tid & 127) / G;
-        const int tpos = tx_min + t * tile + min(tok, tile - 1);
+    int* rtab = rtab_all + (warp - 2) * 12;
+    const int row = tid & 127;
+    const int tok = row / G, hl = row % G;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ts = tm_s(t) + lane_base, to = tm_o(t) + lane_base;
+    const float sl2 = p.scale_log2;
+    int n = 0, nq = 0, nS = 0, nO = 0;
+    // the next item from the ring (ok == 0: the end); false on a failed wait
+    auto fetch = [&](AttnItem& it) -> bool {
+      const int slot = n & (kItemRing - 1);
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&bars[B_ITEMF0 + slot], (n / kItemRing) & 1, abort, p.wait_ns)))
+        return false;
+      it = ring[slot];
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bars[B_ITEME0 + slot]);
+      ++n;
+      return true;
+    };
+    // rotary embedding of an item's query tiles in shared memory, thread = row, once they
+    // have landed; the products read them after every thread's fence and arrival.  The
+    // row's two table rows (512 bytes each) are prefetched into L1 while the tiles load.
+    auto rotate = [&](const AttnItem& it) -> bool {
+      if (t < it.ntiles) {
+        const int tpos = it.tx_min + t * tile + min(tok, tile - 1);
         if (tpos >> 6 < p.rope_hi_rows) {
           const char* ha = reinterpret_cast<const char*>(p.rope_hi + static_cast<int64_t>(tpos >> 6) * (D / 2));
           const char* la = reinterpret_cast<const char*>(p.rope_lo + static_cast<int64_t>(tpos & 63) * (D / 2));
@@ -403,126 +506,148 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const bool okq = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_QFULL], 0, abort, p.wait_ns));
-      if (okq && t < ntiles) {
-        const int row = tid & 127, tok = row / G;
-        if (tok < min(tile, n_all - t * tile)) {
-          const int tpos = tx_min + t * tile + tok;
-          if (tpos >> 6 < p.rope_hi_rows) rotate_q_row<D>(sQ + t * NB * kBox, row, tpos, p.rope_hi, p.rope_lo);
-        }
+      const bool okq = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_QFULL], nq & 1, abort, p.wait_ns));
+      ++nq;
+      if (okq && t < it.ntiles && tok < min(tile, it.n_all - t * tile)) {
+        const int tpos = it.tx_min + t * tile + tok;
+        if (tpos >> 6 < p.rope_hi_rows) rotate_q_row<D>(sQ + t * NB * kBox, row, tpos, p.rope_hi, p.rope_lo);
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars[B_QROT]);
-    }
-    if (t < ntiles) {
-      const int row = tid & 127;
-      const int tok = row / G, hl = row % G;
-      const int n_t = min(tile, n_all - t * tile);  // valid tokens of this tile
-      const int txm = tx_min + t * tile;            // first position of this tile
-      const int txM = txm + n_t - 1;                // last valid position of this tile
-      const int tx = txm + tok;
-      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t ts = tm_s(t) + lane_base, to = tm_o(t) + lane_base;
-      bool ok = true;
-      float m_used = -INFINITY, l = 0.f;
-      const float sl2 = p.scale_log2;
-      for (int f = 0; ok && f < total; ++f) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SFULL0 + t], f & 1, abort, p.wait_ns));
-        if (!ok) break;
-        tc::tc_fence_after();
-        float sv[kKeys];
-        {
-          uint32_t rawv[kKeys];
+      return okq;
+    };
+    AttnItem cur;
+    bool ok = fetch(cur);
+    if (ok && cur.ok && p.rotate_q) ok = rotate(cur);
+    while (ok && cur.ok) {
+      const bool mine = t < cur.ntiles;
+      const int n_t = mine ? min(tile, cur.n_all - t * tile) : 0;  // valid tokens of this tile
+      float l = 0.f;
+      if (mine) {
+        __syncwarp();  // every lane has finished reading the previous item's table
+        if (lane == 0) {
 #pragma unroll
-          for (int i = 0; i < kKeys / 32; ++i) tc::tmem_ld32(ts + i * 32, rawv + i * 32);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int cc = 0; cc < kKeys; ++cc) sv[cc] = __uint_as_float(rawv[cc]);
-        }
-        int len, p0, u0;
-        {
-          const int c0 = rtab[1], c1 = rtab[5];
-          const int r = f < c0 ? 0 : (f < c0 + c1 ? 1 : 2);
-          const int fr = f - (r == 0 ? 0 : (r == 1 ? c0 : c0 + c1));
-          u0 = (rtab[4 * r] + fr) * kKeys;
-          len = rtab[4 * r + 2];
-          p0 = rtab[4 * r + 3];
-        }
-        const bool need_mask = (u0 + kKeys > len) || (p0 + u0 + kKeys - 1 > txm) ||
-                               (p.window > 0 && txM - (p0 + u0) >= p.window);
-        if (need_mask) {
-          // key u0+cc visible iff inside the range, not after the query, inside the window
-          const int lim_len = len - u0;          // cc < lim_len
-          const int lim_causal = tx - p0 - u0;   // cc <= lim_causal
-          const int lim_win = p.window > 0 ? tx - p0 - u0 - p.window : -0x40000000;  // cc > lim_win
-#pragma unroll
-          for (int cc = 0; cc < kKeys; ++cc)
-            if (cc >= lim_len || cc > lim_causal || cc <= lim_win) sv[cc] = -INFINITY;
-        }
-        // row maximum (raw scores; the scale is positive): 8 independent chains of
-        // three-input maxima
-        float mx[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = sv[e];
-#pragma unroll
-        for (int cc = 8; cc < kKeys - 8; cc += 16)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx[e] = max3(mx[e], sv[cc + e], sv[cc + 8 + e]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[kKeys - 8 + e]);
-        const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
-        const bool resc = mt > m_used + kRescale;
-        const float m_new = resc ? mt : m_used;
-        const float base = (m_new == -INFINITY) ? 0.f : m_new;
-        const float factor = resc ? exp2f(m_used - base) : 1.f;  // 0 when nothing was accumulated
-        // p = 2^(s*scale*log2e - base) as fp16 pairs (key order) into the first 64 columns
-        // of S_t; the row sum adds 8 pairs per fp16 accumulator (each below 2^11), then in fp32
-        float rs = 0.f;
-#pragma unroll
-        for (int h2 = 0; h2 < 4; ++h2) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int cc = h2 * 32 + 2 * e;
-            pk[e] = exp2_pair(fmaf(sv[cc], sl2, -base), fmaf(sv[cc + 1], sl2, -base));
+          for (int k = 0; k < 3; ++k) {
+            rtab[4 * k] = cur.lo[k];
+            rtab[4 * k + 1] = cur.cnt[k];
+            rtab[4 * k + 2] = cur.len[k];
+            rtab[4 * k + 3] = cur.pos0[k];
           }
-          tc::tmem_st16(ts + h2 * 16, pk);
-          uint32_t acc2[2];
-#pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            acc2[a] = pk[8 * a];
-#pragma unroll
-            for (int e = 1; e < 8; ++e) acc2[a] = hadd2(acc2[a], pk[8 * a + e]);
-          }
-          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&acc2[0]));
-          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&acc2[1]));
-          rs += (f0.x + f0.y) + (f1.x + f1.y);
         }
-        l = l * factor + rs;
-        m_used = m_new;
-        // O_t holds the products of key tiles < f (all complete: S_t(f) was committed after
-        // them) and no product writes it until P_t(f) is published; rescaled after the
-        // exponentials, when the scores no longer occupy registers
-        if (f >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
+        __syncwarp();
+        const int total = cur.total;
+        const int txm = cur.tx_min + t * tile;  // first position of this tile
+        const int txM = txm + n_t - 1;           // last valid position of this tile
+        const int tx = txm + tok;
+        float m_used = -INFINITY;
+        for (int f = 0; ok && f < total; ++f) {
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SFULL0 + t], nS & 1, abort, p.wait_ns));
+          if (!ok) break;
+          ++nS;
+          tc::tc_fence_after();
+          float sv[kKeys];
+          {
+            uint32_t rawv[kKeys];
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i) {
-            uint32_t ov[32];
-            tc::tmem_ld32(to + i * 32, ov);
+            for (int i = 0; i < kKeys / 32; ++i) tc::tmem_ld32(ts + i * 32, rawv + i * 32);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
-            tc::tmem_st32(to + i * 32, ov);
+            for (int cc = 0; cc < kKeys; ++cc) sv[cc] = __uint_as_float(rawv[cc]);
           }
+          int len, p0, u0;
+          {
+            const int c0 = rtab[1], c1 = rtab[5];
+            const int r = f < c0 ? 0 : (f < c0 + c1 ? 1 : 2);
+            const int fr = f - (r == 0 ? 0 : (r == 1 ? c0 : c0 + c1));
+            u0 = (rtab[4 * r] + fr) * kKeys;
+            len = rtab[4 * r + 2];
+            p0 = rtab[4 * r + 3];
+          }
+          const bool need_mask = (u0 + kKeys > len) || (p0 + u0 + kKeys - 1 > txm) ||
+                                 (p.window > 0 && txM - (p0 + u0) >= p.window);
+          if (need_mask) {
+            // key u0+cc visible iff inside the range, not after the query, inside the window
+            const int lim_len = len - u0;          // cc < lim_len
+            const int lim_causal = tx - p0 - u0;   // cc <= lim_causal
+            const int lim_win = p.window > 0 ? tx - p0 - u0 - p.window : -0x40000000;  // cc > lim_win
+#pragma unroll
+            for (int cc = 0; cc < kKeys; ++cc)
+              if (cc >= lim_len || cc > lim_causal || cc <= lim_win) sv[cc] = -INFINITY;
+          }
+          // row maximum (raw scores; the scale is positive): 8 independent chains of
+          // three-input maxima
+          float mx[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = sv[e];
+#pragma unroll
+          for (int cc = 8; cc < kKeys - 8; cc += 16)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx[e] = max3(mx[e], sv[cc + e], sv[cc + 8 + e]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[kKeys - 8 + e]);
+          const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+          const bool resc = mt > m_used + kRescale;
+          const float m_new = resc ? mt : m_used;
+          const float base = (m_new == -INFINITY) ? 0.f : m_new;
+          const float factor = resc ? exp2f(m_used - base) : 1.f;  // 0 when nothing was accumulated
+          // p = 2^(s*scale*log2e - base) as fp16 pairs (key order) into the first 64 columns
+          // of S_t; the row sum adds 8 pairs per fp16 accumulator (each below 2^11), then in fp32
+          float rs = 0.f;
+#pragma unroll
+          for (int h2 = 0; h2 < 4; ++h2) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int cc = h2 * 32 + 2 * e;
+              pk[e] = exp2_pair(fmaf(sv[cc], sl2, -base), fmaf(sv[cc + 1], sl2, -base));
+            }
+            tc::tmem_st16(ts + h2 * 16, pk);
+            uint32_t acc2[2];
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              acc2[a] = pk[8 * a];
+#pragma unroll
+              for (int e = 1; e < 8; ++e) acc2[a] = hadd2(acc2[a], pk[8 * a + e]);
+            }
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&acc2[0]));
+            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&acc2[1]));
+            rs += (f0.x + f0.y) + (f1.x + f1.y);
+          }
+          l = l * factor + rs;
+          m_used = m_new;
+          // O_t holds the products of key tiles < f (all complete: S_t(f) was committed after
+          // them) and no product writes it until P_t(f) is published; rescaled after the
+          // exponentials, when the scores no longer occupy registers
+          if (f >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+              uint32_t ov[32];
+              tc::tmem_ld32(to + i * 32, ov);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+              tc::tmem_st32(to + i * 32, ov);
+            }
+          }
+          tc::tmem_wait_st();
+          tc::tc_fence_before();
+          tc::mbar_arrive(&bars[B_PFULL0 + t]);
         }
-        tc::tmem_wait_st();
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bars[B_PFULL0 + t]);
       }
-      if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OFULL0 + t], 0, abort, p.wait_ns));
-      if (ok) {
+      if (!ok) break;
+      // the next item's query tiles are rotated before this item's output rows are
+      // written, so that its first products overlap them
+      AttnItem nxt;
+      if (!(ok = fetch(nxt))) break;
+      if (nxt.ok && p.rotate_q && !(ok = rotate(nxt))) break;
+      if (mine) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OFULL0 + t], nO & 1, abort, p.wait_ns));
+        if (!ok) break;
+        ++nO;
         tc::tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint16_t* orow = p.o + (static_cast<int64_t>(seg_start + off + t * tile + tok) * p.Hq + g * G + hl) * D;
+        uint16_t* orow =
+            p.o + (static_cast<int64_t>(cur.seg_start + cur.off + t * tile + tok) * p.Hq + cur.g * G + hl) * D;
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
           uint32_t ov[32];
@@ -530,20 +655,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_wait_ld();
           if (tok < n_t) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int qq = 0; qq < 4; ++qq) {
               uint4 v4;
-              v4.x = pack_bf16(__uint_as_float(ov[q * 8 + 0]) * inv, __uint_as_float(ov[q * 8 + 1]) * inv);
-              v4.y = pack_bf16(__uint_as_float(ov[q * 8 + 2]) * inv, __uint_as_float(ov[q * 8 + 3]) * inv);
-              v4.z = pack_bf16(__uint_as_float(ov[q * 8 + 4]) * inv, __uint_as_float(ov[q * 8 + 5]) * inv);
-              v4.w = pack_bf16(__uint_as_float(ov[q * 8 + 6]) * inv, __uint_as_float(ov[q * 8 + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + i * 32 + q * 8) = v4;
+              v4.x = pack_bf16(__uint_as_float(ov[qq * 8 + 0]) * inv, __uint_as_float(ov[qq * 8 + 1]) * inv);
+              v4.y = pack_bf16(__uint_as_float(ov[qq * 8 + 2]) * inv, __uint_as_float(ov[qq * 8 + 3]) * inv);
+              v4.z = pack_bf16(__uint_as_float(ov[qq * 8 + 4]) * inv, __uint_as_float(ov[qq * 8 + 5]) * inv);
+              v4.w = pack_bf16(__uint_as_float(ov[qq * 8 + 6]) * inv, __uint_as_float(ov[qq * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + i * 32 + qq * 8) = v4;
             }
           }
         }
+        // O_t is read: the next item's first PV products may overwrite it
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars[B_OFREE0 + t]);
       }
+      cur = nxt;
     }
   }
-
   tc::tc_fence_before();
   __syncthreads();
   if (*abort && tid == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_TIMEOUT);
@@ -579,7 +707,9 @@ int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, boo
   p.checks = a.checks;
   p.stall = a.stall;
   p.wait_ns = a.wait_ns;
-  dim3 grid(grid_x, a.Hkv);
+  p.work_ctr = a.work_ctr;
+  // one CTA per SM over all (work item, kv head) pairs (fewer when there are fewer pairs)
+  const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(grid_x) * a.Hkv, sm_count()));
   attn_tc_kernel<D><<<grid, kThreads, LY::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cuda_rc(cudaGetLastError());
 }
