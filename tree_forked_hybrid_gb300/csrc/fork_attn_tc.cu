@@ -158,7 +158,7 @@ __device__ __forceinline__ void rotate_q_row(unsigned char* tile, int row, int t
   }
 }
 
-// One work item of a call: entry r of the longest-first order x kv head g.  Its query
+// One work item of a call: kv head g x entry r of the longest-first order (q = g n_work + r).  Its query
 // tokens, and its key ranges in fixed slots: 0 prefix rows kept outside the stream, 1
 // trunk, 2 own branch (an absent range has length 0).  Every role of a CTA computes it
 // from the tables by itself.
@@ -170,8 +170,11 @@ struct AttnItem {
 
 __device__ __forceinline__ AttnItem attn_item(const int32_t* meta, const MetaLayout& L, const TcParams& p, int q) {
   AttnItem it;
-  const int r = q / p.Hkv;
-  it.g = q - r * p.Hkv;
+  // head-major: the CTAs running at one time mostly share a kv head, so the K/V tiles
+  // they re-read stay in L2
+  const int nw = meta[H_NWORK];
+  it.g = q / nw;
+  const int r = q - it.g * nw;
   it.ok = 0;
   it.status = 0;
   it.total = 0;
