@@ -31,12 +31,12 @@ WORKLOAD_ID = 3
 METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one call of the full-
-# attention layer on this workload, summed over the call's launches (rotary tables, key and
-# query rotation, attention), from one ncu capture of this bench's command.  Keyed by the
+# attention layer on this workload, summed over the call's launches (rotary tables, key
+# rotation, fp16 value copy, attention), from one ncu capture of this bench's command.  Keyed by the
 # SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
 TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
                        "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
-           "sha256": None, "bytes": None}
+           "sha256": "846087ddd4713bfe74f33f2c23af59e912af4523f733ae0ec4bb2a959c8484d0", "bytes": 502141929}
 
 
 def _sources_sha256(paths):
