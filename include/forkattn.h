@@ -169,7 +169,8 @@ int fork_read_status(const fork_meta* m, int32_t* h_status, void* stream);
  * (with FORK_WARP_MMA also rotated queries: the default kernel rotates its query
  * tiles in shared memory); for the default kernel, the values of the stream and
  * of the prefix as fp16 (its PV product multiplies fp16 exponentials by fp16
- * values; inputs beyond the fp16 range, |v| > 65504, are not supported).
+ * values; inputs beyond the fp16 range, |v| > 65504, are not supported) and
+ * the counter through which its CTAs (one per SM) claim work items.
  * 0 only for FORK_WARP_MMA without the rotary embedding. */
 size_t fork_attn_workspace_bytes(int32_t T_cap, int32_t prefix_rows, int32_t Hq, int32_t Hkv,
                                  int32_t d, float rope_theta, uint32_t flags);
@@ -199,7 +200,8 @@ int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* k, const ui
  * runtime that plans all device memory ahead and forbids allocation in its
  * serving loop, because cudaMalloc and cudaFree synchronise the device).
  * Arguments and results are those of fork_attn without the workspace: the
- * scratch fork_attn needs (rotated keys, rotary tables) is taken from an array
+ * scratch fork_attn needs (rotated keys, rotary tables, fp16 values, the
+ * work-item counter) is taken from an array
  * of FORK_NOALLOC_SCRATCH_BYTES bytes owned by the library, which every GPU
  * that loads the library keeps allocated until the process exits.
  *   - Returns FORK_ECAPACITY when fork_attn_workspace_bytes(T_cap,
