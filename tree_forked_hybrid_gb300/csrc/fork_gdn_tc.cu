@@ -557,8 +557,8 @@ __global__ void __launch_bounds__(NT, 1)
       // lower-triangular matrix): first the 16 x 16 blocks (1,0) and (3,2), then the 32 x 32
       // block T_BA = -T_BB (A_BA T_AA) with T_AA, T_BB the two 32 x 32 diagonal blocks.
       // T's blocks (0,1) and (2,3) hold zeros, so the sums run over whole blocks; Y = A_BA T_AA
-      // goes to T's unused upper-right quarter.  Each thread keeps a block of rows x 4 columns
-      // in registers, so every value read from shared memory feeds several products.
+      // goes to T's unused upper-right quarter.  Each thread computes one row x 4 columns; the
+      // 4-column groups of a row are read once per warp (broadcast).
       // rows[i] (+)= sum_k X[r_i][k] * Z[k][c4..c4+3], X and Z row-major with stride ld
       auto blk = [&](float4* acc, int nr, const float* x0, const float* z0, int kn) {
 #pragma unroll 2
@@ -584,44 +584,37 @@ __global__ void __launch_bounds__(NT, 1)
         }
       };
       {
-        // level 1: 64 threads, product pr in {0, 1} -> blocks (2pr+1, 2pr); rows 2rp, 2rp+1
-        const int pr = stid >> 5, rp = (stid >> 2) & 7, c4 = (stid & 3) * 4;
+        // level 1: 128 threads, product pr in {0, 1} -> blocks (2pr+1, 2pr); row rp x columns c4..c4+3
+        const int pr = stid >> 6, rp = (stid >> 2) & 15, c4 = (stid & 3) * 4;
         const int bi = 2 * pr + 1, bj = 2 * pr;
         float* yb = tm + 32 + pr * 16;  // Y = A_ij T_jj [16][16] in T's upper-right quarter (free)
-        if (stid < 64) {
-          float4 acc[4] = {};
-          blk(acc, 2, am + (bi * 16 + 2 * rp) * LDC + bj * 16, tm + (bj * 16) * LDC + bj * 16 + c4, 16);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) *reinterpret_cast<float4*>(yb + (2 * rp + i) * LDC + c4) = acc[i];
+        if (stid < 128) {
+          float4 acc[1] = {};
+          blk(acc, 1, am + (bi * 16 + rp) * LDC + bj * 16, tm + (bj * 16) * LDC + bj * 16 + c4, 16);
+          *reinterpret_cast<float4*>(yb + rp * LDC + c4) = acc[0];
         }
         role_sync(3, NSV);
-        if (stid < 64) {
-          float4 acc[4] = {};
-          blk(acc, 2, tm + (bi * 16 + 2 * rp) * LDC + bi * 16, yb + c4, 16);
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            *reinterpret_cast<float4*>(tm + (bi * 16 + 2 * rp + i) * LDC + bj * 16 + c4) =
-                make_float4(-acc[i].x, -acc[i].y, -acc[i].z, -acc[i].w);
+        if (stid < 128) {
+          float4 acc[1] = {};
+          blk(acc, 1, tm + (bi * 16 + rp) * LDC + bi * 16, yb + c4, 16);
+          *reinterpret_cast<float4*>(tm + (bi * 16 + rp) * LDC + bj * 16 + c4) =
+              make_float4(-acc[0].x, -acc[0].y, -acc[0].z, -acc[0].w);
         }
         role_sync(3, NSV);
       }
       {
-        // level 2: 64 threads, rows 4rq..4rq+3 x columns c4..c4+3 of the 32 x 32 blocks
+        // level 2: all 256 threads, row rq x columns c4..c4+3 of the 32 x 32 blocks
         const int rq = stid >> 3, c4 = (stid & 7) * 4;
-        if (stid < 64) {
-          float4 acc[4] = {};
-          blk(acc, 4, am + (32 + 4 * rq) * LDC, tm + c4, 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(tm + (4 * rq + i) * LDC + 32 + c4) = acc[i];
+        {
+          float4 acc[1] = {};
+          blk(acc, 1, am + (32 + rq) * LDC, tm + c4, 32);
+          *reinterpret_cast<float4*>(tm + rq * LDC + 32 + c4) = acc[0];
         }
         role_sync(3, NSV);
-        if (stid < 64) {
-          float4 acc[4] = {};
-          blk(acc, 4, tm + (32 + 4 * rq) * LDC + 32, tm + 32 + c4, 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<float4*>(tm + (32 + 4 * rq + i) * LDC + c4) =
-                make_float4(-acc[i].x, -acc[i].y, -acc[i].z, -acc[i].w);
+        {
+          float4 acc[1] = {};
+          blk(acc, 1, tm + (32 + rq) * LDC + 32, tm + 32 + c4, 32);
+          *reinterpret_cast<float4*>(tm + (32 + rq) * LDC + c4) = make_float4(-acc[0].x, -acc[0].y, -acc[0].z, -acc[0].w);
         }
         role_sync(3, NSV);
       }
