@@ -59,7 +59,7 @@ constexpr int NT = NCV + NSV + NCH;
 constexpr int KW = 4;
 constexpr int HR = C + KW - 1;  // raw rows staged per chunk
 constexpr int LDC = C + 4;      // plain 64-wide fp32 tiles
-constexpr int kQG = 4;          // questions per CTA in the branch call
+constexpr int kQG = 4;          // questions per CTA in the branch call (8 measured the same)
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S (fp32), its fp16 copy, two U slots, X, the prep's product, two scaled
 // fp16 copies of U^T
@@ -83,12 +83,12 @@ struct Lay {
   static constexpr int GA = TM + C * LDC * 4;     // raw alpha, eta per slot [2][2][64]
   static constexpr int GS = GA + 2 * 2 * C * 4;   // per slot [G, EG, GL, ETA, IG, NQ, NK][64]
   static constexpr int SEG = GS + 2 * 7 * C * 4;  // this CTA's segments: start, len, pos0
-  static constexpr int BAR = SEG + 64;
+  static constexpr int BAR = SEG + (3 * kQG * 4 + 63) / 64 * 64;
   static constexpr int BYTES = BAR + 256;
   static constexpr int SMEM = BYTES + 1024;
 };
 static_assert(Lay::SMEM <= 232448, "shared memory budget");
-static_assert(3 * kQG * 4 <= 64, "segment table");
+static_assert(kQG * 3 <= NT, "segment table filled by one thread per entry");
 static_assert(Lay::YT % 1024 == 0 && Lay::YV % 1024 == 0 && Lay::WT % 1024 == 0 && Lay::PB % 1024 == 0 &&
                   Lay::TP % 1024 == 0 && Lay::TPP % 1024 == 0 && Lay::RAWH % 1024 == 0,
               "128-byte-swizzled tiles start on 1024-byte boundaries");
