@@ -288,12 +288,16 @@ int fork_readout(const fork_meta* m, const uint16_t* h, int32_t D, const uint16_
  *   p_i(o) = exp(w_o . z_i) / sum_{o' in O_i} exp(w_o' . z_i).
  *   h [T_cap, D] bf16 (rows read at each question's last token); g1, g2 [D]
  *   float32; w_gate, w_up [F, D] and w_down [D, F] bf16, row-major; w_opt,
- *   opt_off, p as for fork_readout.  D a multiple of 64, at most 8192; F a
+ *   opt_off, p as for fork_readout; h, g1, g2, the weights, w_opt and the
+ *   workspace 16-byte aligned.  D a multiple of 64, at most 8192; F a
  *   multiple of 64, at most 65536.  Products on the tensor cores with bf16
- *   operands and float32 accumulation; norms, SiLU and eq. (1) in float32.
+ *   operands and float32 accumulation (tcgen05, 128 output columns per CTA,
+ *   when D is a multiple of 128 and F of 256; else warp-level MMA); norms,
+ *   SiLU and eq. (1) in float32.
  *   workspace: device buffer of fork_readout_mlp_workspace_bytes(max_q, D,
  *   F) bytes, 16-byte aligned, owned by the caller (the normalised rows
- *   [Mpad, D] bf16, the activations [Mpad, F] bf16 and y [Mpad, D] float32,
+ *   [Mpad, D] bf16, the activations [Mpad, F] bf16, y [Mpad, D] float32 and,
+ *   on the tcgen05 path, the partial products [Mpad, max(2F, 4D)] float32,
  *   each at a 256-byte-aligned offset, Mpad = max_q rounded up to 64).
  *   FORK_EINVAL for null pointers, bad sizes, misaligned buffers or a short
  *   workspace, with nothing launched.

@@ -108,8 +108,12 @@ def test_readout_mlp_argument_errors_and_workspace_size(lib):
     ref = ctypes.byref(h)
     fake = ctypes.c_void_p(0x1000)
     ws_bytes = lib.fork_readout_mlp_workspace_bytes(8, 256, 512)
-    # Mpad = 64 rows: normalised rows (bf16), activations (bf16), y (float32)
-    assert ws_bytes == 64 * 256 * 2 + 64 * 512 * 2 + 64 * 256 * 4
+    # Mpad = 64 rows: normalised rows (bf16), activations (bf16), y (float32), and for the
+    # tensor-core products (D a multiple of 128, F of 256) the partial products, max(2F, 4D)
+    # float32 values per row
+    assert ws_bytes == 64 * 256 * 2 + 64 * 512 * 2 + 64 * 256 * 4 + 64 * max(2 * 512, 4 * 256) * 4
+    # shapes the tensor-core tiles do not divide: no partial products
+    assert lib.fork_readout_mlp_workspace_bytes(8, 192, 512) == 64 * 192 * 2 + 64 * 512 * 2 + 64 * 192 * 4
     assert lib.fork_readout_mlp_workspace_bytes(8, 100, 512) == 0     # D not a multiple of 64
     assert lib.fork_readout_mlp_workspace_bytes(8, 256, 96) == 0      # F not a multiple of 64
     assert lib.fork_readout_mlp_workspace_bytes(8, 16384, 512) == 0   # D above 8192

@@ -7,12 +7,19 @@
 //   y_i = h_i + W_down a_i
 //   z_i = rmsnorm(y_i) * g2,   p_i(o) = softmax_{o in O_i}(w_o . z_i)   (eq. (1))
 // rmsnorm(x) = x * (mean x^2 + 1e-6)^(-1/2).  Kernels: ro_norm_kernel (gather and
-// norm, a CTA per question), ro_gemm_kernel (bf16 warp-MMA products over the
-// question rows, each weight tile read once per 64-row tile: gate and up with the
-// SwiGLU epilogue, then down with the residual), ro_final_kernel (final norm and
-// eq. (1)).  Reductions run in a fixed order: a question's result does not depend
-// on the rest of the round.
-#include "fork_common.cuh"
+// norm, a CTA per question); ro_tc_kernel (tcgen05 products with the weight tile as
+// the A operand, 128 output columns per CTA, and the question rows as the B operand,
+// 64 per tile: each weight byte is read once and the rows once per 128 columns; the
+// down product's reduction is split over 4 CTAs) with ro_glu_kernel (SwiGLU) and
+// ro_down_kernel (sum of the 4 partial products in order + residual); ro_final_kernel
+// (final norm and eq. (1)).  ro_gemm_kernel (bf16 warp-MMA products, each weight tile
+// read once per 64-row tile) serves the block on every stream row and shapes the
+// tcgen05 tiles do not divide.  Reductions run in a fixed order: a question's result
+// does not depend on the rest of the round.
+#include <algorithm>
+
+#include "fork_attn.cuh"
+#include "tc_ptx.cuh"
 
 namespace fork {
 
@@ -23,6 +30,15 @@ constexpr int kNT = 32;    // output columns per CTA
 constexpr int kKC = 64;    // k per stage
 constexpr int kLD = kKC + 8;  // padded smem row (bf16): fragment loads hit 32 different banks
 constexpr float kEps = 1e-6f;
+// tcgen05 products of the selective block
+constexpr int kTcCols = 128;                  // output columns per CTA (MMA M)
+constexpr int kTcRows = 64;                   // question rows per tile (MMA N)
+constexpr int kTcK = 64;                      // k per stage: one 128-byte swizzled box
+constexpr int kTcStages = 6;
+constexpr int kTcWBox = kTcCols * 128;        // 16 KB
+constexpr int kTcStage = kTcWBox + kTcRows * 128;  // + 8 KB of question rows
+constexpr int kTcSplit = 4;                   // down product: reduction split over 4 CTAs
+constexpr int kTcSmem = kTcStages * kTcStage + 256 + 1024;
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
@@ -68,14 +84,33 @@ __global__ void __launch_bounds__(256) ro_norm_kernel(const int32_t* __restrict_
   if (meta[H_VALID] == 0) return;
   const int i = blockIdx.x;
   if (i >= ro_rows(meta, all)) return;
-  const uint16_t* x = h + static_cast<int64_t>(ro_src(meta, L, all, i)) * D;
+  // 8 elements (16 bytes) per access; every access of a pass issued before its sums
+  const uint4* x4 = reinterpret_cast<const uint4*>(h + static_cast<int64_t>(ro_src(meta, L, all, i)) * D);
+  const int nc = D / 8;
   float ss = 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    const float v = bf2f(x[d]);
-    ss += v * v;
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+    const uint4 v = x4[c];
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(wv[q] << 16), hi = __uint_as_float(wv[q] & 0xffff0000u);
+      ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+    }
   }
   const float inv = 1.f / sqrtf(block_sum(ss, red) / static_cast<float>(D) + kEps);
-  for (int d = threadIdx.x; d < D; d += blockDim.x) A[static_cast<int64_t>(i) * D + d] = f2bf(bf2f(x[d]) * inv * g1[d]);
+  const float4* g4 = reinterpret_cast<const float4*>(g1);
+  uint4* a4 = reinterpret_cast<uint4*>(A + static_cast<int64_t>(i) * D);
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+    const uint4 v = x4[c];
+    const float4 ga = g4[2 * c], gb = g4[2 * c + 1];
+    const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = pack2(__uint_as_float(wv[q] << 16) * inv * gv[2 * q], __uint_as_float(wv[q] & 0xffff0000u) * inv * gv[2 * q + 1]);
+    a4[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // C[r, n] over the question rows r of one 64-row tile and 32 columns n:
@@ -180,6 +215,138 @@ __global__ void __launch_bounds__(128) ro_gemm_kernel(const int32_t* __restrict_
   }
 }
 
+// P[z][r][n] = sum over k in this CTA's range of A[r][k] W[n][k] for the question rows r of
+// row tile blockIdx.y (64) and the columns n0..n0+127 of blockIdx.x: the weight tile is the
+// A operand of tcgen05.mma (M = 128), the question rows the B operand (N = 64), fp32 in
+// TMEM.  z = blockIdx.z selects the matrix (wmap0 for z < ks, else wmap1) and the k slice
+// z % ks of length k_len.  One thread loads (TMA, kTcStages-deep ring), one issues the
+// products; all 128 threads then read TMEM (thread = output column) and store row by row.
+// Rows past the question count are computed from whatever the row buffer holds there and not
+// stored (rows are independent).  Every wait is bounded.
+__global__ void __launch_bounds__(128, 1)
+    ro_tc_kernel(const __grid_constant__ CUtensorMap wmap0, const __grid_constant__ CUtensorMap wmap1,
+                 const __grid_constant__ CUtensorMap amap, const int32_t* __restrict__ meta, int N, int k_len, int ks,
+                 float* __restrict__ P, int rows_pad, uint64_t wait_ns) {
+  extern __shared__ __align__(1024) unsigned char ro_tc_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(ro_tc_raw) + 1023) &
+                                                       ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kTcStages * kTcStage);  // FULL[s], EMPTY[s], DONE
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kTcStages + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 2);
+  if (meta[H_VALID] == 0) return;
+  const int nq = meta[H_NQ];
+  const int m0 = blockIdx.y * kTcRows;
+  if (m0 >= nq) return;
+  const int n0 = blockIdx.x * kTcCols;
+  const int z = blockIdx.z, k0 = (z % ks) * k_len;
+  const int nst = k_len / kTcK;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < 2 * kTcStages + 1; ++i) tc::mbar_init(&bars[i], 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 64);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) {
+    // producer: weight box (64 k x 128 columns) and row box (64 k x 64 rows) per stage
+    const CUtensorMap* wm = z < ks ? &wmap0 : &wmap1;
+    tc::prefetch_tmap(wm);
+    tc::prefetch_tmap(&amap);
+    int issued = 0;
+    for (int i = 0; i < nst; ++i) {
+      const int s = i % kTcStages;
+      if (i >= kTcStages && !tc::mbar_wait(&bars[kTcStages + s], ((i / kTcStages) - 1) & 1, abort, wait_ns)) break;
+      unsigned char* st = sm + s * kTcStage;
+      tc::mbar_expect_tx(&bars[s], kTcStage);
+      tc::tma_load_3d(st, wm, &bars[s], k0 + i * kTcK, 0, n0);
+      tc::tma_load_3d(st + kTcWBox, &amap, &bars[s], k0 + i * kTcK, 0, m0);
+      issued = i + 1;
+    }
+    // the last copies into each slot complete by themselves
+    for (int i = max(0, issued - kTcStages); i < issued; ++i) tc::mbar_drain(&bars[i % kTcStages], (i / kTcStages) & 1);
+  } else if (tid == 32) {
+    // products: 4 k steps of 16 per stage, +32 bytes each in both operands
+    constexpr uint32_t idesc = tc::idesc_bf16(kTcCols, kTcRows, 0, 0);
+    for (int i = 0; i < nst; ++i) {
+      const int s = i % kTcStages;
+      if (!tc::mbar_wait(&bars[s], (i / kTcStages) & 1, abort, wait_ns)) break;
+      tc::tc_fence_after();
+      const uint64_t da = tc::sdesc_sw128(tc::smem_u32(sm + s * kTcStage), 16, 1024);
+      const uint64_t db = tc::sdesc_sw128(tc::smem_u32(sm + s * kTcStage + kTcWBox), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kTcK / 16; ++kk) tc::mma_bf16(tmem, da + kk * 2, db + kk * 2, idesc, (i | kk) ? 1u : 0u);
+      tc::mma_commit(&bars[kTcStages + s]);
+    }
+    tc::mma_commit(&bars[2 * kTcStages]);  // every product issued (also after an abort)
+  }
+  __syncwarp();
+  // the products are complete before TMEM is read or released; every thread then sees the
+  // same abort flag
+  tc::mbar_drain(&bars[2 * kTcStages], 0);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const bool aborted = *abort != 0;
+  if (!aborted) {
+    const int n = n0 + warp * 32 + lane;
+    float* out = P + static_cast<int64_t>(z) * rows_pad * N + n;
+    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+#pragma unroll
+    for (int c = 0; c < kTcRows; c += 32) {
+      uint32_t v[32];
+      tc::tmem_ld32(tmem + lb + c, v);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (m0 + c + e < nq) out[static_cast<int64_t>(m0 + c + e) * N] = __uint_as_float(v[e]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (aborted && tid == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_TIMEOUT);
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 64);
+  }
+}
+
+// a2[r][n] = bf16(silu(gate) * up), gate = P[0][r][n], up = P[1][r][n], for question rows r
+__global__ void __launch_bounds__(256) ro_glu_kernel(const int32_t* __restrict__ meta, const float* __restrict__ P,
+                                                     int F, int rows_pad, uint16_t* __restrict__ a2) {
+  if (meta[H_VALID] == 0) return;
+  const int64_t total = static_cast<int64_t>(meta[H_NQ]) * F;
+  const int64_t plane = static_cast<int64_t>(rows_pad) * F;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float g = P[e], u = P[plane + e];
+    a2[e] = f2bf(g / (1.f + __expf(-g)) * u);
+  }
+}
+
+// y[r][n] = (((P[0] + P[1]) + P[2]) + P[3])[r][n] + h_{q_last(r)}[n] for question rows r
+__global__ void __launch_bounds__(256) ro_down_kernel(const int32_t* __restrict__ meta, MetaLayout L,
+                                                      const float* __restrict__ P, int D, int rows_pad,
+                                                      const uint16_t* __restrict__ h, float* __restrict__ y) {
+  if (meta[H_VALID] == 0) return;
+  const int64_t total = static_cast<int64_t>(meta[H_NQ]) * D;
+  const int64_t plane = static_cast<int64_t>(rows_pad) * D;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(e / D), n = static_cast<int>(e - static_cast<int64_t>(r) * D);
+    float acc = P[e];
+#pragma unroll
+    for (int k = 1; k < kTcSplit; ++k) acc += P[k * plane + e];
+    y[e] = acc + bf2f(h[static_cast<int64_t>(meta[L.q_last + r]) * D + n]);
+  }
+}
+
 // z_i = rmsnorm(y_i) * g2 (shared memory), then eq. (1) over the question's options
 __global__ void __launch_bounds__(256) ro_final_kernel(const int32_t* __restrict__ meta, const float* __restrict__ Y,
                                                        int D, const float* __restrict__ g2,
@@ -190,20 +357,38 @@ __global__ void __launch_bounds__(256) ro_final_kernel(const int32_t* __restrict
   if (meta[H_VALID] == 0) return;
   const int i = blockIdx.x;
   if (i >= meta[H_NQ]) return;
-  const float* y = Y + static_cast<int64_t>(i) * D;
+  // 16-byte accesses throughout: y and g2 as float4, option weights as 8 bf16
+  const float4* y4 = reinterpret_cast<const float4*>(Y + static_cast<int64_t>(i) * D);
+  const float4* g4 = reinterpret_cast<const float4*>(g2);
+  float4* z4 = reinterpret_cast<float4*>(z);
   float ss = 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) ss += y[d] * y[d];
+  for (int c = threadIdx.x; c < D / 4; c += blockDim.x) {
+    const float4 v = y4[c];
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  }
   const float inv = 1.f / sqrtf(block_sum(ss, red) / static_cast<float>(D) + kEps);
-  for (int d = threadIdx.x; d < D; d += blockDim.x) z[d] = y[d] * inv * g2[d];
+  for (int c = threadIdx.x; c < D / 4; c += blockDim.x) {
+    const float4 v = y4[c], g = g4[c];
+    z4[c] = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
+  }
   __syncthreads();
   const int a = off[i], b = off[i + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int o = a + warp; o < b; o += blockDim.x / 32) {
-    const uint16_t* wr = w + static_cast<int64_t>(o) * D;
+    const uint4* w4 = reinterpret_cast<const uint4*>(w + static_cast<int64_t>(o) * D);
     float acc = 0.f;
-    for (int d = 2 * lane; d < D; d += 64) {
-      const uint32_t wv = *reinterpret_cast<const uint32_t*>(wr + d);
-      acc += bf2f(static_cast<uint16_t>(wv & 0xffffu)) * z[d] + bf2f(static_cast<uint16_t>(wv >> 16)) * z[d + 1];
+#pragma unroll 4
+    for (int c = lane; c < D / 8; c += 32) {
+      const uint4 wv = w4[c];
+      const float4 za = z4[2 * c], zb = z4[2 * c + 1];
+      acc = fmaf(__uint_as_float(wv.x << 16), za.x, acc);
+      acc = fmaf(__uint_as_float(wv.x & 0xffff0000u), za.y, acc);
+      acc = fmaf(__uint_as_float(wv.y << 16), za.z, acc);
+      acc = fmaf(__uint_as_float(wv.y & 0xffff0000u), za.w, acc);
+      acc = fmaf(__uint_as_float(wv.z << 16), zb.x, acc);
+      acc = fmaf(__uint_as_float(wv.z & 0xffff0000u), zb.y, acc);
+      acc = fmaf(__uint_as_float(wv.w << 16), zb.z, acc);
+      acc = fmaf(__uint_as_float(wv.w & 0xffff0000u), zb.w, acc);
     }
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     if (lane == 0) p[o] = acc;
@@ -237,17 +422,24 @@ __global__ void __launch_bounds__(256) ro_znorm_kernel(const int32_t* __restrict
 }
 
 struct RoWs {
-  size_t a1, a2, y, total;
+  size_t a1, a2, y, part, total;
 };
-static RoWs ro_ws(int64_t max_q, int64_t D, int64_t F) {
+// rows A of the first product (a1), of the second (a2), y; for the tcgen05 path of the
+// selective block also the partial products (max(2F, 4D) values per row)
+static RoWs ro_ws(int64_t max_q, int64_t D, int64_t F, bool tc) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   const int64_t M = (max_q + kMT - 1) / kMT * kMT;
   RoWs r;
   r.a1 = 0;
   r.a2 = al(r.a1 + static_cast<size_t>(M * D * 2));
   r.y = al(r.a2 + static_cast<size_t>(M * F * 2));
-  r.total = al(r.y + static_cast<size_t>(M * D * 4));
+  r.part = al(r.y + static_cast<size_t>(M * D * 4));
+  r.total = al(r.part + (tc ? static_cast<size_t>(M) * std::max<int64_t>(2 * F, kTcSplit * D) * 4 : 0));
   return r;
+}
+// the tcgen05 path takes D and F that its tiles divide
+static bool ro_tc_shapes(int64_t D, int64_t F) {
+  return D % kTcCols == 0 && F % kTcCols == 0 && F % (kTcSplit * kTcK) == 0;
 }
 
 }  // namespace fork
@@ -256,7 +448,7 @@ using namespace fork;
 
 extern "C" size_t fork_readout_mlp_workspace_bytes(int32_t max_q, int32_t D, int32_t F) {
   if (max_q < 0 || D < 64 || D % 64 != 0 || D > 8192 || F < 64 || F % 64 != 0 || F > 65536) return 0;
-  return ro_ws(max_q, D, F).total;
+  return ro_ws(max_q, D, F, ro_tc_shapes(D, F)).total;
 }
 
 extern "C" int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D, int32_t F, const float* g1,
@@ -270,9 +462,10 @@ extern "C" int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D
   if (!h || !g1 || !w_gate || !w_up || !w_down || !g2 || !w_opt || !opt_off || !p || !workspace) return FORK_EINVAL;
   if (D < 64 || D % 64 != 0 || D > 8192 || F < 64 || F % 64 != 0 || F > 65536) return FORK_EINVAL;
   if (!is_aligned16(h) || !is_aligned16(w_gate) || !is_aligned16(w_up) || !is_aligned16(w_down) ||
-      !is_aligned16(w_opt) || !is_aligned16(workspace))
+      !is_aligned16(w_opt) || !is_aligned16(g1) || !is_aligned16(g2) || !is_aligned16(workspace))
     return FORK_EINVAL;
-  const RoWs w = ro_ws(m->max_q, D, F);
+  const bool tc = ro_tc_shapes(D, F);
+  const RoWs w = ro_ws(m->max_q, D, F, tc);
   if (ws_bytes < w.total) return FORK_EINVAL;
   if ((rc = check_device()) != FORK_OK) return rc;
   if (m->max_q == 0) return FORK_OK;
@@ -284,8 +477,35 @@ extern "C" int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D
   const int32_t* meta = static_cast<const int32_t*>(m->d_buf);
   const int mt = (m->max_q + kMT - 1) / kMT;
   ro_norm_kernel<<<m->max_q, 256, 0, s>>>(meta, L, h, D, g1, a1, 0);
-  ro_gemm_kernel<true><<<dim3(F / kNT, mt), 128, 0, s>>>(meta, L, a1, D, F, w_gate, w_up, a2, nullptr, nullptr, 0);
-  ro_gemm_kernel<false><<<dim3(D / kNT, mt), 128, 0, s>>>(meta, L, a2, F, D, w_down, nullptr, nullptr, y, h, 0);
+  if (tc) {
+    // tensor maps: weights [N rows, K] and question rows [mt * 64, K], 64-element boxes
+    const int rows_pad = mt * kMT;
+    float* part = reinterpret_cast<float*>(ws + w.part);
+    alignas(64) CUtensorMap mg, mu, md, ma1, ma2;
+    if (!encode_map_3d(&mg, w_gate, D, 1, F, kTcK, 1, kTcCols, true) ||
+        !encode_map_3d(&mu, w_up, D, 1, F, kTcK, 1, kTcCols, true) ||
+        !encode_map_3d(&md, w_down, F, 1, D, kTcK, 1, kTcCols, true) ||
+        !encode_map_3d(&ma1, a1, D, 1, rows_pad, kTcK, 1, kTcRows, true) ||
+        !encode_map_3d(&ma2, a2, F, 1, rows_pad, kTcK, 1, kTcRows, true))
+      return FORK_ECUDA;
+    static const int attr = [] {
+      return cudaFuncSetAttribute(ro_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) == cudaSuccess
+                 ? static_cast<int>(FORK_OK)
+                 : static_cast<int>(FORK_ECUDA);
+    }();
+    if (attr != FORK_OK) return attr;
+    const uint64_t wns = wait_ns_of(m);
+    const int eblocks = static_cast<int>(std::min<int64_t>((static_cast<int64_t>(m->max_q) * F + 255) / 256, 8 * sm_count()));
+    ro_tc_kernel<<<dim3(F / kTcCols, mt, 2), 128, kTcSmem, s>>>(mg, mu, ma1, meta, F, D, 1, part, rows_pad, wns);
+    ro_glu_kernel<<<std::max(eblocks, 1), 256, 0, s>>>(meta, part, F, rows_pad, a2);
+    ro_tc_kernel<<<dim3(D / kTcCols, mt, kTcSplit), 128, kTcSmem, s>>>(md, md, ma2, meta, D, F / kTcSplit, kTcSplit,
+                                                                       part, rows_pad, wns);
+    const int dblocks = static_cast<int>(std::min<int64_t>((static_cast<int64_t>(m->max_q) * D + 255) / 256, 8 * sm_count()));
+    ro_down_kernel<<<std::max(dblocks, 1), 256, 0, s>>>(meta, L, part, D, rows_pad, h, y);
+  } else {
+    ro_gemm_kernel<true><<<dim3(F / kNT, mt), 128, 0, s>>>(meta, L, a1, D, F, w_gate, w_up, a2, nullptr, nullptr, 0);
+    ro_gemm_kernel<false><<<dim3(D / kNT, mt), 128, 0, s>>>(meta, L, a2, F, D, w_down, nullptr, nullptr, y, h, 0);
+  }
   const int zbytes = D * 4;
   if (zbytes > 48 * 1024 &&
       cuda_rc(cudaFuncSetAttribute(ro_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, zbytes)) != FORK_OK)
@@ -296,7 +516,7 @@ extern "C" int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D
 
 extern "C" size_t fork_pointwise_rows_workspace_bytes(int32_t T_cap, int32_t D, int32_t F) {
   if (T_cap < 1 || D < 64 || D % 64 != 0 || D > 8192 || F < 64 || F % 64 != 0 || F > 65536) return 0;
-  return ro_ws(T_cap, D, F).total;
+  return ro_ws(T_cap, D, F, false).total;
 }
 
 extern "C" int fork_pointwise_rows(const fork_meta* m, const uint16_t* h, int32_t D, int32_t F, const float* g1,
@@ -310,9 +530,9 @@ extern "C" int fork_pointwise_rows(const fork_meta* m, const uint16_t* h, int32_
   if (!h || !g1 || !w_gate || !w_up || !w_down || !g2 || !z || !workspace) return FORK_EINVAL;
   if (D < 64 || D % 64 != 0 || D > 8192 || F < 64 || F % 64 != 0 || F > 65536) return FORK_EINVAL;
   if (!is_aligned16(h) || !is_aligned16(w_gate) || !is_aligned16(w_up) || !is_aligned16(w_down) ||
-      !is_aligned16(z) || !is_aligned16(workspace))
+      !is_aligned16(g1) || !is_aligned16(z) || !is_aligned16(workspace))
     return FORK_EINVAL;
-  const RoWs w = ro_ws(L.T_cap, D, F);
+  const RoWs w = ro_ws(L.T_cap, D, F, false);
   if (ws_bytes < w.total) return FORK_EINVAL;
   if ((rc = check_device()) != FORK_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
