@@ -10,9 +10,9 @@
 // norm, a CTA per question); ro_tc_kernel (tcgen05 products with the weight tile as
 // the A operand, 128 output columns per CTA, and the question rows as the B operand,
 // 64 per tile: each weight byte is read once and the rows once per 128 columns; the
-// down product's reduction is split over 4 CTAs) with ro_glu_kernel (SwiGLU) and
-// ro_down_kernel (sum of the 4 partial products in order + residual); ro_final_kernel
-// (final norm and eq. (1)).  ro_gemm_kernel (bf16 warp-MMA products, each weight tile
+// down product's reduction is split over 4 CTAs) with ro_glu_kernel (SwiGLU);
+// ro_final_kernel (the 4 partial products summed in order + the residual, final norm
+// and eq. (1)).  ro_gemm_kernel (bf16 warp-MMA products, each weight tile
 // read once per 64-row tile) serves the block on every stream row and shapes the
 // tcgen05 tiles do not divide.  Reductions run in a fixed order: a question's result
 // does not depend on the rest of the round.
@@ -330,26 +330,13 @@ __global__ void __launch_bounds__(256) ro_glu_kernel(const int32_t* __restrict__
   }
 }
 
-// y[r][n] = (((P[0] + P[1]) + P[2]) + P[3])[r][n] + h_{q_last(r)}[n] for question rows r
-__global__ void __launch_bounds__(256) ro_down_kernel(const int32_t* __restrict__ meta, MetaLayout L,
-                                                      const float* __restrict__ P, int D, int rows_pad,
-                                                      const uint16_t* __restrict__ h, float* __restrict__ y) {
-  if (meta[H_VALID] == 0) return;
-  const int64_t total = static_cast<int64_t>(meta[H_NQ]) * D;
-  const int64_t plane = static_cast<int64_t>(rows_pad) * D;
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(e / D), n = static_cast<int>(e - static_cast<int64_t>(r) * D);
-    float acc = P[e];
-#pragma unroll
-    for (int k = 1; k < kTcSplit; ++k) acc += P[k * plane + e];
-    y[e] = acc + bf2f(h[static_cast<int64_t>(meta[L.q_last + r]) * D + n]);
-  }
-}
-
-// z_i = rmsnorm(y_i) * g2 (shared memory), then eq. (1) over the question's options
-__global__ void __launch_bounds__(256) ro_final_kernel(const int32_t* __restrict__ meta, const float* __restrict__ Y,
-                                                       int D, const float* __restrict__ g2,
+// z_i = rmsnorm(y_i) * g2 (shared memory), then eq. (1) over the question's options.  With
+// partial products P (the tcgen05 path), y_i is first formed here as the sum of the
+// kTcSplit partials in order plus h_{q_last(i)}, and stored to Y.
+__global__ void __launch_bounds__(256) ro_final_kernel(const int32_t* __restrict__ meta, MetaLayout L,
+                                                       float* __restrict__ Y, const float* __restrict__ P,
+                                                       int rows_pad, const uint16_t* __restrict__ h, int D,
+                                                       const float* __restrict__ g2,
                                                        const uint16_t* __restrict__ w,
                                                        const int32_t* __restrict__ off, float* __restrict__ p) {
   extern __shared__ float z[];
@@ -358,9 +345,31 @@ __global__ void __launch_bounds__(256) ro_final_kernel(const int32_t* __restrict
   const int i = blockIdx.x;
   if (i >= meta[H_NQ]) return;
   // 16-byte accesses throughout: y and g2 as float4, option weights as 8 bf16
-  const float4* y4 = reinterpret_cast<const float4*>(Y + static_cast<int64_t>(i) * D);
+  float4* y4 = reinterpret_cast<float4*>(Y + static_cast<int64_t>(i) * D);
   const float4* g4 = reinterpret_cast<const float4*>(g2);
   float4* z4 = reinterpret_cast<float4*>(z);
+  if (P) {
+    const int64_t plane = static_cast<int64_t>(rows_pad) * D;
+    const float4* p4 = reinterpret_cast<const float4*>(P + static_cast<int64_t>(i) * D);
+    const uint2* h4 = reinterpret_cast<const uint2*>(h + static_cast<int64_t>(meta[L.q_last + i]) * D);
+    for (int c = threadIdx.x; c < D / 4; c += blockDim.x) {
+      float4 acc = p4[c];
+#pragma unroll
+      for (int k = 1; k < kTcSplit; ++k) {
+        const float4 q = p4[k * plane / 4 + c];
+        acc.x += q.x;
+        acc.y += q.y;
+        acc.z += q.z;
+        acc.w += q.w;
+      }
+      const uint2 hv = h4[c];
+      acc.x += __uint_as_float(hv.x << 16);
+      acc.y += __uint_as_float(hv.x & 0xffff0000u);
+      acc.z += __uint_as_float(hv.y << 16);
+      acc.w += __uint_as_float(hv.y & 0xffff0000u);
+      y4[c] = acc;  // read back below by the same thread
+    }
+  }
   float ss = 0.f;
   for (int c = threadIdx.x; c < D / 4; c += blockDim.x) {
     const float4 v = y4[c];
@@ -500,8 +509,6 @@ extern "C" int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D
     ro_glu_kernel<<<std::max(eblocks, 1), 256, 0, s>>>(meta, part, F, rows_pad, a2);
     ro_tc_kernel<<<dim3(D / kTcCols, mt, kTcSplit), 128, kTcSmem, s>>>(md, md, ma2, meta, D, F / kTcSplit, kTcSplit,
                                                                        part, rows_pad, wns);
-    const int dblocks = static_cast<int>(std::min<int64_t>((static_cast<int64_t>(m->max_q) * D + 255) / 256, 8 * sm_count()));
-    ro_down_kernel<<<std::max(dblocks, 1), 256, 0, s>>>(meta, L, part, D, rows_pad, h, y);
   } else {
     ro_gemm_kernel<true><<<dim3(F / kNT, mt), 128, 0, s>>>(meta, L, a1, D, F, w_gate, w_up, a2, nullptr, nullptr, 0);
     ro_gemm_kernel<false><<<dim3(D / kNT, mt), 128, 0, s>>>(meta, L, a2, F, D, w_down, nullptr, nullptr, y, h, 0);
@@ -510,7 +517,8 @@ extern "C" int fork_readout_mlp(const fork_meta* m, const uint16_t* h, int32_t D
   if (zbytes > 48 * 1024 &&
       cuda_rc(cudaFuncSetAttribute(ro_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, zbytes)) != FORK_OK)
     return FORK_ECUDA;
-  ro_final_kernel<<<m->max_q, 256, zbytes, s>>>(meta, y, D, g2, w_opt, opt_off, p);
+  ro_final_kernel<<<m->max_q, 256, zbytes, s>>>(meta, L, y, tc ? reinterpret_cast<const float*>(ws + w.part) : nullptr,
+                                                 mt * kMT, h, D, g2, w_opt, opt_off, p);
   return cuda_rc(cudaGetLastError());
 }
 
