@@ -607,68 +607,109 @@ def attn_kernel_alone(torch, dr, rnd, stream, reps=10):
     return statistics.mean(x.elapsed_time(y) for x, y in evs)
 
 
-def e2e(torch, dr, rnd, args, stream, dist, local, ws):
-    """Same metric through the public API with host buffers: every step copies
-    the round's inputs from pinned host memory, runs the layer and reads the
-    option probabilities back."""
+def e2e(torch, dr, rnd, args, stream, dist, local, ws, n_copy_streams=4):
+    """Same metric through the public API with host buffers: every step copies the round's
+    inputs from pinned host memory, runs the layer and reads the option probabilities back.
+    Steps are pipelined as a server would run them: two device buffer sets take turns, so
+    step s+1's copies (spread over several copy streams) run while step s computes; a copy
+    into a buffer set waits until the step that last read it has finished."""
+    from tree_forked_hybrid_gb300.runner import DeviceRound
     T = rnd.T
+    rounds = [dr, DeviceRound(rnd, max_req=dr.max_req, max_q=dr.max_q, flags=dr.flags)]
+
+    def dev_tensors(d):
+        out = []
+        for name, lay in d.inputs.items():
+            for k, t in lay.items():
+                out.append(t if k == "conv_w" else t[:T])
+        return out + [d.desc, d.w_opt, d.opt_off]
+
+    devs = [dev_tensors(d) for d in rounds]
     host = []
-    h2d = 0
-    for name, lay in dr.inputs.items():
-        for k, t in lay.items():
-            rows = t if k == "conv_w" else t[:T]
-            hp = torch.empty(rows.shape, dtype=rows.dtype, pin_memory=True)
-            hp.copy_(rows.cpu())
-            host.append((hp, rows))
-            h2d += hp.numel() * hp.element_size()
-    for src in (dr.desc, dr.w_opt, dr.opt_off):
-        hp = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
-        hp.copy_(src.cpu())
-        host.append((hp, src))
-        h2d += hp.numel() * hp.element_size()
-    p_host = torch.empty(dr.p.shape, dtype=dr.p.dtype, pin_memory=True)
-    d2h = p_host.numel() * p_host.element_size()
+    for t in devs[0]:
+        hp = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        hp.copy_(t.cpu())
+        host.append(hp)
+    h2d = sum(hp.numel() * hp.element_size() for hp in host)
+    # largest copies first, each to the least loaded copy stream
+    cstreams = [torch.cuda.Stream() for _ in range(n_copy_streams)]
+    load = [0] * n_copy_streams
+    which = [0] * len(host)
+    for i in sorted(range(len(host)), key=lambda i: -host[i].numel() * host[i].element_size()):
+        j = load.index(min(load))
+        which[i] = j
+        load[j] += host[i].numel() * host[i].element_size()
+    p_host = [torch.empty(d.p.shape, dtype=d.p.dtype, pin_memory=True) for d in rounds]
+    d2h = p_host[0].numel() * p_host[0].element_size()
+    free = [None, None]  # per buffer set: the compute of the step that last read it is done
 
-    ev = []
+    def copies(b, after):
+        done = []
+        for j, cs in enumerate(cstreams):
+            cs.wait_event(after)
+            with torch.cuda.stream(cs):
+                for i, hp in enumerate(host):
+                    if which[i] == j:
+                        devs[b][i].copy_(hp, non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(cs)
+            done.append(e)
+        return done
 
-    def step(mark=False):
-        e = _events(torch, 3) if mark else None
-        for hp, dev in host:
-            dev.copy_(hp, non_blocking=True)
-        if mark:
-            e[0].record(stream)
-        dr.run()
-        if mark:
-            e[1].record(stream)
-        p_host.copy_(dr.p, non_blocking=True)
-        if mark:
-            e[2].record(stream)
-            ev.append(e)
+    def step(s, start):
+        b = s % 2
+        ready = copies(b, free[b] if free[b] is not None else start)
+        for e in ready:
+            stream.wait_event(e)
+        rounds[b].run(stream)
+        p_host[b].copy_(rounds[b].p, non_blocking=True)
+        f = torch.cuda.Event()
+        f.record(stream)
+        free[b] = f
 
-    for _ in range(max(args.warmup, 3)):
-        step()
+    def run_steps(n):
+        start = torch.cuda.Event()
+        start.record(stream)
+        for s in range(n):
+            step(s, start)
+
+    run_steps(max(args.warmup, 3))
     torch.cuda.synchronize()
+    free[0] = free[1] = None
     if dist:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    for s in range(args.steps):
+        step(s, e0)
     e1.record(stream)
     torch.cuda.synchronize()
     ms, tokens_all = aggregate_over_ranks(torch, dist, f"cuda:{local}", e0.elapsed_time(e1), T)
-    # split of one step into its parts (a separate pass with events between the parts)
+    for d in rounds:
+        if d.status() != 0:
+            raise RuntimeError(f"device status {d.status():#x}")
+    # each part of one step timed alone (no overlap): copies, layer, read-back
+    parts = []
     for _ in range(min(args.steps, 10)):
-        step(mark=True)
+        e = _events(torch, 4)
+        e[0].record(stream)
+        for ev in copies(0, e[0]):
+            stream.wait_event(ev)
+        e[1].record(stream)
+        rounds[0].run(stream)
+        e[2].record(stream)
+        p_host[0].copy_(rounds[0].p, non_blocking=True)
+        e[3].record(stream)
+        parts.append(e)
     torch.cuda.synchronize()
-    compute = statistics.mean(a[0].elapsed_time(a[1]) for a in ev)
-    d2h_ms = statistics.mean(a[1].elapsed_time(a[2]) for a in ev)
+    split = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in parts) for i in range(3)]
     per_step = ms / args.steps
     return {"value": tokens_all * args.steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": per_step,
-            "split_ms": {"h2d": max(per_step - compute - d2h_ms, 0.0), "compute": compute, "d2h": d2h_ms,
-                         "note": "h2d = step time minus the event-timed compute and read-back"}}
+            "split_ms": {"h2d": split[0], "compute": split[1], "d2h": split[2],
+                         "note": f"each part timed alone; in the timed steps each step's copies ({n_copy_streams} "
+                                 "copy streams) overlap the previous step's layer (two device buffer sets)"}}
 
 
 if __name__ == "__main__":
