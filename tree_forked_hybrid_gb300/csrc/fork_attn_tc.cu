@@ -12,26 +12,35 @@
 // element is produced by the same sequence of operations whatever else the
 // round holds.
 //
-// One CTA = one work item x one kv head = up to two 128-row query tiles
-// (rows = token x grouped head) that share every K/V tile, 10 warps:
-//   warp 1 (one lane)   TMA producer: both Q tiles once, then K and V tiles
-//                       into two 2-stage rings (K and V slots are freed by
-//                       their own readers);
-//   warp 0              MMA issuer (lane 0) and TMEM owner.  Per key tile j,
-//                       for each query tile t: O_t += P_t(j-1) V(j-1), then
-//                       S_t = Q_t K(j)^T; the two tiles alternate so one
-//                       tile's softmax overlaps the other tile's products;
-//   warps 2-5 / 6-9     softmax of tile 0 / tile 1, one query row per thread
-//                       (warp w reads TMEM lanes 32 (w mod 4) ..; row = tid mod 128):
-//                       S from TMEM, mask, online softmax in the log2 domain
-//                       (the running maximum only moves when it grows by more
-//                       than 2^8, so O is rescaled rarely), P as bf16 written
-//                       back into the TMEM columns of S, where the PV product
-//                       reads it as its A operand; at the end O / l.
+// A work item x one kv head = up to two 128-row query tiles (rows = token x
+// grouped head) that share every K/V tile.  The kernel is persistent: one CTA
+// per SM takes items longest first (blockIdx.x, then the next unclaimed one
+// through an atomic counter), 10 warps:
+//   warp 1 (one lane)   claims items and hands them to the other warps through
+//                       a ring in shared memory; TMA producer: both Q tiles of
+//                       an item (once the previous item's QK^T products have
+//                       read theirs), then K and V tiles into two 2-stage rings
+//                       (K and V of a slot complete one barrier; slots are freed
+//                       by their readers), running on into the next item;
+//   warp 0              MMA issuer (lane 0) and TMEM owner.  Per key tile j:
+//                       O_0 += P_0(j-1) V(j-1), S_0 = Q_0 K(j)^T, then the same
+//                       for tile 1, so one tile's softmax overlaps the other
+//                       tile's products; an item's first PV products overwrite
+//                       O_t once the previous item's rows have been read;
+//   warps 2-5 / 6-9     rotary embedding of tile 0 / 1 in shared memory, then
+//                       its softmax, one query row per thread (warp w reads
+//                       TMEM lanes 32 (w mod 4) ..; row = tid mod 128): S from
+//                       TMEM, mask, online softmax in the log2 domain (the
+//                       running maximum only moves when it grows by more than
+//                       2^8, so O is rescaled rarely), P as fp16 written back
+//                       into the TMEM columns of S, where the PV product reads
+//                       it as its A operand; at the end O / l.  The next item's
+//                       query tiles are rotated before this item's output rows
+//                       are written.
 // TMEM: S/P of tile t at columns 128t, O_t at 256 + t*D (512 columns).
-// Operands are bf16, accumulation f32 in TMEM.  Every wait is bounded; on a
-// timeout the CTA raises the status bit, drains its own copies and MMAs,
-// frees TMEM and exits.
+// QK^T operands are bf16, PV operands fp16 (values converted once per call),
+// accumulation f32 in TMEM.  Every wait is bounded; on a timeout the CTA raises
+// the status bit, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda_fp16.h>
 
 #include "fork_attn.cuh"
