@@ -36,7 +36,7 @@ METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 # SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
 TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
                        "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
-           "sha256": "3b369cb9c91e4ea5c5b1c1c7d7328459732a0a0210bb8542a805d0cb25486e92", "bytes": 502141929}
+           "sha256": "a7dfff50f92e9ee99e1fa4a38d0aefa3d22d4c46d6150df25e7d914edc5dca05", "bytes": 501893679}
 
 
 def _sources_sha256(paths):

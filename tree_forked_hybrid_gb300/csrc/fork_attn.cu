@@ -39,105 +39,108 @@ __global__ void rope_tables_kernel(float2* hi, int hi_rows, float2* lo, int half
 }
 
 // Rotate every row of a stream tensor [T_cap, heads, D] (position from the
-// metadata) and of a prefix tensor [prefix_rows, heads, D] (position = row
-// index inside its request's prefix) into the workspace.  A thread rotates 8
-// pairs (one 16-byte piece of each half) of one head in kRopeRows rows; a block
-// of 256 threads covers kRopeRows * max(1, 256 / (heads * D / 16)) whole rows,
-// so the rows, head and pair group of each thread are fixed (no index division in
-// a loop), and all of a thread's loads are issued before its arithmetic.
-constexpr int kRopeRows = 4;
-
+// metadata) and of a prefix tensor [prefix_rows, heads, D] (position = row index
+// inside its request's prefix) into the workspace.  A thread takes 8 pairs (one
+// 16-byte piece of each half) of one row for every head: the pairs' (cos, sin)
+// are formed once from the two tables, and the loads of 8 heads are issued before
+// their rotation; a block of 256 threads covers 256 / (D / 16) rows.
 template <int D>
 __global__ void __launch_bounds__(256) rope_rows_kernel(const int32_t* __restrict__ meta, MetaLayout L,
                                  const uint16_t* __restrict__ k, const uint16_t* __restrict__ pk,
                                  uint16_t* __restrict__ kr, uint16_t* __restrict__ pkr,
-                                 int prefix_rows, int Hkv, const float2* __restrict__ hi,
+                                 int prefix_rows, int heads, const float2* __restrict__ hi,
                                  const float2* __restrict__ lo, int hi_rows) {
   if (meta[H_VALID] == 0) return;
   constexpr int HALF = D / 2;
-  constexpr int GRP = HALF / 8;  // 8 pairs per thread: one 16-byte load from each half
-  const int per_row = Hkv * GRP;
-  const int nr = per_row >= 256 ? 1 : 256 / per_row;  // rows per block and step
+  constexpr int GRP = HALF / 8;  // 8-pair groups per row
+  constexpr int RPB = 256 / GRP;  // rows per block
   const int T = meta[H_T];
   const int R = meta[H_R];
   const int64_t rows = static_cast<int64_t>(T) + prefix_rows;
-  for (int item = threadIdx.x; item < nr * per_row; item += blockDim.x) {
-    const int r_local = item / per_row, rem = item - r_local * per_row;
-    const int head = rem / GRP, i0 = (rem % GRP) * 8;
-    int tpos[kRopeRows];
-    uint4 xa[kRopeRows], xb[kRopeRows];
-    uint16_t* dst[kRopeRows];
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / GRP;
+  const int i0 = (threadIdx.x % GRP) * 8;
+  if (row >= rows) return;
+  int t;
+  const uint16_t* src;
+  uint16_t* dst;
+  if (row < T) {
+    t = meta[L.tok_pos + row];
+    src = k + row * heads * D;
+    dst = kr + row * heads * D;
+  } else {
+    const int pr = static_cast<int>(row - T);
+    // request owning prefix row pr: last j with prefix_off[j] <= pr
+    int a = 0, b = R;
+    while (b - a > 1) {
+      const int mid = (a + b) >> 1;
+      if (meta[L.req_prefix_off + mid] <= pr) a = mid; else b = mid;
+    }
+    t = pr - meta[L.req_prefix_off + a];
+    src = pk + static_cast<int64_t>(pr) * heads * D;
+    dst = pkr + static_cast<int64_t>(pr) * heads * D;
+  }
+  if (t < 0 || (t >> 6) >= hi_rows) {
+    // position beyond the rotary table: the prefix buffers given to fork_attn are
+    // shorter than the descriptor's prefix lengths
+    atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
+    return;
+  }
+  // (cos, sin) of pairs i0..i0+7 at position t = 64 a + b, by angle addition
+  const float4* A = reinterpret_cast<const float4*>(hi + static_cast<int64_t>(t >> 6) * HALF + i0);
+  const float4* B = reinterpret_cast<const float4*>(lo + static_cast<int64_t>(t & 63) * HALF + i0);
+  float cs[8], sn[8];
 #pragma unroll
-    for (int j = 0; j < kRopeRows; ++j) {
-      const int64_t row = (static_cast<int64_t>(blockIdx.x) * kRopeRows + j) * nr + r_local;
-      dst[j] = nullptr;
-      tpos[j] = -1;
-      if (row >= rows) continue;
-      const int64_t rh = row * Hkv + head;  // row * heads + head
-      const uint16_t* src;
-      if (row < T) {
-        tpos[j] = meta[L.tok_pos + row];
-        src = k + rh * D;
-        dst[j] = kr + rh * D;
-      } else {
-        const int pr = static_cast<int>(row - T);
-        // request owning prefix row pr: last j with prefix_off[j] <= pr
-        int a = 0, b = R;
-        while (b - a > 1) {
-          const int mid = (a + b) >> 1;
-          if (meta[L.req_prefix_off + mid] <= pr) a = mid; else b = mid;
-        }
-        tpos[j] = pr - meta[L.req_prefix_off + a];
-        src = pk + (rh - static_cast<int64_t>(T) * Hkv) * D;
-        dst[j] = pkr + (rh - static_cast<int64_t>(T) * Hkv) * D;
+  for (int q = 0; q < 4; ++q) {
+    const float4 a4 = A[q], b4 = B[q];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float ac = e ? a4.z : a4.x, as = e ? a4.w : a4.y;
+      const float bc = e ? b4.z : b4.x, bs = e ? b4.w : b4.y;
+      cs[2 * q + e] = ac * bc - as * bs;
+      sn[2 * q + e] = as * bc + ac * bs;
+    }
+  }
+  for (int h0 = 0; h0 < heads; h0 += 8) {
+    const int nh = min(8, heads - h0);
+    uint4 xa[8], xb[8];
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh) {
+      if (hh < nh) {
+        xa[hh] = *reinterpret_cast<const uint4*>(src + (h0 + hh) * D + i0);
+        xb[hh] = *reinterpret_cast<const uint4*>(src + (h0 + hh) * D + i0 + HALF);
       }
-      xa[j] = *reinterpret_cast<const uint4*>(src + i0);
-      xb[j] = *reinterpret_cast<const uint4*>(src + i0 + HALF);
     }
 #pragma unroll
-    for (int j = 0; j < kRopeRows; ++j) {
-      if (dst[j] == nullptr) continue;
-      const int t = tpos[j];
-      if (t < 0 || (t >> 6) >= hi_rows) {
-        // position beyond the rotary table: the prefix buffers given to fork_attn are
-        // shorter than the descriptor's prefix lengths
-        atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
-        continue;
-      }
-      const float4* A = reinterpret_cast<const float4*>(hi + static_cast<int64_t>(t >> 6) * HALF + i0);
-      const float4* B = reinterpret_cast<const float4*>(lo + static_cast<int64_t>(t & 63) * HALF + i0);
-      const uint32_t aw[4] = {xa[j].x, xa[j].y, xa[j].z, xa[j].w}, bw[4] = {xb[j].x, xb[j].y, xb[j].z, xb[j].w};
+    for (int hh = 0; hh < 8; ++hh) {
+      if (hh >= nh) continue;
+      const uint32_t aw[4] = {xa[hh].x, xa[hh].y, xa[hh].z, xa[hh].w};
+      const uint32_t bw[4] = {xb[hh].x, xb[hh].y, xb[hh].z, xb[hh].w};
       uint32_t oa[4], ob[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {  // pairs i0+2q, i0+2q+1
-        const float4 a4 = A[q], b4 = B[q];  // (cos, sin) of the two pairs for 64*(t>>6) and t&63
+      for (int q = 0; q < 4; ++q) {
         float ya[2], yb[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float ac = e ? a4.z : a4.x, as = e ? a4.w : a4.y;
-          const float bc = e ? b4.z : b4.x, bs = e ? b4.w : b4.y;
-          const float cs = ac * bc - as * bs, sn = as * bc + ac * bs;
           const float x0 = bf2f(static_cast<uint16_t>(e ? aw[q] >> 16 : aw[q] & 0xffffu));
           const float x1 = bf2f(static_cast<uint16_t>(e ? bw[q] >> 16 : bw[q] & 0xffffu));
-          ya[e] = x0 * cs - x1 * sn;
-          yb[e] = x1 * cs + x0 * sn;
+          ya[e] = x0 * cs[2 * q + e] - x1 * sn[2 * q + e];
+          yb[e] = x1 * cs[2 * q + e] + x0 * sn[2 * q + e];
         }
         oa[q] = static_cast<uint32_t>(f2bf(ya[0])) | (static_cast<uint32_t>(f2bf(ya[1])) << 16);
         ob[q] = static_cast<uint32_t>(f2bf(yb[0])) | (static_cast<uint32_t>(f2bf(yb[1])) << 16);
       }
-      *reinterpret_cast<uint4*>(dst[j] + i0) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-      *reinterpret_cast<uint4*>(dst[j] + i0 + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+      *reinterpret_cast<uint4*>(dst + (h0 + hh) * D + i0) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+      *reinterpret_cast<uint4*>(dst + (h0 + hh) * D + i0 + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
     }
   }
 }
 
-// blocks of rope_rows_kernel for rows_cap rows of `heads` heads
+// blocks of rope_rows_kernel for rows_cap rows
 template <int D>
 static int rope_blocks(int64_t rows_cap, int heads) {
-  const int per_row = heads * (D / 16);
-  const int nr = per_row >= 256 ? 1 : 256 / per_row;
-  const int64_t per_block = static_cast<int64_t>(nr) * kRopeRows;
-  return static_cast<int>((rows_cap + per_block - 1) / per_block);
+  (void)heads;
+  constexpr int RPB = 256 / (D / 16);
+  return static_cast<int>(std::max<int64_t>((rows_cap + RPB - 1) / RPB, 1));
 }
 
 // cuTensorMapEncodeTiled, fetched once through the runtime (no link-time
