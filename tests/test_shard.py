@@ -136,3 +136,38 @@ def _free_port():
 def test_two_gloo_ranks_reproduce_the_whole_round():
     mp = pytest.importorskip("torch.multiprocessing")
     mp.spawn(_rank_main, args=(2, _free_port()), nprocs=2, join=True)
+
+
+def test_split_to_fit_partitions_requests_under_the_capacity():
+    """The graph pool's split of a round over its largest bucket: every request exactly
+    once, each group's stream within the capacity, requests longer than the capacity on
+    their own (they run without a graph)."""
+    rnd = small_round()
+    tok = S.request_tokens(rnd)
+    for cap in (20, 32, 40, 64, 200):
+        groups, big = S.split_to_fit(rnd, cap)
+        seen = sorted([j for g in groups for j in g] + list(big))
+        assert seen == list(range(rnd.R)), cap
+        assert all(int(tok[g].sum()) <= cap for g in groups), cap
+        assert sorted(big) == [j for j in range(rnd.R) if tok[j] > cap], cap
+        assert all(len(g) > 0 for g in groups)
+    # a capacity that holds the whole round gives one group
+    groups, big = S.split_to_fit(rnd, int(tok.sum()))
+    assert len(groups) == 1 and big == []
+    # every request above the capacity: nothing to group
+    groups, big = S.split_to_fit(rnd, 1)
+    assert groups == [] and sorted(big) == [j for j in range(rnd.R) if tok[j] > 1]
+
+
+def test_split_to_fit_sub_rounds_keep_every_question():
+    """Sub-rounds of the split hold, together, every question of the round once, with the
+    same question lengths and option counts."""
+    rnd = small_round()
+    groups, big = S.split_to_fit(rnd, 40)
+    qids = []
+    for g in groups + [[j] for j in big]:
+        sub, q = S.shard_round(rnd, g, T_cap=rnd.T_cap)
+        assert sub.R == len(g) and sub.Nq == len(q)
+        assert list(sub.n_opt) == [int(rnd.n_opt[i]) for i in q]
+        qids.extend(q)
+    assert sorted(qids) == list(range(rnd.Nq))
