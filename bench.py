@@ -36,7 +36,7 @@ METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 # SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
 TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
                        "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
-           "sha256": "a7dfff50f92e9ee99e1fa4a38d0aefa3d22d4c46d6150df25e7d914edc5dca05", "bytes": 501893679}
+           "sha256": "c41e5119a48ff34a147fc280c3824567a8fd5ae88b1cc3d469ef7bd1603671e9", "bytes": 501914833}
 
 
 def _sources_sha256(paths):

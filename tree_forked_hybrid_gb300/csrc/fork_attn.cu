@@ -20,7 +20,15 @@ namespace fork {
 
 static int64_t rope_hi_rows(int64_t max_pos) { return (max_pos + 128 + 63) / 64; }
 
-__global__ void rope_tables_kernel(float2* hi, int hi_rows, float2* lo, int half, double theta) {
+// Inverse frequencies f_i = theta^(-2i/d) of the rotary embedding, formed on the host in
+// fp64 (d/2 <= 64 values, passed by value)
+struct RopeFreq {
+  double f[64];
+};
+
+// (cos, sin) tables: hi[a][i] of the angle 64 a f_i, lo[b][i] of b f_i (b < 64); fp64
+// angles and sincos, stored as fp32
+__global__ void rope_tables_kernel(float2* hi, int hi_rows, float2* lo, int half, const RopeFreq freq) {
   const int64_t n_hi = static_cast<int64_t>(hi_rows) * half;
   const int64_t n = n_hi + 64 * half;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
@@ -29,8 +37,7 @@ __global__ void rope_tables_kernel(float2* hi, int hi_rows, float2* lo, int half
     const int64_t e = is_hi ? idx : idx - n_hi;
     const int i = static_cast<int>(e % half);
     const int64_t t = is_hi ? (e / half) * 64 : e / half;
-    const double f = exp2(-2.0 * i / (2.0 * half) * log2(theta));
-    const double ang = static_cast<double>(t) * f;
+    const double ang = static_cast<double>(t) * freq.f[i];
     double sn, cs;
     sincos(ang, &sn, &cs);
     const float2 v = make_float2(static_cast<float>(cs), static_cast<float>(sn));
@@ -310,7 +317,9 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
     float2* hi = reinterpret_cast<float2*>(ws + w.hi);
     float2* lo = reinterpret_cast<float2*>(ws + w.lo);
     const int hi_rows = static_cast<int>(rope_hi_rows(static_cast<int64_t>(L.T_cap) + prefix_rows));
-    rope_tables_kernel<<<2 * sm_count(), 128, 0, s>>>(hi, hi_rows, lo, d / 2, static_cast<double>(rope_theta));
+    RopeFreq freq;
+    for (int i = 0; i < 64; ++i) freq.f[i] = i < d / 2 ? std::pow(static_cast<double>(rope_theta), -2.0 * i / d) : 0.0;
+    rope_tables_kernel<<<2 * sm_count(), 128, 0, s>>>(hi, hi_rows, lo, d / 2, freq);
     // keys of the stream and of the prefix (grids from the capacities: blocks past the
     // round's rows return); the queries here only for the warp-MMA kernel: the tcgen05
     // kernel rotates each query tile in shared memory once it has landed
