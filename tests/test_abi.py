@@ -132,3 +132,7 @@ def test_readout_mlp_argument_errors_and_workspace_size(lib):
     a = list(good)
     a[5] = ctypes.c_void_p(0x1008)  # misaligned weights
     assert lib.fork_readout_mlp(*a) == 1
+    for i in (4, 8):  # gains read as 16-byte vectors
+        a = list(good)
+        a[i] = ctypes.c_void_p(0x1004)
+        assert lib.fork_readout_mlp(*a) == 1
