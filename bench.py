@@ -34,9 +34,11 @@ METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 # attention layer on this workload, summed over the call's launches (rotary tables, key
 # rotation, fp16 value copy, attention), from one ncu capture of this bench's command.  Keyed by the
 # SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
+# The bytes below were taken before the token-forest instance was added to the attention
+# sources; not re-measured since, so traffic reads null.
 TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
                        "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
-           "sha256": "c41e5119a48ff34a147fc280c3824567a8fd5ae88b1cc3d469ef7bd1603671e9", "bytes": 501914833}
+           "sha256": None, "bytes": 501914833}
 
 
 def _sources_sha256(paths):
@@ -310,6 +312,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--no-block", action="store_true",
                     help="skip the hybrid block timing (pointwise block on the question rows vs every row)")
+    ap.add_argument("--no-forest", action="store_true", help="skip the one-round token-forest line")
     ap.add_argument("--no-graph", action="store_true",
                     help="skip the short-request round timed eagerly and as one CUDA graph replay")
     args = ap.parse_args()
@@ -459,6 +462,11 @@ def main():
             out["graph_replay"] = graph_timing(torch, args, local)
         except Exception as exc:  # reported, never fatal for the main line
             out["graph_replay"] = {"error": f"{type(exc).__name__}: {exc}"}
+    if not args.no_forest and ws == 1:
+        try:
+            out["forest"] = forest_timing(torch, args, local)
+        except Exception as exc:  # reported, never fatal for the main line
+            out["forest"] = {"error": f"{type(exc).__name__}: {exc}"}
     if shard is not None:
         out["sharding"] = gather_shards(dist, dr, rnd, shard, rank, ws)
         out["config"]["sharding"] = (f"one round of {shard['shapes'][0].shape[0]} requests "
@@ -572,6 +580,33 @@ def graph_timing(torch, args, local, wid=1):
     return {"workload": f"short requests: R={rnd.R}, T={rnd.T}, Nq={rnd.Nq}", "bucket_T_cap": cr.T_cap,
             "eager_ms": eager, "graph_ms": replay, "launches_per_round": dr.launches_per_round(),
             "same_probabilities": same}
+
+
+def forest_timing(torch, args, local):
+    """Request trees that fork twice, run as one round of one flat stream: 2 requests with
+    the long-document layer shapes, each a 4096-token trunk with 4 branches of 512 tokens
+    and 4 questions of 64 tokens on every branch (42 nodes, 3 depths, 14,336 tokens).
+    Timed with the metadata resident (one attention call per layer, one recurrence call
+    per depth, the readout) and with the host plan and its copy in every round."""
+    from tree_forked_hybrid_gb300 import workloads as wl
+    from tree_forked_hybrid_gb300.runner import ForestRound
+    w = wl.WORKLOADS[WORKLOAD_ID]
+    parent, node_len = wl.request_forest(2, (4096, 512, 64), (4, 4))
+    t = wl.make_tree_round(parent, node_len, attn_shapes=w.attn, gdn_shape=w.gdn, seed=21)
+    fr = ForestRound(t, device=f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        fr.run()
+    steps = max(args.steps, 10)
+    layers = latency_stats(step_times(torch, lambda: fr.run(meta=False), stream, steps))
+    with_plan = latency_stats(step_times(torch, fr.run, stream, steps))
+    if fr.status() != 0:
+        raise RuntimeError(f"device status {fr.status():#x}")
+    T = int(node_len.sum())
+    return {"workload": "2 request trees: trunk 4096, 4 branches x 512, 4 questions x 64 per branch",
+            "nodes": t.N, "levels": fr.plan.levels, "tokens": T, "round_ms": layers,
+            "round_with_plan_ms": with_plan, "tokens_per_s": T / (layers["median"] / 1e3),
+            "gpu_launches_per_round": fr.launches_per_run()}
 
 
 def attn_kernel_alone(torch, dr, rnd, stream, reps=10):

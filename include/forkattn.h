@@ -69,6 +69,10 @@ extern "C" {
 #define FORK_WARP_MMA 0x4u      /* fork_attn, fork_gdn_*: run the warp-level mma.sync kernels instead
                                    of the tcgen05 ones (same results within rounding; for
                                    comparisons; d = 64 GDN always uses them) */
+#define FORK_FOREST 0x8u        /* fork_attn: the metadata describes a token forest (built by
+                                   fork_forest_plan); every node sees its ancestors' rows and
+                                   its own (see "Token forests" below).  d = 128, no prefix
+                                   rows, not with FORK_WARP_MMA. */
 #define FORK_TEST_STALL 0x100u  /* test hook of the bounded waits (fork_attn, fork_gdn_* with
                                    d = 128): one role of every CTA waits on a barrier that
                                    nothing completes, so the wait runs out after
@@ -264,6 +268,76 @@ int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const uint16_t* k, 
                       const float* alpha, const float* eta, const float* conv_w, int32_t H,
                       int32_t d, int32_t K, int32_t chunk, const float* S_P,
                       const uint16_t* conv_win, uint16_t* o, uint32_t flags, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Token forests (rainbus summary "未来方向" (2): a tree of draft tokens has the
+ * shape of the request tree and can run in the same flat stream; DFlash-TfM
+ * summary "GDN을 위한 롤백 없는 트리 검증": the tree in topological order, the
+ * recurrence in its chunked form).  A forest of N nodes, node k with parent
+ * parent[k] (-1 for a root; parents precede their children) and node_len[k]
+ * tokens of its own, stored node after node in one unpadded stream (node k's
+ * rows start at the sum of the earlier nodes' lengths).  Node k's sequence is
+ * its ancestors' tokens, root first, followed by its own: its first token has
+ * position pos0_k = the sum of its ancestors' lengths.  Every result equals
+ * that of the node's sequence run alone.
+ *   - Attention (fork_attn with FORK_FOREST): key y is visible to query x iff
+ *     y's node is x's node or one of its ancestors, t_y <= t_x and, for a
+ *     sliding window, t_x - t_y < W.  The keys of every ancestor are read in
+ *     place: no row is copied.
+ *   - Gated DeltaNet (fork_gdn_forest, one call per depth): a node starts from
+ *     its parent's end state and conv window, read by the parent's state index,
+ *     and writes its own at its index.
+ *   - Readout (fork_readout): the leaves are the questions, in node order.
+ * ------------------------------------------------------------------------ */
+
+#define FORK_FOREST_MAX_DEPTH 7 /* ancestors of a node, at most (8 levels) */
+#define FORK_FOREST_MAX_LEVELS (FORK_FOREST_MAX_DEPTH + 1)
+/* int32 words of the plan written by fork_forest_plan for N nodes */
+#define FORK_FOREST_PLAN_WORDS(N) ((size_t)(N) + 2 + FORK_FOREST_MAX_LEVELS)
+
+/* Plan a forest on the host (no CUDA call): fill h_image (fork_meta_bytes
+ * bytes for m's capacities, host memory) with the metadata that fork_attn,
+ * fork_gdn_forest and fork_readout read, and h_plan
+ * [FORK_FOREST_PLAN_WORDS(N)] with:
+ *   h_plan[0]           number of levels L (1 + the greatest depth);
+ *   h_plan[1 + l]       first state index of level l, l = 0..L (h_plan[1 + L] = N);
+ *   h_plan[2 + FORK_FOREST_MAX_LEVELS + k]  state index of node k.
+ * State indices order the nodes by depth, then by node number; node k's end
+ * state and conv window live at its state index in the caller's arrays.
+ * The metadata holds one segment per node (in state-index order) with its
+ * stream rows, pos0_k and the state index of its parent (-1 for a root), the
+ * per-token positions (pad rows -1), the last row of every leaf (leaves in
+ * node order) and the attention work list, tile_tokens-token tiles aligned to
+ * each node's first row, launched in non-increasing order of visible keys.
+ * m->d_buf is not touched (copy h_image there, or use fork_build_forest_meta).
+ * Errors: FORK_EINVAL (null pointer, invalid handle, N < 1, a parent not
+ * before its child, a negative length, a leaf without tokens), FORK_ECAPACITY
+ * (N > max_req, more leaves than max_q, more than T_cap tokens, a node deeper
+ * than FORK_FOREST_MAX_DEPTH). */
+int fork_forest_plan(const fork_meta* m, const int32_t* parent, const int32_t* node_len, int32_t N,
+                     int32_t* h_image, int32_t* h_plan);
+
+/* fork_forest_plan, then an asynchronous copy of h_image to m->d_buf on
+ * `stream` (h_image is read before the call returns when it is pageable host
+ * memory; keep pinned memory unchanged until the copy has completed). */
+int fork_build_forest_meta(const fork_meta* m, const int32_t* parent, const int32_t* node_len,
+                           int32_t N, int32_t* h_image, int32_t* h_plan, void* stream);
+
+/* Gated DeltaNet of the nodes with state indices [first, first + count) of a
+ * forest (one level: their parents' states must be complete, i.e. the previous
+ * level's call came earlier on the stream).  Shared arguments as for
+ * fork_gdn_trunk, d = 128.  node_state [N, H, d, d] float32 and node_conv
+ * [N, K-1, 3, H, d] bf16, indexed by state index: a node with pos0 > 0 starts
+ * from its parent's entries, a node with pos0 = 0 from zero; every node writes
+ * its end state and the raw conv inputs of its sequence's last K-1 positions
+ * (zero before position 0) at its own index.  o: the nodes' rows.
+ * Errors: FORK_EINVAL (null pointers, first < 0, count < 0, first + count >
+ * max_req, d != 128, FORK_WARP_MMA). */
+int fork_gdn_forest(const fork_meta* m, int32_t first, int32_t count, const uint16_t* q,
+                    const uint16_t* k, const uint16_t* v, const float* alpha, const float* eta,
+                    const float* conv_w, int32_t H, int32_t d, int32_t K, int32_t chunk,
+                    float* node_state, uint16_t* node_conv, uint16_t* o, uint32_t flags,
+                    void* stream);
 
 /* ------------------------------------------------------------------------
  * Selective readout, eq. (1) (onedev "어떻게 동작하나"; rainbus "前置知识"):

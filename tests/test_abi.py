@@ -30,7 +30,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("fork_build_meta", "fork_attn", "fork_gdn_trunk", "fork_gdn_branches", "fork_readout",
-                 "fork_meta_bytes", "fork_meta_init", "fork_read_status", "fork_attn_workspace_bytes"):
+                 "fork_meta_bytes", "fork_meta_init", "fork_read_status", "fork_attn_workspace_bytes",
+                 "fork_forest_plan", "fork_build_forest_meta", "fork_gdn_forest"):
         assert want in names
 
 
@@ -96,6 +97,23 @@ def test_argument_errors_return_before_any_launch(lib):
                                  None) == 1
     assert lib.fork_readout(ref, fake, 100, fake, fake, fake, 0, None) == 1
     assert lib.fork_readout(ref, None, 128, fake, fake, fake, 0, None) == 1
+    # token forests: attention only at d = 128, without prefix rows, not on the warp-MMA kernel
+    forest = F.FORK_FOREST
+    assert lib.fork_attn(ref, fake, fake, fake, fake, 4, 1, 64, 0, 0.0, 0.1, None, None, 0, None, 0, forest,
+                         None) == 1
+    assert lib.fork_attn(ref, fake, fake, fake, fake, 4, 1, 128, 0, 0.0, 0.1, fake, fake, 8, None, 0, forest,
+                         None) == 1
+    assert lib.fork_attn(ref, fake, fake, fake, fake, 4, 1, 128, 0, 0.0, 0.1, None, None, 0, None, 0,
+                         forest | F.FORK_WARP_MMA, None) == 1
+    # forest levels: d = 128, a node range inside the capacity, both state arrays
+    gf = lambda first, count, d, st, flags=0: lib.fork_gdn_forest(  # noqa: E731
+        ref, first, count, fake, fake, fake, fake, fake, fake, 2, d, 4, 64, st, fake, fake, flags, None)
+    assert gf(0, 2, 64, fake) == 1
+    assert gf(0, 2, 128, None) == 1
+    assert gf(-1, 2, 128, fake) == 1
+    assert gf(0, -1, 128, fake) == 1
+    assert gf(3, 2, 128, fake) == 1       # past max_req = 4
+    assert gf(0, 2, 128, fake, F.FORK_WARP_MMA) == 1
 
 
 def test_readout_mlp_argument_errors_and_workspace_size(lib):

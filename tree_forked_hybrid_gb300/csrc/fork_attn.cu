@@ -279,6 +279,9 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
   if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return FORK_EINVAL;
   if (prefix_rows > 0 && (!prefix_k || !prefix_v || !is_aligned16(prefix_k) || !is_aligned16(prefix_v)))
     return FORK_EINVAL;
+  // token forests: the tcgen05 kernel's forest instance (d = 128), every key in the stream
+  const bool forest = (flags & FORK_FOREST) != 0;
+  if (forest && (d != 128 || warp_mma || prefix_rows != 0 || prefix_k || prefix_v)) return FORK_EINVAL;
   if ((rc = check_device()) != FORK_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -375,7 +378,8 @@ extern "C" int fork_attn(const fork_meta* m, const uint16_t* q, const uint16_t* 
       !make_map(&maps[1], p.k, d, Hkv, L.T_cap, 1, 128) || !make_map(&maps[2], vtc, d, Hkv, L.T_cap, 1, 128) ||
       !make_map(&maps[3], pk, d, Hkv, prow, 1, 128) || !make_map(&maps[4], pv, d, Hkv, prow, 1, 128))
     return FORK_ECUDA;
-  return d == 64 ? launch_attn_tc<64>(p, maps, grid_x, two, s) : launch_attn_tc<128>(p, maps, grid_x, two, s);
+  return d == 64 ? launch_attn_tc<64>(p, maps, grid_x, two, forest, s)
+                 : launch_attn_tc<128>(p, maps, grid_x, two, forest, s);
 }
 
 // ---- fork_attn_noalloc: fork_attn with the library's own scratch area -------------

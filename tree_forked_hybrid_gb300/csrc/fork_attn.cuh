@@ -71,8 +71,10 @@ bool encode_map_3d(CUtensorMap* m, const void* base, int d, int heads, int64_t r
 template <int D>
 int launch_attn_mma(const AttnParams& p, int grid_x, cudaStream_t s);
 
-// maps: q, k, v, prefix k, prefix v (CUtensorMap, 128-byte aligned)
+// maps: q, k, v, prefix k, prefix v (CUtensorMap, 128-byte aligned); forest: the metadata
+// describes a token forest (D = 128)
 template <int D>
-int launch_attn_tc(const AttnParams& p, const CUtensorMap* maps, int grid_x, bool two_tiles, cudaStream_t s);
+int launch_attn_tc(const AttnParams& p, const CUtensorMap* maps, int grid_x, bool two_tiles, bool forest,
+                   cudaStream_t s);
 
 }  // namespace fork

@@ -11,6 +11,11 @@
 // to the range start and query tiles to the segment start: every output
 // element is produced by the same sequence of operations whatever else the
 // round holds.
+// Token forests (rainbus "未来方向" (2): a draft-token tree runs in the same flat
+// stream as the request tree): the segments are the nodes, and a node's queries
+// read the rows of each of its ancestors (root first) and then its own, all in
+// place in the stream; positions continue along the path, so the same per-range
+// rule applies (kernel instance with kForestRanges range slots).
 //
 // A work item x one kv head = up to two 128-row query tiles (rows = token x
 // grouped head) that share every K/V tile.  The kernel is persistent: one CTA
@@ -75,6 +80,8 @@ enum Bar { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KEMPTY0, B_KEMPTY1, B_
            B_SFULL1, B_PFULL0, B_PFULL1, B_OFULL0, B_OFULL1, B_OFREE0, B_OFREE1, B_FIN, B_QROT, B_STALL,
            B_ITEMF0, B_ITEMF1, B_ITEMF2, B_ITEMF3, B_ITEME0, B_ITEME1, B_ITEME2, B_ITEME3, B_COUNT };
 constexpr int kItemRing = 4;  // claimed work items handed from the producer to the other roles
+constexpr int kRoundRanges = 3;                           // prefix, trunk, own branch
+constexpr int kForestRanges = FORK_FOREST_MAX_DEPTH + 1;  // ancestors root first, then the node
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -168,17 +175,41 @@ __device__ __forceinline__ void rotate_q_row(unsigned char* tile, int row, int t
 }
 
 // One work item of a call: kv head g x entry r of the longest-first order (q = g n_work + r).  Its query
-// tokens, and its key ranges in fixed slots: 0 prefix rows kept outside the stream, 1
-// trunk, 2 own branch (an absent range has length 0).  Every role of a CTA computes it
-// from the tables by itself.
+// tokens, and its key ranges in fixed slots (an absent range has length 0): for a round
+// (NR = kRoundRanges) 0 prefix rows kept outside the stream, 1 trunk, 2 own branch; for a
+// forest (NR = kForestRanges) the node's ancestors, root first, then the node itself.  The
+// producer computes it from the tables and hands it to the other roles.
+template <int NR>
 struct AttnItem {
   int ok, status;  // status: the bit to raise when the item is skipped (ok == 0)
   int g, seg_start, off, n_all, ntiles, tx_min, total;
-  int row0[3], len[3], pos0[3], lo[3], cnt[3];
+  int row0[NR], len[NR], pos0[NR], lo[NR], cnt[NR];
 };
 
-__device__ __forceinline__ AttnItem attn_item(const int32_t* meta, const MetaLayout& L, const TcParams& p, int q) {
-  AttnItem it;
+// first key tile and tile count of every range slot: the keys of the range at positions
+// in [tx_min - W + 1, tx_max] (no lower bound without a window), in tiles aligned to the
+// range start
+template <int NR>
+__device__ __forceinline__ void item_key_tiles(AttnItem<NR>& it, int tx_max, int window) {
+#pragma unroll
+  for (int k = 0; k < NR; ++k) {
+    it.lo[k] = 0;
+    it.cnt[k] = 0;
+    if (it.len[k] > 0) {
+      const int umax = min(it.len[k] - 1, tx_max - it.pos0[k]);
+      const int umin = window > 0 ? max(0, it.tx_min - window + 1 - it.pos0[k]) : 0;
+      if (umax >= umin) {
+        it.lo[k] = umin / kKeys;
+        it.cnt[k] = umax / kKeys - it.lo[k] + 1;
+      }
+    }
+    it.total += it.cnt[k];
+  }
+}
+
+__device__ __forceinline__ AttnItem<kRoundRanges> attn_item(const int32_t* meta, const MetaLayout& L,
+                                                            const TcParams& p, int q) {
+  AttnItem<kRoundRanges> it;
   // head-major: the CTAs running at one time mostly share a kv head, so the K/V tiles
   // they re-read stay in L2
   const int nw = meta[H_NWORK];
@@ -219,21 +250,67 @@ __device__ __forceinline__ AttnItem attn_item(const int32_t* meta, const MetaLay
   it.row0[2] = it.seg_start;
   it.len[2] = c > 0 ? seg_len : 0;
   it.pos0[2] = seg_pos0;
-#pragma unroll
-  for (int k = 0; k < 3; ++k) {
-    it.lo[k] = 0;
-    it.cnt[k] = 0;
-    if (it.len[k] > 0) {
-      const int umax = min(it.len[k] - 1, tx_max - it.pos0[k]);
-      const int umin = p.window > 0 ? max(0, it.tx_min - p.window + 1 - it.pos0[k]) : 0;
-      if (umax >= umin) {
-        it.lo[k] = umin / kKeys;
-        it.cnt[k] = umax / kKeys - it.lo[k] + 1;
-      }
-    }
-    it.total += it.cnt[k];
-  }
+  item_key_tiles(it, tx_max, p.window);
   it.ok = it.total > 0;  // always, for a valid item (a token sees itself)
+  return it;
+}
+
+// A work item of a forest: segment s is a node, seg_state_idx its parent's segment (-1 for a
+// root).  The parent chain is walked twice (depth first, then the slots from the parent up
+// to the root); a chain longer than kForestRanges - 1 or leaving the table skips the item.
+__device__ __forceinline__ AttnItem<kForestRanges> attn_item_forest(const int32_t* meta, const MetaLayout& L,
+                                                                    const TcParams& p, int q) {
+  AttnItem<kForestRanges> it;
+  const int nw = meta[H_NWORK];
+  it.g = q / nw;
+  const int r = q - it.g * nw;
+  it.ok = 0;
+  it.status = 0;
+  it.total = 0;
+  const int w = meta[L.work_order + r];
+  if (p.checks && !attn_item_in_bounds(meta, L, w)) {
+    it.status = FORK_STATUS_CHECK;
+    return it;
+  }
+  const int s = meta[L.work_seg + w];
+  it.off = meta[L.work_off + w];
+  it.seg_start = meta[L.seg_start + s];
+  const int seg_len = meta[L.seg_len + s];
+  const int seg_pos0 = meta[L.seg_pos0 + s];
+  const int tile = kRows / p.G;
+  it.n_all = min(p.two_tiles ? 2 * tile : tile, seg_len - it.off);
+  it.ntiles = it.n_all > tile ? 2 : 1;
+  it.tx_min = seg_pos0 + it.off;
+  const int tx_max = it.tx_min + it.n_all - 1;
+  const int nseg = meta[H_NSEG], T = meta[H_T];
+  int na = 0;
+  for (int a = meta[L.seg_state_idx + s]; a >= 0; a = meta[L.seg_state_idx + a]) {
+    if (na == kForestRanges - 1 || a >= nseg) {
+      it.status = FORK_STATUS_BAD_DESC;
+      return it;
+    }
+    ++na;
+  }
+#pragma unroll
+  for (int k = 0; k < kForestRanges; ++k) {
+    it.row0[k] = 0;
+    it.len[k] = 0;
+    it.pos0[k] = 0;
+  }
+  for (int k = na - 1, a = meta[L.seg_state_idx + s]; k >= 0; --k, a = meta[L.seg_state_idx + a]) {
+    it.row0[k] = meta[L.seg_start + a];
+    it.len[k] = meta[L.seg_len + a];
+    it.pos0[k] = meta[L.seg_pos0 + a];
+    if (p.checks && (it.row0[k] < 0 || it.len[k] < 0 || it.row0[k] + it.len[k] > T)) {
+      it.status = FORK_STATUS_CHECK;
+      return it;
+    }
+  }
+  it.row0[na] = it.seg_start;
+  it.len[na] = seg_len;
+  it.pos0[na] = seg_pos0;
+  item_key_tiles(it, tx_max, p.window);
+  it.ok = it.total > 0;
   return it;
 }
 
@@ -243,7 +320,7 @@ __device__ __forceinline__ AttnItem attn_item(const int32_t* meta, const MetaLay
 // loads run on into the next item as slots free up, and the next item's query tiles land
 // while the current item's last products and output rows finish.  Barrier phases follow
 // running counts (key tiles F, items, per-tile S and O), identical in every role.
-template <int D>
+template <int D, int NR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap pkmap,
@@ -257,6 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* meta = p.meta;
   const MetaLayout& L = p.L;
   if (meta[H_VALID] == 0) return;
+  if (NR == kForestRanges && meta[H_FOREST] != 1) {  // round tables given to the forest instance
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_DESC);
+    return;
+  }
   const int n_items = meta[H_NWORK] * p.Hkv;
   if (static_cast<int>(blockIdx.x) >= n_items) return;
   const int G = p.G;
@@ -269,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // first position per slot), read in the key-tile loop instead of holding registers
   int* rtab_all = reinterpret_cast<int*>(smem + LY::BAR + B_COUNT * 8 + 16);
   // claimed work items (AttnItem, ok == 0 marks the end), written by the producer
-  AttnItem* ring = reinterpret_cast<AttnItem*>(smem + LY::BAR + B_COUNT * 8 + 16 + 8 * 12 * 4);
-  static_assert(B_COUNT * 8 + 16 + 8 * 12 * 4 + kItemRing * sizeof(AttnItem) <= 2048, "barrier region");
+  AttnItem<NR>* ring = reinterpret_cast<AttnItem<NR>*>(smem + LY::BAR + B_COUNT * 8 + 16 + 8 * (4 * NR) * 4);
+  static_assert(B_COUNT * 8 + 16 + 8 * (4 * NR) * 4 + kItemRing * sizeof(AttnItem<NR>) <= 2048, "barrier region");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -312,12 +393,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   struct KT {
     int r, row0, len, pos0, t;
   };
-  auto key_tile = [&](const AttnItem& it, int f) -> KT {
-    if (f < it.cnt[0]) return {0, it.row0[0], it.len[0], it.pos0[0], it.lo[0] + f};
-    f -= it.cnt[0];
-    if (f < it.cnt[1]) return {1, it.row0[1], it.len[1], it.pos0[1], it.lo[1] + f};
-    f -= it.cnt[1];
-    return {2, it.row0[2], it.len[2], it.pos0[2], it.lo[2] + f};
+  auto key_tile = [&](const AttnItem<NR>& it, int f) -> KT {
+    if constexpr (NR == kRoundRanges) {
+      if (f < it.cnt[0]) return {0, it.row0[0], it.len[0], it.pos0[0], it.lo[0] + f};
+      f -= it.cnt[0];
+      if (f < it.cnt[1]) return {1, it.row0[1], it.len[1], it.pos0[1], it.lo[1] + f};
+      f -= it.cnt[1];
+      return {2, it.row0[2], it.len[2], it.pos0[2], it.lo[2] + f};
+    } else {
+      int r = 0;
+      while (r < NR - 1 && f >= it.cnt[r]) {
+        f -= it.cnt[r];
+        ++r;
+      }
+      return {r, it.row0[r], it.len[r], it.pos0[r], it.lo[r] + f};
+    }
   };
 
   if (warp == 1) {
@@ -334,9 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int F = 0, issued = 0, nq = 0, n = 0;
       for (int q = blockIdx.x;; q = static_cast<int>(gridDim.x) + atomicAdd(p.work_ctr, 1)) {
-        AttnItem it;
+        AttnItem<NR> it;
         if (q < n_items) {
-          it = attn_item(meta, L, p, q);
+          if constexpr (NR == kRoundRanges) it = attn_item(meta, L, p, q);
+          else it = attn_item_forest(meta, L, p, q);
           if (!it.ok) {  // skipped by every role: never handed on
             if (it.status) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, it.status);
             continue;
@@ -366,8 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int f = 0; f < it.total; ++f, ++F) {
           const int st = F & 1;
           const KT kt = key_tile(it, f);
-          const CUtensorMap* km = kt.r == 0 ? &pkmap : &kmap;
-          const CUtensorMap* vm = kt.r == 0 ? &pvmap : &vmap;
+          const bool pre = NR == kRoundRanges && kt.r == 0;  // a round's prefix rows
+          const CUtensorMap* km = pre ? &pkmap : &kmap;
+          const CUtensorMap* vm = pre ? &pvmap : &vmap;
           const int row = kt.row0 + kt.t * kKeys;
           if (F >= 2 && !(ok = wait(B_KEMPTY0 + st, ((F >> 1) - 1) & 1))) break;
           tc::mbar_expect_tx_only(&bars[B_KVFULL0 + st], NB * kBox);
@@ -437,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; ok; ++n) {
         const int slot = n & (kItemRing - 1);
         if (!(ok = wait(B_ITEMF0 + slot, (n / kItemRing) & 1))) break;
-        const AttnItem it = ring[slot];
+        const AttnItem<NR> it = ring[slot];
         tc::mbar_arrive(&bars[B_ITEME0 + slot]);
         if (!it.ok) break;
         const int ntiles = it.ntiles, total = it.total;
@@ -484,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ===================== softmax warpgroups (tile t = (warp - 2) / 4, row = tid % 128) ====
     const int t = (warp - 2) >> 2;
-    int* rtab = rtab_all + (warp - 2) * 12;
+    int* rtab = rtab_all + (warp - 2) * (4 * NR);
     const int row = tid & 127;
     const int tok = row / G, hl = row % G;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -492,11 +584,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     int n = 0, nq = 0, nS = 0, nO = 0;
     // the next item from the ring (ok == 0: the end); false on a failed wait
-    auto fetch = [&](AttnItem& it) -> bool {
+    // (forest: the item's range table goes straight to this warp's table here; the
+    // previous item's key loop, its only reader, is over)
+    auto fetch = [&](AttnItem<NR>& it) -> bool {
       const int slot = n & (kItemRing - 1);
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&bars[B_ITEMF0 + slot], (n / kItemRing) & 1, abort, p.wait_ns)))
         return false;
-      it = ring[slot];
+      if constexpr (NR == kRoundRanges) {
+        it = ring[slot];
+      } else {
+        const AttnItem<NR>& rs = ring[slot];
+        it.ok = rs.ok;
+        it.g = rs.g;
+        it.seg_start = rs.seg_start;
+        it.off = rs.off;
+        it.n_all = rs.n_all;
+        it.ntiles = rs.ntiles;
+        it.tx_min = rs.tx_min;
+        it.total = rs.total;
+        __syncwarp();  // every lane has finished reading the previous item's table
+        if (lane < NR) {
+          rtab[4 * lane] = rs.lo[lane];
+          rtab[4 * lane + 1] = rs.cnt[lane];
+          rtab[4 * lane + 2] = rs.len[lane];
+          rtab[4 * lane + 3] = rs.pos0[lane];
+        }
+      }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bars[B_ITEME0 + slot]);
       ++n;
@@ -505,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rotary embedding of an item's query tiles in shared memory, thread = row, once they
     // have landed; the products read them after every thread's fence and arrival.  The
     // row's two table rows (512 bytes each) are prefetched into L1 while the tiles load.
-    auto rotate = [&](const AttnItem& it) -> bool {
+    auto rotate = [&](const AttnItem<NR>& it) -> bool {
       if (t < it.ntiles) {
         const int tpos = it.tx_min + t * tile + min(tok, tile - 1);
         if (tpos >> 6 < p.rope_hi_rows) {
@@ -528,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive(&bars[B_QROT]);
       return okq;
     };
-    AttnItem cur;
+    AttnItem<NR> cur;
     bool ok = fetch(cur);
     if (ok && cur.ok && p.rotate_q) ok = rotate(cur);
     while (ok && cur.ok) {
@@ -536,17 +649,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_t = mine ? min(tile, cur.n_all - t * tile) : 0;  // valid tokens of this tile
       float l = 0.f;
       if (mine) {
-        __syncwarp();  // every lane has finished reading the previous item's table
-        if (lane == 0) {
+        if constexpr (NR == kRoundRanges) {
+          __syncwarp();  // every lane has finished reading the previous item's table
+          if (lane == 0) {
 #pragma unroll
-          for (int k = 0; k < 3; ++k) {
-            rtab[4 * k] = cur.lo[k];
-            rtab[4 * k + 1] = cur.cnt[k];
-            rtab[4 * k + 2] = cur.len[k];
-            rtab[4 * k + 3] = cur.pos0[k];
+            for (int k = 0; k < 3; ++k) {
+              rtab[4 * k] = cur.lo[k];
+              rtab[4 * k + 1] = cur.cnt[k];
+              rtab[4 * k + 2] = cur.len[k];
+              rtab[4 * k + 3] = cur.pos0[k];
+            }
           }
+          __syncwarp();
         }
-        __syncwarp();
         const int total = cur.total;
         const int txm = cur.tx_min + t * tile;  // first position of this tile
         const int txM = txm + n_t - 1;           // last valid position of this tile
@@ -567,10 +682,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < kKeys; ++cc) sv[cc] = __uint_as_float(rawv[cc]);
           }
           int len, p0, u0;
-          {
+          if constexpr (NR == kRoundRanges) {
             const int c0 = rtab[1], c1 = rtab[5];
             const int r = f < c0 ? 0 : (f < c0 + c1 ? 1 : 2);
             const int fr = f - (r == 0 ? 0 : (r == 1 ? c0 : c0 + c1));
+            u0 = (rtab[4 * r] + fr) * kKeys;
+            len = rtab[4 * r + 2];
+            p0 = rtab[4 * r + 3];
+          } else {
+            int r = 0, fr = f;
+            while (r < NR - 1 && fr >= rtab[4 * r + 1]) {
+              fr -= rtab[4 * r + 1];
+              ++r;
+            }
             u0 = (rtab[4 * r] + fr) * kKeys;
             len = rtab[4 * r + 2];
             p0 = rtab[4 * r + 3];
@@ -649,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // the next item's query tiles are rotated before this item's output rows are
       // written, so that its first products overlap them
-      AttnItem nxt;
+      AttnItem<NR> nxt;
       if (!(ok = fetch(nxt))) break;
       if (nxt.ok && p.rotate_q && !(ok = rotate(nxt))) break;
       if (mine) {
@@ -697,9 +821,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---- host side -------------------------------------------------------------------
 
 template <int D>
-int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, bool two_tiles, cudaStream_t s) {
+int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, bool two_tiles, bool forest,
+                   cudaStream_t s) {
   using LY = TcLayout<D>;
-  if (cuda_rc(cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM)) != FORK_OK)
+  // token forests: d = 128 only (the one instance built)
+  auto kern = attn_tc_kernel<D, kRoundRanges>;
+  if (forest) {
+    if constexpr (D == 128) kern = attn_tc_kernel<D, kForestRanges>;
+    else return FORK_EINVAL;
+  }
+  if (cuda_rc(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM)) != FORK_OK)
     return FORK_ECUDA;
   TcParams p;
   p.meta = a.meta;
@@ -722,11 +853,11 @@ int launch_attn_tc(const AttnParams& a, const CUtensorMap* maps, int grid_x, boo
   p.work_ctr = a.work_ctr;
   // one CTA per SM over all (work item, kv head) pairs (fewer when there are fewer pairs)
   const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(grid_x) * a.Hkv, sm_count()));
-  attn_tc_kernel<D><<<grid, kThreads, LY::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  kern<<<grid, kThreads, LY::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cuda_rc(cudaGetLastError());
 }
 
-template int launch_attn_tc<64>(const AttnParams&, const CUtensorMap*, int, bool, cudaStream_t);
-template int launch_attn_tc<128>(const AttnParams&, const CUtensorMap*, int, bool, cudaStream_t);
+template int launch_attn_tc<64>(const AttnParams&, const CUtensorMap*, int, bool, bool, cudaStream_t);
+template int launch_attn_tc<128>(const AttnParams&, const CUtensorMap*, int, bool, bool, cudaStream_t);
 
 }  // namespace fork

@@ -16,6 +16,7 @@ constexpr int kMinTile = 8;             // smallest attention tile (Hq/Hkv = 16)
 enum Hdr : int {
   H_MAGIC = 0, H_TCAP, H_MAXREQ, H_MAXQ, H_MAXSEG, H_MAXWORK,
   H_R, H_NQ, H_T, H_NSEG, H_TILE, H_NWORK, H_STATUS, H_PREFIX_TOTAL, H_VALID,
+  H_FOREST,  // 1: the tables describe a token forest (fork_forest_plan), 0: a round
   H_WORDS = 32
 };
 

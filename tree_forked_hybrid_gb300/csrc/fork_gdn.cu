@@ -558,12 +558,56 @@ extern "C" int fork_gdn_trunk(const fork_meta* m, const uint16_t* q, const uint1
   p.S_ckpt = S_ckpt;
   p.conv_ckpt = conv_ckpt;
   p.o = o;
+  p.seg_base = 0;
+  p.n_segs = -1;
   p.checks = (flags & FORK_CHECKS) ? 1 : 0;
   p.stall = (flags & FORK_TEST_STALL) ? 1 : 0;
   p.wait_ns = wait_ns_of(m);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 128 && !(flags & FORK_WARP_MMA)) return launch_gdn_tc(p, false, m->max_req, s);
   return d == 64 ? launch_gdn<64, false>(p, m->max_req, s) : launch_gdn<128, false>(p, m->max_req, s);
+}
+
+// One level of a token forest: the nodes with state indices [first, first + count), each a
+// trunk whose start state and conv window are its parent's (node_state / node_conv at the
+// segment's state index), writing its own at its index.
+extern "C" int fork_gdn_forest(const fork_meta* m, int32_t first, int32_t count, const uint16_t* q,
+                               const uint16_t* k, const uint16_t* v, const float* alpha, const float* eta,
+                               const float* conv_w, int32_t H, int32_t d, int32_t K, int32_t chunk,
+                               float* node_state, uint16_t* node_conv, uint16_t* o, uint32_t flags,
+                               void* stream) {
+  MetaLayout L;
+  int rc = gdn_common_checks(m, &L, q, k, v, alpha, eta, conv_w, H, d, K, chunk, o);
+  if (rc != FORK_OK) return rc;
+  if (!node_state || !node_conv || !is_aligned16(node_state) || !is_aligned16(node_conv)) return FORK_EINVAL;
+  if (d != 128 || (flags & FORK_WARP_MMA)) return FORK_EINVAL;
+  if (first < 0 || count < 0 || static_cast<int64_t>(first) + count > m->max_req) return FORK_EINVAL;
+  if ((rc = check_device()) != FORK_OK) return rc;
+  if (count == 0) return FORK_OK;
+  GdnParams p;
+  p.meta = static_cast<const int32_t*>(m->d_buf);
+  p.L = L;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.alpha = alpha;
+  p.eta = eta;
+  p.conv_w = conv_w;
+  p.H = H;
+  p.K = K;
+  p.state_in = node_state;
+  p.hist_in = node_conv;
+  p.S_P = node_state;
+  p.conv_win = node_conv;
+  p.S_ckpt = nullptr;
+  p.conv_ckpt = nullptr;
+  p.o = o;
+  p.seg_base = first;
+  p.n_segs = count;
+  p.checks = (flags & FORK_CHECKS) ? 1 : 0;
+  p.stall = (flags & FORK_TEST_STALL) ? 1 : 0;
+  p.wait_ns = wait_ns_of(m);
+  return launch_gdn_tc(p, false, count, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const uint16_t* k,
@@ -595,6 +639,8 @@ extern "C" int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const ui
   p.S_ckpt = nullptr;
   p.conv_ckpt = nullptr;
   p.o = o;
+  p.seg_base = 0;
+  p.n_segs = -1;
   p.checks = (flags & FORK_CHECKS) ? 1 : 0;
   p.stall = (flags & FORK_TEST_STALL) ? 1 : 0;
   p.wait_ns = wait_ns_of(m);

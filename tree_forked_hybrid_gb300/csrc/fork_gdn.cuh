@@ -15,13 +15,15 @@ struct GdnParams {
   const float* eta;
   const float* conv_w;      // [3, H, D, K]
   int H, K;
-  const float* state_in;    // trunk: init_state (resume) or null; branch: S_P
+  const float* state_in;    // trunk: init_state (resume) or null; branch: S_P; forest: node states
   const uint16_t* hist_in;  // trunk: init_conv or null; branch: conv_win
   float* S_P;               // trunk output
   uint16_t* conv_win;       // trunk output
   float* S_ckpt;
   uint16_t* conv_ckpt;
   uint16_t* o;
+  int seg_base;             // trunk call: first segment of the call (a forest level; 0 for a round)
+  int n_segs;               // trunk call: its segments (-1: every trunk of the round)
   int checks;               // FORK_CHECKS
   int stall;                // FORK_TEST_STALL (tcgen05 kernel)
   uint64_t wait_ns;         // limit of a bounded wait (tcgen05 kernel)

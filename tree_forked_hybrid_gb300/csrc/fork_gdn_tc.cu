@@ -16,7 +16,8 @@
 // Y itself.
 //
 // One CTA = one trunk (call 1) or a group of up to kQG questions of one request
-// (call 2) x one head; d = 128.  16 warps in three roles that work on consecutive chunks
+// (call 2) x one head; d = 128.  A node of a token forest runs as a trunk that starts
+// from its parent's end state (the state index of the trunk's segment).  16 warps in three roles that work on consecutive chunks
 // (two slots of row tiles, so the roles overlap):
 //   warps 0-3   conv of chunk k+1 for q and k: raw rows by TMA (the chunk and the three
 //               rows before it, 128-byte swizzled; the next chunk's rows are requested as
@@ -180,10 +181,12 @@ __global__ void __launch_bounds__(NT, 1)
     seg_first = R + x;
     seg_end = R + min(x + kQG, fq + nq);
   } else {
-    if (x >= R) return;
-    j = x;
-    seg_first = x;
-    seg_end = x + 1;
+    // a round's trunks, or the segments [seg_base, seg_base + n_segs) of a forest level
+    if (x >= (p.n_segs >= 0 ? p.n_segs : R)) return;
+    j = p.seg_base + x;
+    if (j >= R) return;
+    seg_first = j;
+    seg_end = j + 1;
   }
   if (p.checks && !gdn_segs_in_bounds(meta, L, seg_first, seg_end, j)) {
     if (threadIdx.x == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_CHECK);
@@ -199,9 +202,17 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
     return;
   }
+  // index of the start state and conv window: the request's own (a question reads S_P[j], a
+  // resumed trunk its init_state[j]), or a forest node's parent's (its segment's state index)
+  const int in_idx = BRANCH ? j : meta[L.seg_state_idx + j];
+  if (resumed && (in_idx < 0 || in_idx >= R)) {
+    if (tid == 0) atomicOr(const_cast<int32_t*>(meta) + H_STATUS, FORK_STATUS_BAD_PREFIX);
+    return;
+  }
   const uint16_t* hist = (BRANCH || resumed) ? p.hist_in : nullptr;
   const float* S0 = (BRANCH || resumed) ? p.state_in : nullptr;
-  const int64_t state_base = (static_cast<int64_t>(j) * H + h) * D * D;
+  const int64_t state_base = (static_cast<int64_t>(j) * H + h) * D * D;  // outputs
+  const int64_t in_base = (static_cast<int64_t>(in_idx) * H + h) * D * D;
 
   unsigned char* raw = sm + Lay::RAW;
   unsigned char* yv = sm + Lay::YV;
@@ -237,7 +248,7 @@ __global__ void __launch_bounds__(NT, 1)
   }
   // a checkpoint at the first position of a trunk is its start state
   if (!BRANCH && ck >= 0 && p.S_ckpt && ck == meta[L.seg_pos0 + j]) {
-    for (int e = tid; e < D * D; e += NT) p.S_ckpt[state_base + e] = S0 ? S0[state_base + e] : 0.f;
+    for (int e = tid; e < D * D; e += NT) p.S_ckpt[state_base + e] = S0 ? S0[in_base + e] : 0.f;
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__(NT, 1)
     for (int e = r; e < (s_hi - s_lo) * (KW - 1) * D; e += 128) {
       const int s3 = s_lo + e / ((KW - 1) * D), i = (e / D) % (KW - 1), c = e % D;
       const uint16_t hv =
-          hist ? hist[((static_cast<int64_t>(j * (KW - 1) + i) * 3 + s3) * H + h) * D + c] : uint16_t(0);
+          hist ? hist[((static_cast<int64_t>(in_idx * (KW - 1) + i) * 3 + s3) * H + h) * D + c] : uint16_t(0);
       *reinterpret_cast<uint16_t*>(raw + (s3 * 2 + (c >> 6)) * Lay::RAWH + sw(i, (c & 63) >> 3) + (c & 7) * 2) = hv;
     }
   };
@@ -733,7 +744,7 @@ __global__ void __launch_bounds__(NT, 1)
       for (int cb = 0; cb < D; cb += 32) {
         uint32_t a[32], hv[16];
         if (src) {
-          const float4* s4 = reinterpret_cast<const float4*>(src + state_base + static_cast<int64_t>(v) * D + cb);
+          const float4* s4 = reinterpret_cast<const float4*>(src + in_base + static_cast<int64_t>(v) * D + cb);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const float4 f = s4[q];
@@ -1029,7 +1040,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (o_seg >= 0) return src[(static_cast<int64_t>(start + o_seg) * H + h) * D + c];
       const int r = KW - 1 + o_seg;
       if (r < 0 || hist == nullptr) return 0;
-      return hist[((static_cast<int64_t>(j * (KW - 1) + r) * 3 + s) * H + h) * D + c];
+      return hist[((static_cast<int64_t>(in_idx * (KW - 1) + r) * 3 + s) * H + h) * D + c];
     };
     for (int e = tid; e < (KW - 1) * 3 * D; e += NT) {
       const int i = e / (3 * D), s = (e / D) % 3, c = e % D;

@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(1024) meta_tables_kernel(const int32_t* __rest
     meta[H_TILE] = tile;
     meta[H_STATUS] = status;
     meta[H_VALID] = status ? 0 : 1;
+    meta[H_FOREST] = 0;
   }
   if (status) {
     if (threadIdx.x == 0) {

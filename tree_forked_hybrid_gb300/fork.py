@@ -22,7 +22,10 @@ FORK_STATUS_CHECK = 0x20
 FORK_DETERMINISTIC = 0x1
 FORK_CHECKS = 0x2
 FORK_WARP_MMA = 0x4
+FORK_FOREST = 0x8
 FORK_TEST_STALL = 0x100
+FORK_FOREST_MAX_DEPTH = 7  # ancestors of a forest node, at most (include/forkattn.h)
+FORK_FOREST_MAX_LEVELS = FORK_FOREST_MAX_DEPTH + 1
 FORK_NOALLOC_SCRATCH_BYTES = 32 << 20  # size of the library's scratch array (include/forkattn.h)
 
 _lib = None
@@ -75,6 +78,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fork_gdn_branches": (ctypes.c_int, [MP, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                              u32, vp]),
         "fork_readout": (ctypes.c_int, [MP, vp, i32, vp, vp, vp, u32, vp]),
+        "fork_forest_plan": (ctypes.c_int, [MP, vp, vp, i32, vp, vp]),
+        "fork_build_forest_meta": (ctypes.c_int, [MP, vp, vp, i32, vp, vp, vp]),
+        "fork_gdn_forest": (ctypes.c_int, [MP, i32, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
+                                           u32, vp]),
         "fork_readout_mlp_workspace_bytes": (sz, [i32, i32, i32]),
         "fork_readout_mlp": (ctypes.c_int, [MP, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, u32, vp]),
         "fork_pointwise_rows_workspace_bytes": (sz, [i32, i32, i32]),
@@ -192,6 +199,60 @@ def fork_gdn_branches(meta: Meta, q, k, v, alpha, eta, conv_w, H: int, d: int, K
     _check("fork_gdn_branches", load().fork_gdn_branches(
         meta.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), _ptr(conv_w), H, d, K, chunk,
         _ptr(S_P), _ptr(conv_win), _ptr(o), flags, _stream(stream)))
+
+
+class ForestPlan:
+    """The plan that fork_forest_plan writes next to the metadata image: the levels (first
+    state index of each depth, and the end) and each node's state index."""
+
+    def __init__(self, words, N: int):
+        import numpy as np
+        w = np.asarray(words)
+        self.levels = int(w[0])
+        self.level_first = w[1:2 + self.levels].astype(np.int64)
+        self.state_index = w[2 + FORK_FOREST_MAX_LEVELS:2 + FORK_FOREST_MAX_LEVELS + N].astype(np.int64)
+
+
+def _forest_args(parent, node_len, nbytes: int):
+    import numpy as np
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    ln = np.ascontiguousarray(node_len, dtype=np.int32)
+    img = np.zeros(nbytes // 4, dtype=np.int32)
+    plan = np.zeros(par.shape[0] + 2 + FORK_FOREST_MAX_LEVELS, dtype=np.int32)
+    ptr = lambda a: ctypes.c_void_p(a.ctypes.data)  # noqa: E731
+    return par, ln, img, plan, ptr
+
+
+def fork_forest_plan(T_cap: int, max_req: int, max_q: int, tile_tokens: int, parent, node_len):
+    """Host-only plan of a token forest (no device involved): (metadata image, ForestPlan).
+    The handle passed to the C call describes the capacities; its buffer is the image."""
+    L = load()
+    nbytes = L.fork_meta_bytes(T_cap, max_req, max_q)
+    if nbytes == 0:
+        raise ValueError("invalid metadata capacities")
+    par, ln, img, plan, ptr = _forest_args(parent, node_len, nbytes)
+    h = fork_meta()
+    _check("fork_meta_init", L.fork_meta_init(ctypes.byref(h), ptr(img), nbytes, T_cap, max_req, max_q,
+                                              tile_tokens))
+    _check("fork_forest_plan", L.fork_forest_plan(ctypes.byref(h), ptr(par), ptr(ln), int(par.shape[0]), ptr(img),
+                                                  ptr(plan)))
+    return img, ForestPlan(plan, int(par.shape[0]))
+
+
+def fork_build_forest_meta(meta: Meta, parent, node_len, stream=None) -> ForestPlan:
+    """Plan a token forest on the host and copy its metadata into meta's device buffer."""
+    nbytes = meta.buf.numel() * 4
+    par, ln, img, plan, ptr = _forest_args(parent, node_len, nbytes)
+    _check("fork_build_forest_meta", load().fork_build_forest_meta(
+        meta.ref, ptr(par), ptr(ln), int(par.shape[0]), ptr(img), ptr(plan), _stream(stream)))
+    return ForestPlan(plan, int(par.shape[0]))
+
+
+def fork_gdn_forest(meta: Meta, first: int, count: int, q, k, v, alpha, eta, conv_w, H: int, d: int, K: int,
+                    chunk: int, node_state, node_conv, o, flags: int = 0, stream=None):
+    _check("fork_gdn_forest", load().fork_gdn_forest(
+        meta.ref, first, count, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), _ptr(conv_w), H, d, K, chunk,
+        _ptr(node_state), _ptr(node_conv), _ptr(o), flags, _stream(stream)))
 
 
 def fork_readout(meta: Meta, h, D: int, w_opt, opt_off, p, flags: int = 0, stream=None):

@@ -10,7 +10,7 @@ import numpy as np
 H_WORDS = 32
 MIN_TILE = 8
 HDR = ("magic", "T_cap", "max_req", "max_q", "max_seg", "max_work", "R", "Nq", "T", "nseg", "tile",
-       "n_work", "status", "prefix_total", "valid")
+       "n_work", "status", "prefix_total", "valid", "forest")
 
 
 def _align(w: int) -> int:

@@ -400,3 +400,100 @@ class TreeRunner:
                 li = leaf_index[k]
                 p[t.opt_off[li]:t.opt_off[li + 1]] = pp[lv.round.opt_off[i]:lv.round.opt_off[i + 1]]
         return attn, gdn, p
+
+
+class ForestRound:
+    """A forest of token trees as ONE round of one flat stream (rainbus summary "未来方向"
+    (2): a draft-token tree has the shape of the request tree and runs in the same
+    stream; DFlash-TfM summary "GDN을 위한 롤백 없는 트리 검증": the tree in topological
+    order).  The rows stay where the tree stores them (node after node); the metadata
+    (``fork_build_forest_meta``) gives every node its ancestors' rows and its parent's
+    state index.  Each attention layer is one ``fork_attn`` call (FORK_FOREST): a node's
+    queries read its ancestors' keys in place.  The recurrence runs one
+    ``fork_gdn_forest`` call per depth: a node starts from its parent's end state and
+    conv window (read by index) and leaves its own in ``node_state`` / ``node_conv``
+    at its state index.  The leaves are the readout's questions.  Nothing is copied
+    between nodes."""
+
+    def __init__(self, tree, device="cuda", flags: int = 0, T_cap: Optional[int] = None):
+        self.tree = tree
+        self.device = device
+        self.flags = flags
+        a0 = tree.attn_shapes[0]
+        G = a0.Hq // a0.Hkv
+        for a in tree.attn_shapes:
+            if a.Hq // a.Hkv != G:
+                raise ValueError("attention layers of one forest share the GQA group size")
+        T = int(tree.node_len.sum())
+        self.T = T
+        self.T_cap = T_cap or max(T, 1)
+        n_leaves = len(tree.leaves())
+        self.meta = F.Meta(self.T_cap, tree.N, max(n_leaves, 1), 256 // G, device)
+        self.plan: Optional[F.ForestPlan] = None
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.inputs: Dict[str, Dict[str, torch.Tensor]] = {}
+        for name, lay in tree.layers.items():
+            self.inputs[name] = {}
+            for k, v in lay.items():
+                if k == "conv_w":
+                    self.inputs[name][k] = _f32(v, device)
+                    continue
+                rows = np.zeros((self.T_cap,) + v.shape[1:], dtype=v.dtype)
+                n = min(T, v.shape[0])
+                rows[:n] = v[:n]
+                self.inputs[name][k] = _bf16(rows, device) if v.dtype == np.uint16 else _f32(rows, device)
+        self.attn_out = {a.name: torch.zeros((self.T_cap, a.Hq, a.d), **bf) for a in tree.attn_shapes}
+        self.attn_ws = {}
+        for a in tree.attn_shapes:
+            nb = F.fork_attn_workspace_bytes(self.T_cap, 0, a.Hq, a.Hkv, a.d, a.rope_theta, flags)
+            self.attn_ws[a.name] = torch.empty(max(nb, 16), dtype=torch.uint8, device=device) if nb else None
+        g = tree.gdn_shape
+        self.gdn_out = torch.zeros((self.T_cap, g.H, g.dv), **bf)
+        self.node_state = torch.zeros((tree.N, g.H, g.dv, g.dk), dtype=torch.float32, device=device)
+        self.node_conv = torch.zeros((tree.N, g.K - 1, 3, g.H, g.dk), **bf)
+        D = g.H * g.dv
+        self.w_opt = _bf16(tree.w_opt if tree.w_opt.shape[0] else np.zeros((1, D), np.uint16), device)
+        self.opt_off = torch.from_numpy(tree.opt_off.astype(np.int32)).to(device)
+        self.p = torch.zeros(max(int(tree.opt_off[-1]), 1), dtype=torch.float32, device=device)
+
+    def build_meta(self, stream=None):
+        """Plan the forest on the host and copy its metadata to the device."""
+        self.plan = F.fork_build_forest_meta(self.meta, self.tree.parent, self.tree.node_len, stream)
+
+    def launches_per_run(self) -> int:
+        """Kernels of ``run`` (the metadata is a copy, not a kernel)."""
+        n = sum(4 if a.rope_theta else 2 for a in self.tree.attn_shapes)  # rotary tables + keys, fp16 values, attention
+        return n + self.plan.levels + 1  # one recurrence launch per depth, readout
+
+    def run(self, stream=None, meta: bool = True):
+        """The whole layer; ``meta=False`` reuses the metadata of an earlier run."""
+        t = self.tree
+        if meta or self.plan is None:
+            self.build_meta(stream)
+        for a in t.attn_shapes:
+            inp = self.inputs[a.name]
+            F.fork_attn(self.meta, inp["q"], inp["k"], inp["v"], self.attn_out[a.name], a.Hq, a.Hkv, a.d,
+                        a.window, a.rope_theta, 1.0 / math.sqrt(a.d), None, None, self.attn_ws[a.name],
+                        self.flags | F.FORK_FOREST, stream)
+        g = t.gdn_shape
+        inp = self.inputs[g.name]
+        lf = self.plan.level_first
+        for lv in range(self.plan.levels):
+            F.fork_gdn_forest(self.meta, int(lf[lv]), int(lf[lv + 1] - lf[lv]), inp["q"], inp["k"], inp["v"],
+                              inp["alpha"], inp["eta"], inp["conv_w"], g.H, g.dk, g.K, g.chunk, self.node_state,
+                              self.node_conv, self.gdn_out, self.flags, stream)
+        F.fork_readout(self.meta, self.gdn_out, g.H * g.dv, self.w_opt, self.opt_off, self.p, self.flags, stream)
+
+    def status(self) -> int:
+        return F.fork_read_status(self.meta)
+
+    def outputs(self):
+        """Attention and GDN rows (node after node), the leaves' probabilities and every
+        node's end state in node order (host float32)."""
+        T = self.T
+        attn = {n: o[:T].float().cpu().numpy() for n, o in self.attn_out.items()}
+        gdn = self.gdn_out[:T].float().cpu().numpy()
+        p = self.p[:int(self.tree.opt_off[-1])].cpu().numpy()
+        idx = torch.from_numpy(self.plan.state_index).to(self.device)
+        S_end = self.node_state.index_select(0, idx).cpu().numpy()
+        return attn, gdn, p, S_end

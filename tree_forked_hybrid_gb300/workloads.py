@@ -447,6 +447,25 @@ class TreeRound:
         return out[::-1]
 
 
+def request_forest(n_req: int, level_len, fanout):
+    """Parent and length arrays of n_req identical request trees: a trunk of level_len[0]
+    tokens; every node of depth d < len(fanout) has fanout[d] children of level_len[d + 1]
+    tokens each.  Nodes are listed tree after tree, depth first (parents before children)."""
+    parent, node_len = [], []
+
+    def add(p, d):
+        k = len(parent)
+        parent.append(p)
+        node_len.append(int(level_len[d]))
+        if d < len(fanout):
+            for _ in range(fanout[d]):
+                add(k, d + 1)
+
+    for _ in range(n_req):
+        add(-1, 0)
+    return np.array(parent, np.int32), np.array(node_len, np.int32)
+
+
 def make_tree_round(parent, node_len, *, attn_shapes, gdn_shape, seed=0, n_opt=None) -> TreeRound:
     """A forest with explicit structure; rows, gates, conv and option weights drawn
     as for a round (same draw order: layers, conv weights, option weights)."""
