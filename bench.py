@@ -34,11 +34,9 @@ METRIC = "ForkAttention layer tokens/s per round (attn+GDN) and % of roofline"
 # attention layer on this workload, summed over the call's launches (rotary tables, key
 # rotation, fp16 value copy, attention), from one ncu capture of this bench's command.  Keyed by the
 # SHA-256 of the attention sources: once they change, traffic reads null until re-measured.
-# The bytes below were taken before the token-forest instance was added to the attention
-# sources; not re-measured since, so traffic reads null.
 TRAFFIC = {"sources": ["tree_forked_hybrid_gb300/csrc/fork_attn.cu", "tree_forked_hybrid_gb300/csrc/fork_attn_tc.cu",
                        "tree_forked_hybrid_gb300/csrc/fork_attn.cuh", "tree_forked_hybrid_gb300/csrc/tc_ptx.cuh"],
-           "sha256": None, "bytes": 501914833}
+           "sha256": "dc0b115b6e0d162682b32c5572ded0319d10b7c3050d872c541df3e2976163e6", "bytes": 501405440}
 
 
 def _sources_sha256(paths):
