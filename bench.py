@@ -462,7 +462,7 @@ def main():
             out["graph_replay"] = {"error": f"{type(exc).__name__}: {exc}"}
     if not args.no_forest and ws == 1:
         try:
-            out["forest"] = forest_timing(torch, args, local)
+            out["forest"] = forest_timing(torch, args, local, peaks)
         except Exception as exc:  # reported, never fatal for the main line
             out["forest"] = {"error": f"{type(exc).__name__}: {exc}"}
     if shard is not None:
@@ -580,7 +580,7 @@ def graph_timing(torch, args, local, wid=1):
             "same_probabilities": same}
 
 
-def forest_timing(torch, args, local):
+def forest_timing(torch, args, local, peaks):
     """Request trees that fork twice, run as one round of one flat stream: 2 requests with
     the long-document layer shapes, each a 4096-token trunk with 4 branches of 512 tokens
     and 4 questions of 64 tokens on every branch (42 nodes, 3 depths, 14,336 tokens).
@@ -601,10 +601,22 @@ def forest_timing(torch, args, local):
     if fr.status() != 0:
         raise RuntimeError(f"device status {fr.status():#x}")
     T = int(node_len.sum())
-    return {"workload": "2 request trees: trunk 4096, 4 branches x 512, 4 questions x 64 per branch",
-            "nodes": t.N, "levels": fr.plan.levels, "tokens": T, "round_ms": layers,
-            "round_with_plan_ms": with_plan, "tokens_per_s": T / (layers["median"] / 1e3),
-            "gpu_launches_per_round": fr.launches_per_run()}
+    res = {"workload": "2 request trees: trunk 4096, 4 branches x 512, 4 questions x 64 per branch",
+           "nodes": t.N, "levels": fr.plan.levels, "tokens": T, "round_ms": layers,
+           "round_with_plan_ms": with_plan, "tokens_per_s": T / (layers["median"] / 1e3),
+           "gpu_launches_per_round": fr.launches_per_run()}
+    try:
+        from tree_forked_hybrid_gb300 import roofline as RL
+        work = RL.forest_work(t)
+        t_f = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+        t_b = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        t_roof = max(t_f, t_b)
+        res["layer_roofline"] = {"t_roof_us": t_roof * 1e6, "frac": t_roof / (layers["median"] / 1e3),
+                                 "bound": "tensor" if t_f >= t_b else "hbm", "flops": work["flops"],
+                                 "bytes": work["bytes"]}
+    except Exception as exc:  # the timing above stands without it
+        res["layer_roofline"] = {"error": f"{type(exc).__name__}: {exc}"}
+    return res
 
 
 def attn_kernel_alone(torch, dr, rnd, stream, reps=10):

@@ -57,3 +57,38 @@ def test_attention_and_layer_work_formulas():
     # the slower of the two limits
     assert RL.roofline_time({"flops": 2e12, "bytes": 1e9}, 1000.0, 1000.0) == pytest.approx(2e-3)
     assert RL.roofline_time({"flops": 1e9, "bytes": 3e9}, 1000.0, 1000.0) == pytest.approx(3e-3)
+
+
+FORESTS = [
+    ([-1, 0, 0, 1, 1, 1, 2, 2, 3, 3, -1], [30, 12, 8, 9, 4, 33, 6, 1, 5, 17, 45]),
+    ([-1, 0, 1, 2, 3, 4, 5, 6, 6, 6], [5, 3, 0, 7, 1, 2, 9, 4, 3, 6]),
+    ([-1, 0, -1, 1, 2, 1, 4, 4, 0], [0, 6, 10, 3, 20, 2, 1, 8, 5]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(FORESTS)))
+@pytest.mark.parametrize("window", [0, 5, 13])
+def test_forest_work_counts_the_pairs_of_every_path(case, window):
+    """Visible pairs of a forest counted by brute force: each node's sequence (ancestors'
+    rows, then its own) built from the tree, every query against every key of it."""
+    parent, node_len = FORESTS[case]
+    a = wl.AttnShape("attn", 4, 2, 16, window, 10000.0)
+    t = wl.make_tree_round(parent, node_len, attn_shapes=(a,), gdn_shape=G, seed=case)
+    start = t.node_start
+    brute = 0
+    for k in range(t.N):
+        chain = [k] + t.ancestors(k)[::-1]
+        rows = np.concatenate([np.arange(start[c], start[c] + node_len[c]) for c in chain[::-1]])
+        n = rows.shape[0]
+        for i in range(n - node_len[k], n):
+            brute += sum(1 for y in range(n) if y <= i and (window == 0 or i - y < window))
+    w = RL.forest_work(t)
+    assert w["attn"]["attn"]["flops"] == 4 * a.d * a.Hq * brute
+    T = int(np.sum(node_len))
+    assert w["T"] == T and w["attn"]["attn"]["bytes"] == T * (2 * a.Hq + 2 * a.Hkv) * a.d * 2
+    # states: every node writes its end state; a node with tokens before it reads its parent's
+    pos0 = RL.forest_first_positions(t)
+    assert pos0.tolist() == [sum(node_len[c] for c in t.ancestors(k)) for k in range(t.N)]
+    H, d = G.H, G.dk
+    assert w["gdn"]["bytes"] == T * H * (8 * d + 8) + (t.N + int((pos0 > 0).sum())) * H * d * d * 4
+    assert w["flops"] == w["attn"]["attn"]["flops"] + w["gdn"]["flops"] + w["readout"]["flops"]
