@@ -1,8 +1,9 @@
 """Python binding of the C ABI in include/forkattn.h (argument marshalling only).
 
 Every function here has the name of the C entry point it calls and passes
-device pointers of torch tensors plus the current CUDA stream.  No arithmetic
-of the layer happens here: if the library cannot be loaded, the call fails.
+device pointers of torch tensors plus the current CUDA stream (the token-forest
+planner takes host arrays).  No arithmetic of the layer happens here: if the
+library cannot be loaded, the call fails.
 """
 from __future__ import annotations
 
@@ -10,6 +11,7 @@ import ctypes
 import os
 from typing import Optional
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -206,21 +208,23 @@ class ForestPlan:
     state index of each depth, and the end) and each node's state index."""
 
     def __init__(self, words, N: int):
-        import numpy as np
         w = np.asarray(words)
         self.levels = int(w[0])
         self.level_first = w[1:2 + self.levels].astype(np.int64)
         self.state_index = w[2 + FORK_FOREST_MAX_LEVELS:2 + FORK_FOREST_MAX_LEVELS + N].astype(np.int64)
 
 
-def _forest_args(parent, node_len, nbytes: int):
-    import numpy as np
+def _host_ptr(a: np.ndarray) -> ctypes.c_void_p:
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _forest_arrays(parent, node_len, nbytes: int):
+    """int32 host arrays of a forest call: parents, lengths, the metadata image, the plan."""
     par = np.ascontiguousarray(parent, dtype=np.int32)
     ln = np.ascontiguousarray(node_len, dtype=np.int32)
     img = np.zeros(nbytes // 4, dtype=np.int32)
     plan = np.zeros(par.shape[0] + 2 + FORK_FOREST_MAX_LEVELS, dtype=np.int32)
-    ptr = lambda a: ctypes.c_void_p(a.ctypes.data)  # noqa: E731
-    return par, ln, img, plan, ptr
+    return par, ln, img, plan
 
 
 def fork_forest_plan(T_cap: int, max_req: int, max_q: int, tile_tokens: int, parent, node_len):
@@ -230,21 +234,22 @@ def fork_forest_plan(T_cap: int, max_req: int, max_q: int, tile_tokens: int, par
     nbytes = L.fork_meta_bytes(T_cap, max_req, max_q)
     if nbytes == 0:
         raise ValueError("invalid metadata capacities")
-    par, ln, img, plan, ptr = _forest_args(parent, node_len, nbytes)
+    par, ln, img, plan = _forest_arrays(parent, node_len, nbytes)
     h = fork_meta()
-    _check("fork_meta_init", L.fork_meta_init(ctypes.byref(h), ptr(img), nbytes, T_cap, max_req, max_q,
+    _check("fork_meta_init", L.fork_meta_init(ctypes.byref(h), _host_ptr(img), nbytes, T_cap, max_req, max_q,
                                               tile_tokens))
-    _check("fork_forest_plan", L.fork_forest_plan(ctypes.byref(h), ptr(par), ptr(ln), int(par.shape[0]), ptr(img),
-                                                  ptr(plan)))
+    _check("fork_forest_plan", L.fork_forest_plan(ctypes.byref(h), _host_ptr(par), _host_ptr(ln), int(par.shape[0]),
+                                                  _host_ptr(img), _host_ptr(plan)))
     return img, ForestPlan(plan, int(par.shape[0]))
 
 
 def fork_build_forest_meta(meta: Meta, parent, node_len, stream=None) -> ForestPlan:
     """Plan a token forest on the host and copy its metadata into meta's device buffer."""
     nbytes = meta.buf.numel() * 4
-    par, ln, img, plan, ptr = _forest_args(parent, node_len, nbytes)
+    par, ln, img, plan = _forest_arrays(parent, node_len, nbytes)
     _check("fork_build_forest_meta", load().fork_build_forest_meta(
-        meta.ref, ptr(par), ptr(ln), int(par.shape[0]), ptr(img), ptr(plan), _stream(stream)))
+        meta.ref, _host_ptr(par), _host_ptr(ln), int(par.shape[0]), _host_ptr(img), _host_ptr(plan),
+        _stream(stream)))
     return ForestPlan(plan, int(par.shape[0]))
 
 
