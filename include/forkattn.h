@@ -11,10 +11,12 @@
  * Conventions shared by every entry point
  *   - All pointers named d_* or described as "device" are CUDA device
  *     pointers; the caller allocates and owns every buffer (metadata,
- *     workspace, inputs, outputs).  The library allocates nothing and keeps
- *     no global state between calls, with one exception: fork_attn_noalloc
- *     takes its scratch from a file-scope device array that the library owns
- *     (and caches that array's device address per device).
+ *     workspace, inputs, outputs).  The library allocates no device memory
+ *     and keeps no global state between calls, with one exception:
+ *     fork_attn_noalloc takes its scratch from a file-scope device array that
+ *     the library owns (and caches that array's device address per device).
+ *     The host-side forest planner uses host scratch of its own, freed before
+ *     it returns.
  *   - bf16 tensors are passed as uint16_t bit patterns (bfloat16), row-major
  *     with the layout stated per argument.  Every base pointer must be
  *     16-byte aligned.
