@@ -22,8 +22,9 @@
  *     16-byte aligned.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous and stream-ordered; none synchronises the host except
- *     fork_read_status, so a sequence of calls can be captured in a CUDA
- *     graph.  Grid sizes depend only on the capacities fixed at metadata
+ *     fork_read_status (and fork_build_forest_meta given pageable host memory,
+ *     whose copy waits for the stream), so a sequence of calls can be captured
+ *     in a CUDA graph.  Grid sizes depend only on the capacities fixed at metadata
  *     build time (T_cap, max_req, max_q) and on the shape arguments.
  *   - Return value: FORK_OK or a host-detected error code (nothing is
  *     launched then).  Errors found on the device (an inconsistent
@@ -319,9 +320,10 @@ int fork_gdn_branches(const fork_meta* m, const uint16_t* q, const uint16_t* k, 
 int fork_forest_plan(const fork_meta* m, const int32_t* parent, const int32_t* node_len, int32_t N,
                      int32_t* h_image, int32_t* h_plan);
 
-/* fork_forest_plan, then an asynchronous copy of h_image to m->d_buf on
- * `stream` (h_image is read before the call returns when it is pageable host
- * memory; keep pinned memory unchanged until the copy has completed). */
+/* fork_forest_plan, then a copy of h_image to m->d_buf on `stream`.  From
+ * pageable host memory the copy first waits for the work already on the
+ * stream and has read h_image when the call returns; from pinned memory it is
+ * asynchronous: keep h_image unchanged until the copy has completed. */
 int fork_build_forest_meta(const fork_meta* m, const int32_t* parent, const int32_t* node_len,
                            int32_t N, int32_t* h_image, int32_t* h_plan, void* stream);
 
