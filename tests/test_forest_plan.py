@@ -198,3 +198,23 @@ def test_planner_rejects_bad_forests():
         F.fork_forest_plan(64, 16, 8, 16, deep, [1] * len(deep))
     assert e.value.code == 2
     F.fork_forest_plan(64, 16, 8, 16, deep[:-1], [1] * (len(deep) - 1))  # the deepest allowed
+
+
+def test_planner_equals_hand_derived_tables():
+    """tests/golden/forest_cases.txt: tables worked out by hand from the forest rule."""
+    from tests.golden_io import load_meta_cases
+    cases = load_meta_cases("forest_cases.txt")
+    assert cases
+    for name, c in cases.items():
+        parent, node_len = c["parent"], c["node_len"]
+        N = parent.shape[0]
+        T_cap, tile = int(c["T_cap"][0]), int(c["tile"][0])
+        img, plan = F.fork_forest_plan(T_cap, N, N, tile, parent, node_len)
+        m = LY.unpack(img, T_cap, N, N)
+        assert m["T"] == int(c["T"][0]) and m["forest"] == 1, name
+        assert plan.levels == int(c["levels"][0]), name
+        assert plan.level_first.tolist() == c["level_first"].tolist(), name
+        assert plan.state_index.tolist() == c["state_index"].tolist(), name
+        for key in ("tok_req", "tok_pos", "seg_start", "seg_len", "seg_pos0", "seg_state_idx", "q_last",
+                    "work_seg", "work_off", "work_order"):
+            assert m[key][:c[key].shape[0]].tolist() == c[key].tolist(), (name, key)
