@@ -218,3 +218,23 @@ def test_planner_equals_hand_derived_tables():
         for key in ("tok_req", "tok_pos", "seg_start", "seg_len", "seg_pos0", "seg_state_idx", "q_last",
                     "work_seg", "work_off", "work_order"):
             assert m[key][:c[key].shape[0]].tolist() == c[key].tolist(), (name, key)
+
+
+def test_request_forest_shape():
+    """The bench's forest: identical request trees, depth first, parents before children."""
+    from tree_forked_hybrid_gb300 import workloads as wl
+    parent, node_len = wl.request_forest(2, (4096, 512, 64), (4, 4))
+    assert len(parent) == 2 * (1 + 4 + 16) and int(node_len.sum()) == 2 * (4096 + 4 * 512 + 16 * 64)
+    assert all(-1 <= p < k for k, p in enumerate(parent))
+    roots = [k for k in range(len(parent)) if parent[k] < 0]
+    assert roots == [0, 21]
+    for k in range(len(parent)):
+        kids = [c for c in range(len(parent)) if parent[c] == k]
+        depth = 0
+        a = k
+        while parent[a] >= 0:
+            a, depth = parent[a], depth + 1
+        assert len(kids) == (4 if depth < 2 else 0)
+        assert node_len[k] == (4096, 512, 64)[depth]
+    _, plan, _ = plan_of(parent, node_len, tile=64, T_cap=int(node_len.sum()))
+    assert plan.levels == 3 and plan.level_first.tolist() == [0, 2, 10, 42]
