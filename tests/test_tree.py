@@ -87,10 +87,11 @@ def test_depth_one_tree_is_a_round():
 
 
 def test_chain_is_one_sequence():
-    t = wl.make_tree_round([-1, 0, 1], [6, 9, 5], attn_shapes=(A1,), gdn_shape=G, seed=5)
+    # the window (6 keys) crosses the node boundaries at rows 6 and 15
+    t = wl.make_tree_round([-1, 0, 1], [6, 9, 5], attn_shapes=(A1, A2), gdn_shape=G, seed=5)
     res = tree_oracle(t)
     L = f32_layers(t.layers)
-    for name, a in (("attn", A1),):
+    for name, a in (("attn", A1), ("swa", A2)):
         o = orc.attention_sequence(L[name]["q"][:20], L[name]["k"][:20], L[name]["v"][:20], window=a.window,
                                    rope_theta=a.rope_theta)
         # the tree oracle computes each node's query rows in separate calls: equal up to the
@@ -101,6 +102,11 @@ def test_chain_is_one_sequence():
                                   g["conv_w"])
     assert np.array_equal(res["gdn"], o)
     assert np.array_equal(res["S_end"][2], S)
+    # every node's end state is the sequence's state after that node's last row
+    for k, n in ((0, 6), (1, 15)):
+        _, S_k, _, _ = orc.gdn_sequence(g["q"][:n], g["k"][:n], g["v"][:n], g["alpha"][:n], g["eta"][:n],
+                                        g["conv_w"])
+        assert np.array_equal(res["S_end"][k], S_k), k
 
 
 def test_node_results_do_not_depend_on_other_branches():
